@@ -1,0 +1,237 @@
+/*
+ * ssd_oracle.c -- the CPU oracle for the Mamba-2 SSD forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file: only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark do.  It shares no code, header, table or constant with the CUDA
+ * library; the two meet only through the seeded input generator.
+ *
+ * Everything is plain, single-threaded fp64 C with no blocking, fusion or
+ * reordering beyond what the cited definition states, so that it can be read
+ * against the source by eye.
+ *
+ * Sources (cited by page title and section):
+ *   [P1] "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
+ *        NVIDIA CUDA Tile" (trishampatil.com), sections "The Mamba-2
+ *        Recurrence", "Step 1: Jump the State Across a Chunk with One Matmul",
+ *        "Step 2: Compute a Chunk of Outputs from One State", "Step 3: Add Back
+ *        the Decay, Safely, in Log-Space", "Kernel 1: chunk_cumsum".
+ *   [P2] The zhiding.cn Chinese rendering of the NVIDIA / Jane Street cuTile
+ *        Mamba-2 article, section "Mamba-2架构" (the recurrence and the chunked
+ *        closed forms, given there as LaTeX).
+ *
+ * Layouts (row-major, contiguous; b = batch, t = token, h = head, g = group):
+ *   x    [batch, seqlen, nheads, headdim]      dt   [batch, seqlen, nheads]
+ *   B, C [batch, seqlen, ngroups, dstate]      A, D [nheads]
+ *   init, final [batch, nheads, headdim, dstate]   y [batch, seqlen, nheads, headdim]
+ * The state of one head is held as S[p][n] (headdim x dstate); the pages write
+ * the same matrix as (dstate x headdim), which changes nothing in the math.
+ * Head h reads group h / (nheads / ngroups) of B and C ([P1] "Kernel 2:
+ * fwd_pass_state", the group index used by the kernel body).
+ *
+ * Parity status of each function is recorded in its comment; every function
+ * here is pinned by the CPU tests (tests/test_oracle_pins.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARGS 1
+#define ORACLE_NO_MEMORY 2
+
+static int dims_ok(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                   int64_t dstate, int64_t ngroups) {
+    if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1)
+        return 0;
+    if (nheads % ngroups != 0) return 0;
+    return 1;
+}
+
+/*
+ * ssd_oracle_recurrence -- the plain sequential recurrence, token by token.
+ *
+ * [P2] "Mamba-2架构": h_t = exp(A*dt_t) h_{t-1} + dt_t B_t x_t^T and
+ * y_t = c_t^T h_t + D x_t.  [P1] "The Mamba-2 Recurrence" states the same
+ * (dt_t > 0, A < 0, so exp(A*dt_t) lies in (0, 1]).  The output reads the
+ * state AFTER the token-t update (h_t, not h_{t-1}): the causal mask of the
+ * chunk form keeps the diagonal, which needs h_t.
+ *
+ * Arguments: D may be NULL (treated as 0); init may be NULL (zero state);
+ * final_state may be NULL (not written).  If ckpt is not NULL and
+ * ckpt_every > 0, the state held BEFORE token c*ckpt_every is written to
+ * ckpt[b, h, c] for c = 0 .. ceil(seqlen/ckpt_every)-1 (layout
+ * [batch, nheads, nchunks, headdim, dstate]); these are the chunk-start
+ * states that the chunked method carries between chunks.
+ * Returns 0 on success, nonzero on bad arguments or allocation failure.
+ */
+int ssd_oracle_recurrence(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                          int64_t dstate, int64_t ngroups,
+                          const double* x, const double* dt, const double* A,
+                          const double* B, const double* C, const double* D,
+                          const double* init, double* y, double* final_state,
+                          int64_t ckpt_every, double* ckpt) {
+    if (!dims_ok(batch, seqlen, nheads, headdim, dstate, ngroups)) return ORACLE_BAD_ARGS;
+    if (!x || !dt || !A || !B || !C || !y) return ORACLE_BAD_ARGS;
+    const int64_t P = headdim, N = dstate, H = nheads, G = ngroups, L = seqlen;
+    const int64_t heads_per_group = H / G;
+    const int64_t nchunks = (ckpt && ckpt_every > 0) ? (L + ckpt_every - 1) / ckpt_every : 0;
+    double* S = (double*)malloc((size_t)(P * N) * sizeof(double));
+    if (!S) return ORACLE_NO_MEMORY;
+
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t g = h / heads_per_group;
+            if (init) memcpy(S, init + ((b * H + h) * P) * N, (size_t)(P * N) * sizeof(double));
+            else memset(S, 0, (size_t)(P * N) * sizeof(double));
+
+            for (int64_t t = 0; t < L; ++t) {
+                if (nchunks > 0 && t % ckpt_every == 0) {
+                    double* dst = ckpt + (((b * H + h) * nchunks + t / ckpt_every) * P) * N;
+                    memcpy(dst, S, (size_t)(P * N) * sizeof(double));
+                }
+                const double dtv = dt[(b * L + t) * H + h];
+                const double decay = exp(A[h] * dtv);
+                const double* xt = x + ((b * L + t) * H + h) * P;
+                const double* Bt = B + ((b * L + t) * G + g) * N;
+                const double* Ct = C + ((b * L + t) * G + g) * N;
+                /* h_t = exp(a_t) h_{t-1} + b_t x_t^T with b_t = dt_t B_t */
+                for (int64_t p = 0; p < P; ++p)
+                    for (int64_t n = 0; n < N; ++n)
+                        S[p * N + n] = decay * S[p * N + n] + dtv * Bt[n] * xt[p];
+                /* y_t = c_t^T h_t + D x_t */
+                double* yt = y + ((b * L + t) * H + h) * P;
+                const double Dh = D ? D[h] : 0.0;
+                for (int64_t p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < N; ++n) acc += Ct[n] * S[p * N + n];
+                    yt[p] = acc + Dh * xt[p];
+                }
+            }
+            if (final_state)
+                memcpy(final_state + ((b * H + h) * P) * N, S, (size_t)(P * N) * sizeof(double));
+        }
+    }
+    free(S);
+    return ORACLE_OK;
+}
+
+/*
+ * ssd_oracle_chunk_cumsum -- the per-chunk cumulative decay sums.
+ *
+ * [P1] "Kernel 1: chunk_cumsum": for head h and token t in chunk c,
+ * G[b, h, t] = log2(e) * sum_{k = c*Q .. t} A[h] * dt[b, k, h]: an inclusive
+ * sum that restarts at every chunk start, scaled by log2(e) so that the later
+ * exponentials can be taken base 2 (e^v = 2^(v log2 e)).  The output here is
+ * laid out [batch, nheads, seqlen] (the token-contiguous layout that [P2]
+ * "Mamba-2性能优化" recommends); the pages' kernel stores [batch, seqlen, nheads].
+ * Returns 0 on success.
+ */
+int ssd_oracle_chunk_cumsum(int64_t batch, int64_t seqlen, int64_t nheads, int64_t chunk,
+                            const double* dt, const double* A, double* G) {
+    if (batch < 0 || seqlen < 0 || nheads < 1 || chunk < 1 || !dt || !A || !G)
+        return ORACLE_BAD_ARGS;
+    const double log2e = 1.0 / log(2.0);
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t h = 0; h < nheads; ++h) {
+            double run = 0.0;
+            for (int64_t t = 0; t < seqlen; ++t) {
+                if (t % chunk == 0) run = 0.0;
+                run += A[h] * dt[(b * seqlen + t) * nheads + h];
+                G[(b * nheads + h) * seqlen + t] = log2e * run;
+            }
+        }
+    return ORACLE_OK;
+}
+
+/*
+ * ssd_oracle_chunked -- the chunked closed form, used ONLY to pin the
+ * recurrence above (it is an independent evaluation of the same function).
+ *
+ * [P2] "Mamba-2架构" and [P1] "Step 3: Add Back the Decay, Safely, in
+ * Log-Space": inside a chunk of T tokens with start state h, let g hold the
+ * inclusive cumulative sum of a_t = A*dt_t (natural log space here, no base-2
+ * scaling) and g_last its value at the chunk's last token.  Then
+ *   h_next = exp(g_last) h + (exp(g_last - g) * B)^T X            (jump)
+ *   Y = exp(g) * (C h) + ((exp(g_i - g_j) * (C B^T)) o M) X + D X  (outputs)
+ * with b_j = dt_j B_j (so the dt factor rides on B), M the causal mask that
+ * keeps j <= i.  A ragged last chunk simply has fewer tokens; g_last is the
+ * value at its last real token.  Arguments as ssd_oracle_recurrence, plus the
+ * chunk length Q >= 1.
+ */
+int ssd_oracle_chunked(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                       int64_t dstate, int64_t ngroups, int64_t Q,
+                       const double* x, const double* dt, const double* A,
+                       const double* B, const double* C, const double* D,
+                       const double* init, double* y, double* final_state) {
+    if (!dims_ok(batch, seqlen, nheads, headdim, dstate, ngroups) || Q < 1) return ORACLE_BAD_ARGS;
+    if (!x || !dt || !A || !B || !C || !y) return ORACLE_BAD_ARGS;
+    const int64_t P = headdim, N = dstate, H = nheads, G = ngroups, L = seqlen;
+    const int64_t heads_per_group = H / G;
+    double* S = (double*)malloc((size_t)(P * N) * sizeof(double));
+    double* Snew = (double*)malloc((size_t)(P * N) * sizeof(double));
+    double* g = (double*)malloc((size_t)Q * sizeof(double));
+    if (!S || !Snew || !g) { free(S); free(Snew); free(g); return ORACLE_NO_MEMORY; }
+
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t grp = h / heads_per_group;
+            if (init) memcpy(S, init + ((b * H + h) * P) * N, (size_t)(P * N) * sizeof(double));
+            else memset(S, 0, (size_t)(P * N) * sizeof(double));
+            const double Dh = D ? D[h] : 0.0;
+
+            for (int64_t c0 = 0; c0 < L; c0 += Q) {
+                const int64_t T = (L - c0 < Q) ? (L - c0) : Q;
+                double run = 0.0;
+                for (int64_t i = 0; i < T; ++i) {
+                    run += A[h] * dt[(b * L + c0 + i) * H + h];
+                    g[i] = run;
+                }
+                const double glast = g[T - 1];
+
+                /* outputs of the chunk from the chunk-start state S */
+                for (int64_t i = 0; i < T; ++i) {
+                    const int64_t ti = c0 + i;
+                    const double* Ci = C + ((b * L + ti) * G + grp) * N;
+                    const double* xi = x + ((b * L + ti) * H + h) * P;
+                    double* yi = y + ((b * L + ti) * H + h) * P;
+                    for (int64_t p = 0; p < P; ++p) {
+                        /* exp(g_i) * (C h)_i */
+                        double inter = 0.0;
+                        for (int64_t n = 0; n < N; ++n) inter += Ci[n] * S[p * N + n];
+                        /* sum_{j<=i} exp(g_i - g_j) (C_i . B_j) dt_j x_j */
+                        double intra = 0.0;
+                        for (int64_t j = 0; j <= i; ++j) {
+                            const int64_t tj = c0 + j;
+                            const double* Bj = B + ((b * L + tj) * G + grp) * N;
+                            double cb = 0.0;
+                            for (int64_t n = 0; n < N; ++n) cb += Ci[n] * Bj[n];
+                            intra += exp(g[i] - g[j]) * cb * dt[(b * L + tj) * H + h] *
+                                     x[((b * L + tj) * H + h) * P + p];
+                        }
+                        yi[p] = exp(g[i]) * inter + intra + Dh * xi[p];
+                    }
+                }
+
+                /* jump the state across the chunk */
+                for (int64_t p = 0; p < P; ++p)
+                    for (int64_t n = 0; n < N; ++n) {
+                        double acc = 0.0;
+                        for (int64_t j = 0; j < T; ++j) {
+                            const int64_t tj = c0 + j;
+                            acc += exp(glast - g[j]) * dt[(b * L + tj) * H + h] *
+                                   B[((b * L + tj) * G + grp) * N + n] *
+                                   x[((b * L + tj) * H + h) * P + p];
+                        }
+                        Snew[p * N + n] = exp(glast) * S[p * N + n] + acc;
+                    }
+                memcpy(S, Snew, (size_t)(P * N) * sizeof(double));
+            }
+            if (final_state)
+                memcpy(final_state + ((b * H + h) * P) * N, S, (size_t)(P * N) * sizeof(double));
+        }
+    }
+    free(S); free(Snew); free(g);
+    return ORACLE_OK;
+}
