@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the SSD forward pass (tokens/s and roofline fraction).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one whole forward pass -- chunk_cumsum, fwd_pass_state and
+compute_out -- over one batch of the workload's synthetic inputs, resident in
+HBM.  Each timed step is bracketed by CUDA events on the launching stream and
+preceded by an untimed 256 MiB write that flushes L2.  For N > 1 (torchrun,
+one process per GPU) every rank runs an independent replica on its own batch
+(the (batch, head) slices are independent; there is no exchange step), the
+timed region is bracketed by a barrier and a device synchronize, and the job
+time is the maximum over ranks.
+
+Besides the headline value the JSON line carries:
+  roofline      the dominant kernel's algorithmic HBM bytes per launch over its
+                CUDA-event duration, against the measured copy bandwidth;
+  e2e           the same metric through the public API with pinned host
+                buffers, host<->device copies inside the timed region;
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the workload;
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+``--impl reference`` times the oracle alone (rank 0 only) on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from state_space_sequence_chunk_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "mamba2_layer_bf16"
+METRIC = "SSD fwd tokens/s on 1 GB300 and % of roofline (HBM GB/s / tensor-pipe)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# --- algorithmic byte model (per launch; the method's minimum traffic) -----------
+
+def byte_model(w: synth.Workload) -> dict:
+    """Bytes each kernel must move if it reads its operands once and writes its
+    results once (the three-kernel method; no per-token states, no Q x Q matrix)."""
+    b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk
+    s = 2 if w.dtype == "bf16" else 4
+    nc = -(-L // Q)
+    Lp = nc * Q
+    x = b * L * H * P * s
+    bc = b * L * G * N * s
+    dt = b * L * H * 4
+    gcs = b * H * Lp * 4
+    hid = b * H * nc * P * N * s
+    st = b * H * P * N * 4
+    init = st if w.init_std > 0 else 0
+    D = H * 4 if w.with_D else 0
+    return {
+        "chunk_cumsum": dt + H * 4 + 2 * gcs,                    # dt, A -> Gcs, dtT
+        "fwd_pass_state": x + bc + 2 * gcs + init + hid + st,    # x, B, Gcs, dtT, init -> hiddens, final
+        "compute_out": x + 2 * bc + 2 * gcs + hid + D + x,       # x, B, C, Gcs, dtT, hiddens, D -> y
+    }
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dram_traffic_record():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by kernel,
+    with the source digest they were taken at."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    rec = {}
+    if os.path.exists(p):
+        for line in open(p):
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#"):
+                rec[(parts[0], parts[1])] = (float(parts[2]), parts[3])
+    return rec
+
+
+def source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "state_space_sequence_chunk_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# --- clocks ----------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --- CPU oracle baseline ---------------------------------------------------------
+
+def cpu_baseline(w: synth.Workload, inp: dict, target_s: float) -> dict:
+    """The fp64 oracle, single-threaded, on whole-sequence (batch, head) slices
+    of the workload; projected to the full workload's tokens/s."""
+    import oracle
+    lib = oracle.load()
+    H, G = w.nheads, w.ngroups
+    pairs = [(b, h) for b in range(w.batch) for h in range(H)]
+    rng = np.random.default_rng(0)
+    order = rng.permutation(len(pairs))
+
+    def run(bh):
+        b, h = bh
+        g = h // (H // G)
+        oracle.recurrence(
+            inp["x"][b:b + 1, :, h:h + 1], inp["dt"][b:b + 1, :, h:h + 1], inp["A"][h:h + 1],
+            inp["B"][b:b + 1, :, g:g + 1], inp["C"][b:b + 1, :, g:g + 1],
+            None if inp["D"] is None else inp["D"][h:h + 1],
+            None if inp["init_state"] is None else inp["init_state"][b:b + 1, h:h + 1], lib=lib)
+
+    done, t_total = 0, 0.0
+    while done < len(pairs) and t_total < target_s:
+        t0 = time.perf_counter()
+        run(pairs[order[done]])
+        t_total += time.perf_counter() - t0
+        done += 1
+    per_slice = t_total / done
+    full_s = per_slice * len(pairs)
+    return {"value": w.tokens / full_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {len(pairs)} (batch, head) slices, full {w.seqlen}-token "
+                      f"sequences, fp64, single thread; {t_total:.1f} s measured, "
+                      f"projected {full_s:.1f} s for the whole workload"}
+
+
+def reference_arm(args, w: synth.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = synth.make_inputs(w)
+    import oracle
+    lib = oracle.load()
+    H, G = w.nheads, w.ngroups
+    pairs = [(b, h) for b in range(w.batch) for h in range(H)]
+
+    def step(i):
+        b, h = pairs[i % len(pairs)]
+        g = h // (H // G)
+        # bounded sample of the workload: one (batch, head) slice, first 512 tokens
+        T = min(w.seqlen, 512)
+        oracle.recurrence(
+            inp["x"][b:b + 1, :T, h:h + 1], inp["dt"][b:b + 1, :T, h:h + 1], inp["A"][h:h + 1],
+            inp["B"][b:b + 1, :T, g:g + 1], inp["C"][b:b + 1, :T, g:g + 1],
+            None if inp["D"] is None else inp["D"][h:h + 1],
+            None if inp["init_state"] is None else inp["init_state"][b:b + 1, h:h + 1], lib=lib)
+        return T
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    toks = 0
+    for i in range(args.steps):
+        toks += step(args.warmup + i)
+    el = time.perf_counter() - t0
+    # tokens of the full workload per second: one slice-token is 1/(H) of a token
+    value = toks / el / H
+    ms_per_step = w.tokens / value * 1e3
+    sample = (f"each step: one (batch, head) slice x {min(w.seqlen, 512)} tokens of the "
+              f"workload, fp64 oracle, single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w: synth.Workload) -> dict:
+    return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+            "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk,
+            "io_dtype": w.dtype, "state_dtype": "f32",
+            "l2": "flushed before every timed step (256 MiB write)"}
+
+
+# --- GPU arm ---------------------------------------------------------------------
+
+def main():
+    args = parse()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+
+    import ctypes
+    import torch
+    import torch.distributed as dist
+
+    import state_space_sequence_chunk_gb300 as ssd
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    lib = ssd.load_library()
+    inp = synth.make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def up(a, dtype=None):
+        if a is None:
+            return None
+        t = torch.from_numpy(a).to(dev)
+        return t.to(dtype) if dtype is not None else t
+
+    x, B, C = up(inp["x"], tdt), up(inp["B"], tdt), up(inp["C"], tdt)
+    dt, A, D, init = up(inp["dt"]), up(inp["A"]), up(inp["D"]), up(inp["init_state"])
+    y = torch.empty_like(x)
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=dev)
+    dims = ssd.dims_for(x, B, w.chunk)
+    ws_bytes = ssd.ssd_fwd_workspace_bytes(dims)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        ssd.ssd_fwd(x, dt, A, B, C, D, init, chunk_size=w.chunk, workspace=ws, out=y,
+                    final_out=fin)
+
+    def sync_all():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        fwd()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+
+    # headline: K whole steps, each timed with events, L2 flushed in between
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sync_all()
+    for s0, s1 in evs:
+        flush.fill_(1)
+        s0.record(stream)
+        fwd()
+        s1.record(stream)
+    sync_all()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.tokens / (ms_per_step * 1e-3)
+
+    # per-kernel breakdown through the three step entry points (same launches)
+    gb, hb = ssd.ssd_intermediate_bytes(dims)
+    gcs = ws[:gb].view(torch.float32)
+    off = (gb + 255) // 256 * 256
+    dtT = ws[off:off + gb].view(torch.float32)
+    hid = ws[2 * off:2 * off + hb]
+    P = ctypes.c_void_p
+    ptr = lambda t: None if t is None else P(t.data_ptr())
+    st = P(stream.cuda_stream)
+    kern = {"chunk_cumsum": lambda: lib.ssd_chunk_cumsum(ctypes.byref(dims), ptr(dt), ptr(A),
+                                                         ptr(gcs), ptr(dtT), st),
+            "fwd_pass_state": lambda: lib.ssd_fwd_pass_state(ctypes.byref(dims), ptr(x), ptr(B),
+                                                             ptr(gcs), ptr(dtT), ptr(init),
+                                                             ptr(hid), ptr(fin), st),
+            "compute_out": lambda: lib.ssd_compute_out(ctypes.byref(dims), ptr(x), ptr(B),
+                                                       ptr(C), ptr(gcs), ptr(dtT), ptr(hid),
+                                                       ptr(D), ptr(y), st)}
+    per = {k: [] for k in kern}
+    nrep = max(10, min(args.steps, 50))
+    for _ in range(nrep):
+        for k, f in kern.items():
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = f()
+            e1.record(stream)
+            if rc != 0:
+                raise RuntimeError(f"{k} returned {rc}")
+            per[k].append((e0, e1))
+    torch.cuda.synchronize()
+    kms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in per.items()}
+
+    # e2e through the public API with pinned host buffers
+    host = {k: (None if v is None else torch.from_numpy(v).to(tdt if k in ("x", "B", "C") else
+                                                          torch.float32).pin_memory())
+            for k, v in inp.items()}
+    y_h = torch.empty(y.shape, dtype=tdt).pin_memory()
+    f_h = torch.empty(fin.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = y_h.numel() * y_h.element_size() + f_h.numel() * f_h.element_size()
+    dev_in = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                dev_in[k].copy_(v, non_blocking=True)
+        ssd.ssd_fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"],
+                    dev_in["D"], dev_in["init_state"], chunk_size=w.chunk, workspace=ws, out=y,
+                    final_out=fin)
+        y_h.copy_(y, non_blocking=True)
+        f_h.copy_(fin, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_n = max(5, min(args.steps, 20))
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(e2e_n)]
+    sync_all()
+    for s0, s1 in eev:
+        flush.fill_(1)
+        s0.record(stream)
+        e2e_step()
+        s1.record(stream)
+    sync_all()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    clocks = sampler.stop()
+
+    if rank == 0:
+        model = byte_model(w)
+        dom = max(kms, key=kms.get)
+        peak, peak_kind = measured_peaks()
+        achieved = model[dom] / (kms[dom] * 1e-3) / 1e9
+        traffic = None
+        rec = dram_traffic_record().get((dom, w.name))
+        if rec is not None and rec[1] == source_digest():
+            traffic = rec[0]
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": config_of(w),
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "algorithmic_bytes": model[dom]},
+            "kernels_ms": kms,
+            "method_roofline_frac": sum(model.values()) / (ms_per_step * 1e-3) / 1e9 / peak,
+            "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked-scan forward pass.
+ *
+ * The method: "Accelerating Mamba-2 with High-Performance Forward Pass Kernels
+ * in NVIDIA CUDA Tile" (trishampatil.com), sections "The Mamba-2 Recurrence"
+ * through "Kernel 3: compute_out"; the formulas are printed in full in the
+ * zhiding.cn rendering of the same NVIDIA / Jane Street article, section
+ * "Mamba-2架构".  Per head, with decay a_t = A*dt_t < 0:
+ *
+ *     h_t = exp(a_t) h_{t-1} + dt_t B_t x_t^T          y_t = C_t^T h_t + D x_t
+ *
+ * evaluated chunk by chunk: chunk_cumsum (in-chunk log-space decay sums G),
+ * fwd_pass_state (the state at every chunk start, carried with the jump
+ * h <- exp(G_last) h + (exp(G_last - G) o B)^T X) and compute_out
+ * (Y = exp(G) o (C h) + ((exp(G_i - G_j) o C B^T) o M)(dt o X) + D X).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers (the current CUDA device), to
+ *    contiguous row-major arrays in the layouts given below, 16-byte aligned.
+ *    The caller owns every buffer; the library allocates no device memory and
+ *    keeps no per-call state.  Inputs are only read.
+ *  - Letters: b = batch, L = seqlen, H = nheads, P = headdim, N = dstate,
+ *    G = ngroups (H % G == 0; head h reads group h / (H/G) of B and C),
+ *    Q = chunk_size, nc = ceil(L / Q), Lp = nc * Q.
+ *  - Layouts:  x, y [b, L, H, P] (dims.dtype)      dt [b, L, H] (fp32)
+ *              B, C [b, L, G, N] (dims.dtype)      A, D [H] (fp32)
+ *              init_state, final_state [b, H, P, N] (fp32)
+ *    Intermediates (chunk_cumsum / fwd_pass_state outputs):
+ *              Gcs, dtT [b, H, Lp] (fp32; token-contiguous, padded to Lp;
+ *                  Gcs is pre-scaled by log2(e); padded tokens carry dt = 0)
+ *              hiddens [b, H, nc, P, N] (dims.dtype): the state before each
+ *                  chunk's first token.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream: no host synchronisation inside.
+ *  - Errors: all arguments are validated on the host BEFORE anything is
+ *    enqueued; on an error the call returns a status != SSD_OK and launches
+ *    nothing.  A failure reported by the CUDA runtime while enqueuing returns
+ *    SSD_ERR_CUDA.  Nothing throws across this ABI.
+ *  - Supported sizes: dtype SSD_F32 or SSD_BF16 (x, B, C, y share it);
+ *    Q in {64, 128, 256}; P in {16, 32, ..., 128} (multiple of 16);
+ *    N in {16, 32, ..., 256} (multiple of 16); H % G == 0; batch >= 0 and
+ *    seqlen >= 0 (an empty problem enqueues at most a copy of init_state to
+ *    final_state).  The device must be compute capability 10.3.
+ */
+#ifndef SSD_GB300_SSD_H
+#define SSD_GB300_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_ABI_VERSION 1
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_NULL = 1,       /* a required pointer is NULL                         */
+    SSD_ERR_SHAPE = 2,      /* unsupported or inconsistent sizes                  */
+    SSD_ERR_DTYPE = 3,      /* unknown dtype code                                 */
+    SSD_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned                   */
+    SSD_ERR_WORKSPACE = 5,  /* workspace smaller than ssd_fwd_workspace_bytes()   */
+    SSD_ERR_ARCH = 6,       /* the current device is not compute capability 10.3  */
+    SSD_ERR_CUDA = 7,       /* the CUDA runtime reported an error                 */
+    SSD_ERR_ALIAS = 8       /* an output overlaps an input                        */
+} ssd_status;
+
+/* Problem sizes.  `dtype` is an ssd_dtype: the element type of x, B, C, y and
+ * of the hiddens intermediate.  `reserved` must be 0. */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size;
+    int32_t dtype;
+    int32_t reserved;
+} ssd_dims;
+
+/* Version of this ABI (SSD_ABI_VERSION of the library that was built). */
+int ssd_abi_version(void);
+
+/* Static English text for a status code; never NULL. */
+const char* ssd_status_string(ssd_status s);
+
+/* Bytes of device workspace that ssd_fwd needs for `d` (the Gcs, dtT and
+ * hiddens intermediates, each 256-byte aligned); 0 if `d` is invalid or empty. */
+size_t ssd_fwd_workspace_bytes(const ssd_dims* d);
+
+/* Byte sizes of the two intermediate kinds: Gcs (== dtT) and hiddens.  Returns
+ * SSD_OK, or an error for invalid `d` (outputs then untouched). */
+ssd_status ssd_intermediate_bytes(const ssd_dims* d, size_t* gcs_bytes, size_t* hiddens_bytes);
+
+/*
+ * ssd_fwd -- the whole forward pass: chunk_cumsum, fwd_pass_state and
+ * compute_out, in that order, on `stream`.
+ *   x, dt, A, B, C      inputs (required).
+ *   D                   per-head skip weight [H], or NULL for D = 0.
+ *   init_state          [b, H, P, N] fp32, or NULL for a zero initial state.
+ *   y                   output [b, L, H, P] (required).
+ *   final_state         output [b, H, P, N] fp32, or NULL to skip.  It may be
+ *                       the same pointer as init_state (in-place update: each
+ *                       state slice is read before it is written); any other
+ *                       overlap with an input is SSD_ERR_ALIAS.
+ *   workspace           device scratch of >= ssd_fwd_workspace_bytes(d) bytes,
+ *                       owned by the caller; its contents on entry do not
+ *                       matter and on exit hold Gcs, dtT and hiddens.
+ */
+ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const float* A,
+                   const void* B, const void* C, const float* D, const float* init_state,
+                   void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
+ * ssd_chunk_cumsum -- step 1 ("Kernel 1: chunk_cumsum").
+ *   Gcs[b, h, t] = log2(e) * sum_{k = chunk start .. t} A[h] * dt[b, k, h]
+ *   dtT[b, h, t] = dt[b, t, h]
+ * for t < L; for L <= t < Lp both treat dt as 0 (so Gcs holds the value at the
+ * last real token and dtT holds 0).  Gcs and dtT: [b, H, Lp] fp32.
+ */
+ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A,
+                            float* Gcs, float* dtT, void* stream);
+
+/*
+ * ssd_fwd_pass_state -- step 2 ("Kernel 2: fwd_pass_state").
+ * For every (b, h), walking the chunks in order from S = init_state (or 0):
+ *   hiddens[b, h, c] = S                                  (in dims.dtype)
+ *   S <- 2^{g_last} S + X_c^T (B_c o (dt_c 2^{g_last - g_c}))
+ * where g = Gcs of chunk c and g_last its value at the chunk's last real token.
+ * final_state (fp32, may be NULL, may equal init_state) receives the last S.
+ */
+ssd_status ssd_fwd_pass_state(const ssd_dims* d, const void* x, const void* B,
+                              const float* Gcs, const float* dtT, const float* init_state,
+                              void* hiddens, float* final_state, void* stream);
+
+/*
+ * ssd_compute_out -- step 3 ("Kernel 3: compute_out").  For every (b, chunk, h):
+ *   Y = 2^{g} o (C h^T) + ((2^{g_i - g_j} [i >= j]) o (C B^T)) (dt o X) + D X
+ * with h = hiddens[b, h, c]; the Q x Q matrix never leaves the chip.  D may be
+ * NULL (D = 0).  y [b, L, H, P] in dims.dtype.
+ */
+ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, const void* C,
+                           const float* Gcs, const float* dtT, const void* hiddens,
+                           const float* D, void* y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_SSD_H */

@@ -1,1 +1,193 @@
-"""GB300-native Mamba-2 SSD chunked-scan forward pass."""
+"""GB300-native (sm_103a) Mamba-2 SSD chunked-scan forward pass.
+
+A thin ctypes binding over the C ABI in ``include/ssd.h`` (``_lib/libssd.so``,
+built in-tree by :mod:`state_space_sequence_chunk_gb300.build`).  The Python
+side only marshals arguments: it allocates outputs and workspace with torch,
+passes raw device pointers and torch's current CUDA stream, and turns status
+codes into exceptions.  Every step of the computation runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback -- if the library is missing,
+the calls raise.
+
+Entry points (same names as the C ABI):
+
+* :func:`ssd_fwd` -- the whole forward pass, ``(y, final_state)``.
+* :func:`ssd_chunk_cumsum`, :func:`ssd_fwd_pass_state`,
+  :func:`ssd_compute_out` -- the three steps one at a time.
+* :func:`ssd_fwd_workspace_bytes`, :func:`ssd_intermediate_bytes`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libssd.so")
+
+SSD_F32, SSD_BF16 = 0, 1
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE",
+          4: "SSD_ERR_ALIGN", 5: "SSD_ERR_WORKSPACE", 6: "SSD_ERR_ARCH", 7: "SSD_ERR_CUDA",
+          8: "SSD_ERR_ALIAS"}
+EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
+           "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
+           "ssd_compute_out"]
+
+
+class SSDError(RuntimeError):
+    """A non-OK status returned by the library."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS.get(code, code)}: {message}")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("chunk_size", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libssd.so (cached).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not found at {path}; build it with "
+                "`python -m state_space_sequence_chunk_gb300.build` (or __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        vp, dp = ctypes.c_void_p, ctypes.POINTER(Dims)
+        sz = ctypes.c_size_t
+        lib.ssd_abi_version.argtypes, lib.ssd_abi_version.restype = [], ctypes.c_int
+        lib.ssd_status_string.argtypes, lib.ssd_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+        lib.ssd_fwd_workspace_bytes.argtypes, lib.ssd_fwd_workspace_bytes.restype = [dp], sz
+        lib.ssd_intermediate_bytes.argtypes = [dp, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        lib.ssd_intermediate_bytes.restype = ctypes.c_int
+        lib.ssd_fwd.argtypes = [dp] + [vp] * 10 + [sz, vp]
+        lib.ssd_fwd.restype = ctypes.c_int
+        lib.ssd_chunk_cumsum.argtypes = [dp] + [vp] * 5
+        lib.ssd_chunk_cumsum.restype = ctypes.c_int
+        lib.ssd_fwd_pass_state.argtypes = [dp] + [vp] * 8
+        lib.ssd_fwd_pass_state.restype = ctypes.c_int
+        lib.ssd_compute_out.argtypes = [dp] + [vp] * 9
+        lib.ssd_compute_out.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(code: int):
+    if code != 0:
+        msg = load_library().ssd_status_string(code).decode()
+        raise SSDError(code, msg)
+
+
+def dims_for(x: torch.Tensor, B: torch.Tensor, chunk_size: int) -> Dims:
+    """ssd_dims for x [b, L, H, P] and B [b, L, G, N]."""
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [b, L, H, P] and B [b, L, G, N]")
+    if x.dtype == torch.bfloat16:
+        dt_code = SSD_BF16
+    elif x.dtype == torch.float32:
+        dt_code = SSD_F32
+    else:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    return Dims(b, L, H, P, N, G, int(chunk_size), dt_code, 0)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def ssd_fwd_workspace_bytes(dims: Dims) -> int:
+    return int(load_library().ssd_fwd_workspace_bytes(ctypes.byref(dims)))
+
+
+def ssd_intermediate_bytes(dims: Dims):
+    g, h = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().ssd_intermediate_bytes(ctypes.byref(dims), ctypes.byref(g), ctypes.byref(h)))
+    return g.value, h.value
+
+
+def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_size: int = 256,
+            return_final_state: bool = True, workspace=None, out=None, final_out=None):
+    """The whole SSD forward pass on x's device and torch's current stream.
+
+    x [b, L, H, P] and B, C [b, L, G, N] share one dtype (float32 or bfloat16);
+    dt [b, L, H], A [H], D [H], init_state [b, H, P, N] are float32.
+    Returns ``(y, final_state)`` (final_state None unless requested).
+    ``workspace`` (uint8 CUDA tensor), ``out`` and ``final_out`` may be given
+    to reuse buffers.
+    """
+    lib = load_library()
+    dims = dims_for(x, B, chunk_size)
+    y = out if out is not None else torch.empty_like(x)
+    fin = None
+    if return_final_state:
+        fin = final_out if final_out is not None else torch.empty(
+            (x.shape[0], x.shape[2], x.shape[3], B.shape[3]), dtype=torch.float32, device=x.device)
+    nbytes = int(lib.ssd_fwd_workspace_bytes(ctypes.byref(dims)))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    _check(lib.ssd_fwd(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                       _ptr(init_state), _ptr(y), _ptr(fin), _ptr(workspace),
+                       ctypes.c_size_t(workspace.numel()), _stream()))
+    return y, fin
+
+
+def ssd_chunk_cumsum(dt, A, chunk_size: int, x_dtype=torch.bfloat16):
+    """Step 1: returns ``(Gcs, dtT)``, both [b, H, Lp] float32."""
+    lib = load_library()
+    b, L, H = dt.shape
+    dims = Dims(b, L, H, 16, 16, 1, int(chunk_size),
+                SSD_BF16 if x_dtype == torch.bfloat16 else SSD_F32, 0)
+    nc = (L + chunk_size - 1) // chunk_size
+    Gcs = torch.empty((b, H, nc * chunk_size), dtype=torch.float32, device=dt.device)
+    dtT = torch.empty_like(Gcs)
+    _check(lib.ssd_chunk_cumsum(ctypes.byref(dims), _ptr(dt), _ptr(A), _ptr(Gcs), _ptr(dtT),
+                                _stream()))
+    return Gcs, dtT
+
+
+def ssd_fwd_pass_state(x, B, Gcs, dtT, init_state=None, chunk_size: int = 256,
+                       return_final_state: bool = True):
+    """Step 2: returns ``(hiddens [b, H, nc, P, N] in x.dtype, final_state)``."""
+    lib = load_library()
+    dims = dims_for(x, B, chunk_size)
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    nc = (L + chunk_size - 1) // chunk_size
+    hid = torch.empty((b, H, nc, P, N), dtype=x.dtype, device=x.device)
+    fin = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device) if return_final_state else None
+    _check(lib.ssd_fwd_pass_state(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(Gcs), _ptr(dtT),
+                                  _ptr(init_state), _ptr(hid), _ptr(fin), _stream()))
+    return hid, fin
+
+
+def ssd_compute_out(x, B, C, Gcs, dtT, hiddens, D=None, chunk_size: int = 256):
+    """Step 3: returns y [b, L, H, P] in x.dtype."""
+    lib = load_library()
+    dims = dims_for(x, B, chunk_size)
+    y = torch.empty_like(x)
+    _check(lib.ssd_compute_out(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(C), _ptr(Gcs), _ptr(dtT),
+                               _ptr(hiddens), _ptr(D), _ptr(y), _stream()))
+    return y

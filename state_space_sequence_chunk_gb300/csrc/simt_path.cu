@@ -1,0 +1,264 @@
+// simt_path.cu -- fwd_pass_state and compute_out on the CUDA cores (fp32 FMA).
+//
+// These are the straightforward tiled forms of steps 2 and 3 of "Accelerating
+// Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA CUDA Tile"
+// (sections "Kernel 2: fwd_pass_state" and "Kernel 3: compute_out"), with all
+// arithmetic in fp32.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+
+// ---------------------------------------------------------------------------
+// fwd_pass_state: one CTA per (16 rows of P, batch*head).  Thread t owns row
+// p = t / 16 of the tile and state columns n = t % 16 + 16 k.  Chunks are walked
+// in order; each chunk is consumed in sub-chunks of 32 tokens staged in shared
+// memory.  Per chunk: store S as the chunk's start state, then
+//   S <- 2^{g_last} S + sum_q x[q][p] * (dt_q 2^{g_last - g_q}) * B[q][n].
+// ---------------------------------------------------------------------------
+constexpr int kPT = 16;    // rows of P per CTA
+constexpr int kSub = 32;   // tokens per staged sub-chunk
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+fwd_pass_state_simt(const T* __restrict__ x, const T* __restrict__ B,
+                    const float* __restrict__ Gcs, const float* __restrict__ dtT,
+                    const float* init, T* __restrict__ hiddens, float* final_state,
+                    int L, int H, int P, int N, int G, int Q, int nc, int Lp, int hpg) {
+    extern __shared__ float sm[];
+    float* xs = sm;                    // [kSub][kPT]
+    float* bs = xs + kSub * kPT;       // [kSub][N]
+    float* sc = bs + kSub * N;         // [kSub] per-token scale
+
+    const int p0 = blockIdx.x * kPT;
+    const int bh = blockIdx.y, bidx = bh / H, h = bh % H, grp = h / hpg;
+    const int tid = threadIdx.x, pl = tid / 16, nl = tid % 16;
+    const int p = p0 + pl;
+    const int nper = N / 16;
+
+    float S[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        S[k] = 0.f;
+        if (k < nper && init) S[k] = init[(((int64_t)bidx * H + h) * P + p) * N + nl + 16 * k];
+    }
+    const float* grow = Gcs + (int64_t)bh * Lp;
+    const float* drow = dtT + (int64_t)bh * Lp;
+
+    for (int c = 0; c < nc; ++c) {
+        // chunk-start state
+        T* hrow = hiddens + ((((int64_t)bidx * H + h) * nc + c) * P + p) * N;
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            if (k < nper) hrow[nl + 16 * k] = from_f32<T>(S[k]);
+
+        const int t0 = c * Q;
+        const float glast = grow[t0 + Q - 1];  // padded tokens repeat the last real value
+        float acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+
+        for (int s0 = 0; s0 < Q; s0 += kSub) {
+            __syncthreads();
+            for (int i = tid; i < kSub * kPT; i += kThreads) {
+                const int q = i / kPT, pp = i % kPT, tg = t0 + s0 + q;
+                xs[i] = tg < L ? to_f32(x[(((int64_t)bidx * L + tg) * H + h) * P + p0 + pp]) : 0.f;
+            }
+            for (int i = tid; i < kSub * N; i += kThreads) {
+                const int q = i / N, n = i % N, tg = t0 + s0 + q;
+                bs[i] = tg < L ? to_f32(B[(((int64_t)bidx * L + tg) * G + grp) * N + n]) : 0.f;
+            }
+            if (tid < kSub) {
+                const int tq = t0 + s0 + tid;
+                sc[tid] = drow[tq] * exp2f(glast - grow[tq]);
+            }
+            __syncthreads();
+            for (int q = 0; q < kSub; ++q) {
+                const float xv = xs[q * kPT + pl] * sc[q];
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    if (k < nper) acc[k] = fmaf(xv, bs[q * N + nl + 16 * k], acc[k]);
+            }
+        }
+        const float e = exp2f(glast);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) S[k] = fmaf(e, S[k], acc[k]);
+    }
+    if (final_state) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            if (k < nper) final_state[(((int64_t)bidx * H + h) * P + p) * N + nl + 16 * k] = S[k];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// compute_out: one CTA per (32 query rows, chunk, batch*head).  Thread t owns
+// row i = t / 8 and columns p = t % 8 + 8 k.
+//   acc = 2^{g_i} (C_i . h^T)
+//   for each 32-token key block j <= i:
+//       cb[i][j] = C_i . B_j, masked to j <= i and scaled by 2^{g_i - g_j} dt_j
+//       acc += cb . X_j
+//   y = acc + D x_i
+// The mask is a select, so the unsafe above-diagonal exponentials never reach
+// the output ("Kernel 3: compute_out").
+// ---------------------------------------------------------------------------
+constexpr int kRows = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __restrict__ C,
+                 const float* __restrict__ Gcs, const float* __restrict__ dtT,
+                 const T* __restrict__ hiddens, const float* __restrict__ D, T* __restrict__ y,
+                 int L, int H, int P, int N, int G, int Q, int nc, int Lp, int hpg) {
+    extern __shared__ float sm[];
+    const int NS = N + 1;              // padded row stride
+    float* cs = sm;                    // [kRows][NS]   query rows of C
+    float* bs = cs + kRows * NS;       // [kRows][NS]   key rows of B
+    float* hs = bs + kRows * NS;       // [P][33]       32-column slice of h
+    float* xs = hs + P * 33;           // [kRows][P]    key rows of X
+    float* cb = xs + kRows * P;        // [kRows][33]
+    float* gq = cb + kRows * 33;       // [Q]
+    float* dq = gq + Q;                // [Q]
+
+    const int i0 = blockIdx.x * kRows, c = blockIdx.y, bh = blockIdx.z;
+    const int bidx = bh / H, h = bh % H, grp = h / hpg;
+    const int tid = threadIdx.x, il = tid / 8, pl = tid % 8;
+    const int pper = P / 8;
+    const int t0 = c * Q;
+
+    for (int i = tid; i < Q; i += kThreads) {
+        gq[i] = Gcs[(int64_t)bh * Lp + t0 + i];
+        dq[i] = dtT[(int64_t)bh * Lp + t0 + i];
+    }
+    for (int i = tid; i < kRows * N; i += kThreads) {
+        const int r = i / N, n = i % N, tg = t0 + i0 + r;
+        cs[r * NS + n] = tg < L ? to_f32(C[(((int64_t)bidx * L + tg) * G + grp) * N + n]) : 0.f;
+    }
+
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+
+    // state term C_i . h^T, h staged 32 state columns at a time
+    const T* hbase = hiddens + (((int64_t)bidx * H + h) * nc + c) * (int64_t)P * N;
+    for (int n0 = 0; n0 < N; n0 += 32) {
+        __syncthreads();
+        for (int i = tid; i < P * 32; i += kThreads) {
+            const int pp = i / 32, nn = i % 32;
+            hs[pp * 33 + nn] = (n0 + nn < N) ? to_f32(hbase[(int64_t)pp * N + n0 + nn]) : 0.f;
+        }
+        __syncthreads();
+        const int nlim = min(32, N - n0);
+        for (int nn = 0; nn < nlim; ++nn) {
+            const float cv = cs[il * NS + n0 + nn];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (k < pper) acc[k] = fmaf(cv, hs[(pl + 8 * k) * 33 + nn], acc[k]);
+        }
+    }
+    const int irow = i0 + il;
+    {
+        const float sgi = exp2f(gq[irow]);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] *= sgi;
+    }
+
+    // intra-chunk term, key blocks j0 <= i0
+    for (int j0 = 0; j0 <= i0; j0 += kRows) {
+        __syncthreads();
+        for (int i = tid; i < kRows * N; i += kThreads) {
+            const int r = i / N, n = i % N, tg = t0 + j0 + r;
+            bs[r * NS + n] = tg < L ? to_f32(B[(((int64_t)bidx * L + tg) * G + grp) * N + n]) : 0.f;
+        }
+        for (int i = tid; i < kRows * P; i += kThreads) {
+            const int r = i / P, pp = i % P, tg = t0 + j0 + r;
+            xs[i] = tg < L ? to_f32(x[(((int64_t)bidx * L + tg) * H + h) * P + pp]) : 0.f;
+        }
+        __syncthreads();
+        // 32 x 32 block of C B^T: thread -> row il, columns pl + 8 k (k < 4)
+        for (int k = 0; k < 4; ++k) {
+            const int jl = pl + 8 * k;
+            float s = 0.f;
+            for (int n = 0; n < N; ++n) s = fmaf(cs[il * NS + n], bs[jl * NS + n], s);
+            const int ig = i0 + il, jg = j0 + jl;
+            // select, never multiply: 2^{g_i - g_j} may overflow above the diagonal
+            const float w = (jg <= ig) ? s * exp2f(gq[ig] - gq[jg]) * dq[jg] : 0.f;
+            cb[il * 33 + jl] = w;
+        }
+        __syncthreads();
+        for (int jl = 0; jl < kRows; ++jl) {
+            const float w = cb[il * 33 + jl];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (k < pper) acc[k] = fmaf(w, xs[jl * P + pl + 8 * k], acc[k]);
+        }
+    }
+
+    const int tg = t0 + irow;
+    if (tg < L) {
+        const float dv = D ? D[h] : 0.f;
+        const int64_t base = (((int64_t)bidx * L + tg) * H + h) * P;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k < pper) {
+                const int pp = pl + 8 * k;
+                y[base + pp] = from_f32<T>(acc[k] + dv * to_f32(x[base + pp]));
+            }
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_fps(const Problem& p, const void* x, const void* B, const float* Gcs,
+                       const float* dtT, const float* init, void* hid, float* fin,
+                       cudaStream_t stream) {
+    const size_t smem = (size_t)(kSub * kPT + kSub * p.N + kSub) * sizeof(float);
+    auto kern = fwd_pass_state_simt<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(p.P / kPT), (unsigned)(p.b * p.H));
+    kern<<<grid, kThreads, smem, stream>>>((const T*)x, (const T*)B, Gcs, dtT, init, (T*)hid,
+                                           fin, (int)p.L, (int)p.H, (int)p.P, (int)p.N,
+                                           (int)p.G, (int)p.Q, (int)p.nc, (int)p.Lp, (int)p.hpg);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_co(const Problem& p, const void* x, const void* B, const void* C,
+                      const float* Gcs, const float* dtT, const void* hid, const float* D,
+                      void* y, cudaStream_t stream) {
+    const int NS = (int)p.N + 1;
+    const size_t smem = (size_t)(2 * kRows * NS + p.P * 33 + kRows * p.P + kRows * 33 + 2 * p.Q) *
+                        sizeof(float);
+    auto kern = compute_out_simt<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(p.Q / kRows), (unsigned)p.nc, (unsigned)(p.b * p.H));
+    kern<<<grid, kThreads, smem, stream>>>((const T*)x, (const T*)B, (const T*)C, Gcs, dtT,
+                                           (const T*)hid, D, (T*)y, (int)p.L, (int)p.H,
+                                           (int)p.P, (int)p.N, (int)p.G, (int)p.Q, (int)p.nc,
+                                           (int)p.Lp, (int)p.hpg);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_pass_state(const Problem& p, const void* x, const void* B,
+                                  const float* Gcs, const float* dtT, const float* init,
+                                  void* hiddens, float* final_state, cudaStream_t stream) {
+    if (p.dtype == SSD_BF16)
+        return launch_fps<__nv_bfloat16>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
+    return launch_fps<float>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
+}
+
+cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, const void* C,
+                               const float* Gcs, const float* dtT, const void* hiddens,
+                               const float* D, void* y, cudaStream_t stream) {
+    if (p.dtype == SSD_BF16)
+        return launch_co<__nv_bfloat16>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+    return launch_co<float>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+}
+
+}  // namespace ssd

@@ -1,0 +1,46 @@
+// ssd_internal.cuh -- shared declarations of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// log2(e): G is stored pre-multiplied by it so that every later exponential is
+// a base-2 one ("Kernel 1: chunk_cumsum": e^v = 2^(v log2 e)).
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Problem sizes after validation, with the derived quantities.
+struct Problem {
+    int64_t b, L, H, P, N, G, Q;
+    int64_t nc;   // number of chunks, ceil(L / Q)
+    int64_t Lp;   // padded token count nc * Q (row length of Gcs / dtT)
+    int64_t hpg;  // heads per group, H / G
+    int dtype;    // ssd_dtype
+    int esize;    // bytes per element of x, B, C, y, hiddens
+};
+
+// Launchers (defined next to their kernels).  All enqueue on `stream` and
+// return cudaGetLastError().
+cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* Gcs,
+                                float* dtT, cudaStream_t stream);
+cudaError_t launch_fwd_pass_state(const Problem& p, const void* x, const void* B,
+                                  const float* Gcs, const float* dtT, const float* init,
+                                  void* hiddens, float* final_state, cudaStream_t stream);
+cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, const void* C,
+                               const float* Gcs, const float* dtT, const void* hiddens,
+                               const float* D, void* y, cudaStream_t stream);
+
+// Element loads/stores shared by the kernels.
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+}  // namespace ssd

@@ -1,0 +1,129 @@
+"""The C ABI on the host: the library loads, exports every entry point that
+include/*.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import state_space_sequence_chunk_gb300 as ssd
+from state_space_sequence_chunk_gb300 import build as ssd_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssd_build.build()
+    return ssd.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(ssd_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_binding_exports():
+    assert set(ssd.EXPORTS) <= set(declared_functions())
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ssd_abi_version() == 1
+    for code in range(0, 9):
+        s = lib.ssd_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.ssd_status_string(99) == b"unknown status"
+
+
+def dims(**kw):
+    base = dict(batch=2, seqlen=300, nheads=4, headdim=64, dstate=128, ngroups=2,
+                chunk_size=128, dtype=ssd.SSD_BF16, reserved=0)
+    base.update(kw)
+    return ssd.Dims(*[base[k] for k, _ in ssd.Dims._fields_])
+
+
+def test_workspace_bytes(lib):
+    d = dims()
+    nc = 3
+    gcs = 2 * 4 * nc * 128 * 4
+    hid = 2 * 4 * nc * 64 * 128 * 2
+    ru = lambda v: (v + 255) // 256 * 256
+    assert ssd.ssd_fwd_workspace_bytes(d) == 2 * ru(gcs) + ru(hid)
+    assert ssd.ssd_intermediate_bytes(d) == (gcs, hid)
+    assert ssd.ssd_fwd_workspace_bytes(dims(seqlen=0)) == 0
+    assert ssd.ssd_fwd_workspace_bytes(dims(chunk_size=100)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk_size=96), 2), (dict(headdim=40), 2), (dict(headdim=256), 2),
+    (dict(dstate=8), 2), (dict(dstate=272), 2), (dict(ngroups=3), 2), (dict(nheads=0), 2),
+    (dict(batch=-1), 2), (dict(dtype=5), 3), (dict(reserved=1), 2)])
+def test_bad_shapes_rejected(lib, kw, code):
+    d = dims(**kw)
+    P = ctypes.c_void_p
+    a = [P(0x100000 * (i + 1)) for i in range(10)]
+    rc = lib.ssd_fwd(ctypes.byref(d), *a, ctypes.c_size_t(1 << 40), None)
+    assert rc == code
+
+
+def _fwd_args(n=10):
+    # distinct, 16-byte aligned, far-apart fake device addresses (never dereferenced:
+    # every call below fails validation before anything is enqueued)
+    return [ctypes.c_void_p(0x10000000000 * (i + 1)) for i in range(n)]
+
+
+def test_null_misaligned_alias_workspace(lib):
+    d = dims()
+    big = ctypes.c_size_t(1 << 40)
+    a = _fwd_args()
+    # x, dt, A, B, C, D, init, y, final, workspace
+    null_x = list(a); null_x[0] = None
+    assert lib.ssd_fwd(ctypes.byref(d), *null_x, big, None) == 1
+    null_ws = list(a); null_ws[9] = None
+    assert lib.ssd_fwd(ctypes.byref(d), *null_ws, big, None) == 1
+    mis = list(a); mis[3] = ctypes.c_void_p(a[3].value + 8)
+    assert lib.ssd_fwd(ctypes.byref(d), *mis, big, None) == 4
+    assert lib.ssd_fwd(ctypes.byref(d), *a, ctypes.c_size_t(100), None) == 5
+    alias = list(a); alias[7] = ctypes.c_void_p(a[0].value + 4096)   # y inside x
+    assert lib.ssd_fwd(ctypes.byref(d), *alias, big, None) == 8
+    alias = list(a); alias[9] = ctypes.c_void_p(a[4].value + 256)    # workspace inside C
+    assert lib.ssd_fwd(ctypes.byref(d), *alias, big, None) == 8
+    # D and init_state are optional: NULL passes validation and only fails at the
+    # device check (no GPU here) -- never with a validation code
+    opt = list(a); opt[5] = None; opt[6] = None; opt[8] = None
+    rc = lib.ssd_fwd(ctypes.byref(d), *opt, big, None)
+    assert rc in (0, 6, 7)
+
+
+def test_per_step_validation(lib):
+    d = dims()
+    a = _fwd_args()
+    assert lib.ssd_chunk_cumsum(ctypes.byref(d), a[0], None, a[2], a[3], None) == 1
+    assert lib.ssd_chunk_cumsum(ctypes.byref(d), a[0], a[1], a[2], a[2], None) == 8
+    assert lib.ssd_fwd_pass_state(ctypes.byref(d), a[0], a[1], a[2], a[3], a[4], None, a[6],
+                                  None) == 1
+    hid_in_x = ctypes.c_void_p(a[0].value + 1024)
+    assert lib.ssd_fwd_pass_state(ctypes.byref(d), a[0], a[1], a[2], a[3], a[4], hid_in_x, a[6],
+                                  None) == 8
+    assert lib.ssd_compute_out(ctypes.byref(d), a[0], a[1], a[2], a[3], a[4], a[5], None,
+                               ctypes.c_void_p(a[0].value), None) == 8
+
+
+def test_binding_raises_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="CUDA library not found"):
+        saved = ssd._lib
+        ssd._lib = None
+        try:
+            ssd.load_library(str(tmp_path / "nope.so"))
+        finally:
+            ssd._lib = saved

@@ -1,0 +1,229 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Every comparison is element by element on the same seeded inputs, with the
+bound max|out - ref| / max|ref| <= 1e-3 (fp32 inputs) or 1e-2 (bf16 inputs).
+Small problems are compared in full; the full-size workloads on sampled
+(batch, head) slices, each of which is an exact, independent recurrence.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import state_space_sequence_chunk_gb300 as ssd
+from state_space_sequence_chunk_gb300 import build as ssd_build
+from state_space_sequence_chunk_gb300 import synth
+from harness import TOL, gpu_fwd, oracle_fwd, rel_err, small, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    ssd_build.build()
+    ssd.load_library()
+
+
+# --- step 1: chunk_cumsum ---------------------------------------------------
+
+@pytest.mark.parametrize("Q,L", [(64, 64), (64, 301), (128, 1000), (256, 257), (256, 4096)])
+def test_chunk_cumsum(Q, L):
+    w = small(seqlen=L, nheads=37, chunk=Q, batch=2)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, w.dtype)
+    Gcs, dtT = ssd.ssd_chunk_cumsum(dev["dt"], dev["A"], Q)
+    torch.cuda.synchronize()
+    Gcs, dtT = Gcs.cpu().numpy(), dtT.cpu().numpy()
+    ref = oracle.chunk_cumsum(inp["dt"], inp["A"], Q)
+    assert rel_err(Gcs[:, :, :L], ref) < 2e-5
+    assert np.array_equal(dtT[:, :, :L], np.moveaxis(inp["dt"], 1, 2))
+    # padded tail: dt reads as 0, so G repeats the value at the last real token
+    assert not np.any(dtT[:, :, L:])
+    if Gcs.shape[2] > L:
+        assert np.array_equal(Gcs[:, :, L:], np.repeat(Gcs[:, :, L - 1:L], Gcs.shape[2] - L, 2))
+    # decay-mask invariant: G never increases inside a chunk, so every kept
+    # entry 2^{g_i - g_j} (i >= j) is at most 1
+    d = np.diff(Gcs.reshape(2, 37, -1, Q), axis=3)
+    assert np.all(d <= 0)
+
+
+# --- step 2: fwd_pass_state -------------------------------------------------
+
+@pytest.mark.parametrize("dtype,Q,L,P,N", [("f32", 64, 300, 32, 16), ("f32", 128, 700, 64, 64),
+                                           ("bf16", 256, 600, 64, 128), ("bf16", 128, 128, 16, 256),
+                                           ("bf16", 64, 1000, 128, 32)])
+def test_fwd_pass_state(dtype, Q, L, P, N):
+    w = small(seqlen=L, headdim=P, dstate=N, chunk=Q, dtype=dtype, nheads=4, ngroups=2, batch=2)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, dtype)
+    Gcs, dtT = ssd.ssd_chunk_cumsum(dev["dt"], dev["A"], Q)
+    hid, fin = ssd.ssd_fwd_pass_state(dev["x"], dev["B"], Gcs, dtT, dev["init_state"], Q)
+    torch.cuda.synchronize()
+    _, fin_ref, ck_ref = oracle_fwd(inp, ckpt_every=Q)
+    assert rel_err(hid.float().cpu().numpy(), ck_ref) < TOL[dtype]
+    assert rel_err(fin.cpu().numpy(), fin_ref) < TOL[dtype]
+
+
+# --- the whole pass on small and edge-case problems --------------------------
+
+CASES = [
+    # dtype, Q, L, H, G, P, N, init, D
+    ("f32", 64, 256, 2, 1, 32, 16, False, True),      # tiny workload shape
+    ("f32", 64, 1, 2, 1, 32, 16, True, True),         # one token
+    ("f32", 64, 63, 3, 3, 16, 32, True, False),       # shorter than a chunk, G = H
+    ("f32", 128, 389, 4, 2, 64, 64, True, True),      # ragged tail
+    ("bf16", 256, 511, 4, 1, 64, 128, False, True),   # ragged, Q = 256
+    ("bf16", 256, 4096, 2, 1, 64, 128, True, True),
+    ("bf16", 128, 130, 8, 2, 64, 128, True, True),    # 4 heads per group
+    ("bf16", 64, 200, 2, 2, 128, 256, True, True),    # largest P and N
+    ("bf16", 128, 333, 2, 1, 16, 16, True, True),     # smallest P and N
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-Q{c[1]}-L{c[2]}-H{c[3]}G{c[4]}-P{c[5]}N{c[6]}"
+                                              for c in CASES])
+def test_fwd_small(case):
+    dtype, Q, L, H, G, P, N, with_init, with_D = case
+    w = small(seqlen=L, nheads=H, ngroups=G, headdim=P, dstate=N, chunk=Q, dtype=dtype,
+              init_std=0.1 if with_init else 0.0, with_D=with_D, batch=2)
+    inp = synth.make_inputs(w)
+    y, fin = gpu_fwd(to_device(inp, dtype), Q)
+    y_ref, fin_ref = oracle_fwd(inp)
+    assert np.all(np.isfinite(y))
+    assert rel_err(y, y_ref) < TOL[dtype]
+    assert rel_err(fin, fin_ref) < TOL[dtype]
+
+
+# --- the five workloads -------------------------------------------------------
+
+SAMPLES = {"tiny_fp32": None, "small_fp32": None,
+           "mamba2_layer_bf16": [(0, 0), (1, 17), (2, 40), (3, 79)],
+           "long_context_bf16": [(0, 5), (0, 23)],
+           "short_streams_bf16": [(0, 0), (5, 3), (64, 12), (127, 31)]}
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_workload(name):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    y, fin = gpu_fwd(to_device(inp, w.dtype), w.chunk)
+    bh = SAMPLES[name]
+    if bh is None:
+        y_ref, fin_ref = oracle_fwd(inp)
+        assert rel_err(y, y_ref) < TOL[w.dtype]
+        assert rel_err(fin, fin_ref) < TOL[w.dtype]
+    else:
+        refs = oracle_fwd(inp, bh=bh)
+        ys = np.stack([y[b, :, h] for b, h in bh])
+        ys_ref = np.stack([r[0][0, :, 0] for r in refs])
+        fs = np.stack([fin[b, h] for b, h in bh])
+        fs_ref = np.stack([r[1][0, 0] for r in refs])
+        assert rel_err(ys, ys_ref) < TOL[w.dtype]
+        assert rel_err(fs, fs_ref) < TOL[w.dtype]
+    assert np.all(np.isfinite(y))
+
+
+# --- properties -----------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_size_invariance(dtype):
+    """The recurrence has no chunk parameter: every chunk size meets the bound
+    against one oracle run."""
+    w = small(seqlen=777, nheads=4, ngroups=2, headdim=64, dstate=64, dtype=dtype)
+    inp = synth.make_inputs(w)
+    y_ref, fin_ref = oracle_fwd(inp)
+    dev = to_device(inp, dtype)
+    for Q in (64, 128, 256):
+        y, fin = gpu_fwd(dev, Q)
+        assert rel_err(y, y_ref) < TOL[dtype], Q
+        assert rel_err(fin, fin_ref) < TOL[dtype], Q
+
+
+def test_split_composition():
+    """final_state fed back as init_state continues the sequence."""
+    w = small(seqlen=700, dtype="f32", headdim=32, dstate=32)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, "f32")
+    y_full, f_full = gpu_fwd(dev, 64)
+    L1 = 300
+    d1 = {k: (v[:, :L1].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in dev.items()}
+    y1, f1 = gpu_fwd(d1, 64)
+    d2 = {k: (v[:, L1:].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in dev.items()}
+    d2["init_state"] = torch.from_numpy(f1).cuda()
+    y2, f2 = gpu_fwd(d2, 64)
+    assert rel_err(np.concatenate([y1, y2], axis=1), y_full) < 1e-4
+    assert rel_err(f2, f_full) < 1e-4
+
+
+@pytest.mark.parametrize("dtype,Q", [("f32", 128), ("bf16", 256)])
+def test_strong_decay_never_overflows(dtype, Q):
+    """Decays of up to -46 per token (log2 units): above the diagonal 2^{g_i - g_j}
+    overflows to inf, and the mask must discard it (a select, not a product)."""
+    w = small(seqlen=600, dtype=dtype, chunk=Q, headdim=32, dstate=32)
+    inp = synth.make_inputs(w)
+    inp["A"] = np.full_like(inp["A"], -16.0)
+    inp["dt"] = np.full_like(inp["dt"], 2.0)
+    y, fin = gpu_fwd(to_device(inp, dtype), Q)
+    y_ref, fin_ref = oracle_fwd(inp)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(fin))
+    assert rel_err(y, y_ref) < TOL[dtype]
+    assert rel_err(fin, fin_ref) < TOL[dtype]
+
+
+def test_inplace_state_update():
+    w = small(seqlen=300, dtype="bf16", chunk=128, headdim=64, dstate=128)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, "bf16")
+    y_ref, f_ref = gpu_fwd(dev, 128)
+    state = dev["init_state"].clone()
+    y, f = ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], state,
+                       chunk_size=128, final_out=state)
+    torch.cuda.synchronize()
+    assert np.array_equal(state.cpu().numpy(), f_ref)
+    assert np.array_equal(y.float().cpu().numpy(), y_ref)
+
+
+def test_empty_inputs():
+    w = small(seqlen=0, dtype="bf16", chunk=64)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, "bf16")
+    y, fin = ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                         dev["init_state"], chunk_size=64)
+    torch.cuda.synchronize()
+    assert y.numel() == 0
+    assert np.array_equal(fin.cpu().numpy(), inp["init_state"])
+    w0 = small(seqlen=10, batch=0, dtype="bf16")
+    d0 = to_device(synth.make_inputs(w0), "bf16")
+    y0, f0 = ssd.ssd_fwd(d0["x"], d0["dt"], d0["A"], d0["B"], d0["C"], d0["D"], d0["init_state"],
+                         chunk_size=64)
+    assert y0.numel() == 0 and f0.numel() == 0
+
+
+def test_deterministic_and_stream_ordered():
+    w = small(seqlen=1000, dtype="bf16", chunk=256, headdim=64, dstate=128)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, "bf16")
+    y1, f1 = gpu_fwd(dev, 256)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y2, f2 = ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                             dev["init_state"], chunk_size=256)
+    s.synchronize()
+    assert np.array_equal(y1, y2.float().cpu().numpy())
+    assert np.array_equal(f1, f2.cpu().numpy())
+
+
+def test_errors_are_raised():
+    w = small(seqlen=100, dtype="bf16", chunk=64)
+    dev = to_device(synth.make_inputs(w), "bf16")
+    small_ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ssd.SSDError, match="SSD_ERR_WORKSPACE"):
+        ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], workspace=small_ws,
+                    chunk_size=64)
+    with pytest.raises(ssd.SSDError, match="SSD_ERR_SHAPE"):
+        ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=96)
+    with pytest.raises(ssd.SSDError, match="SSD_ERR_ALIAS"):
+        ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=64,
+                    out=dev["x"])
