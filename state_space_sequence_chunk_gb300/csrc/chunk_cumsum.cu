@@ -63,12 +63,29 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
             if (lane >= off) incl += o;
         }
         const float excl = incl - run;
+        float out[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) out[k] = (vals[k] + excl) * kLog2e;
+        if (t0 + Q > L) {
+            // ragged last chunk: the padded slots take exactly the value at the
+            // last real token, so that g_last (read at the chunk's last slot) is
+            // bit-identical to it
+            const int last = L - 1 - t0, src_lane = last / per_lane, src_k = last % per_lane;
+            float v = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k == src_k) v = out[k];
+            v = __shfl_sync(0xffffffffu, v, src_lane);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (t0 + lane * per_lane + k > L - 1) out[k] = v;
+        }
         float* grow = Gcs + ((int64_t)b * H + h) * Lp + t0 + lane * per_lane;
         float* drow = dtT + ((int64_t)b * H + h) * Lp + t0 + lane * per_lane;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             if (k < per_lane) {
-                grow[k] = (vals[k] + excl) * kLog2e;
+                grow[k] = out[k];
                 drow[k] = tile[lane * per_lane + k][j];
             }
         }
