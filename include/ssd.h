@@ -143,6 +143,45 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
                            const float* Gcs, const float* dtT, const void* hiddens,
                            const float* D, void* y, void* stream);
 
+/* Size of the fixed device scratch buffer used by ssd_fwd_noalloc: 32 MiB. */
+#define SSD_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/*
+ * ssd_fwd_noalloc -- ssd_fwd for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that cannot call cudaMalloc or any other allocator on their path: a host
+ * framework that owns all device memory and hands out only its own fixed
+ * buffers, a latency-critical loop that must not call cudaMalloc/cudaFree
+ * (those calls can synchronise the device and take driver-wide locks), or a
+ * process whose device memory is already fully reserved by a pool.  Such a
+ * caller still passes every input and
+ * output; the scratch that ssd_fwd takes as `workspace` (the Gcs, dtT and
+ * hiddens intermediates) lives instead in one statically sized device array of
+ * SSD_NOALLOC_WORKSPACE_BYTES inside this library.  Every GPU that loads the
+ * library holds that array until the process exits.
+ *
+ * Arguments, layouts, ownership and results are those of ssd_fwd, minus the
+ * workspace.  Problems whose ssd_fwd_workspace_bytes() exceeds
+ * SSD_NOALLOC_WORKSPACE_BYTES are rejected with SSD_ERR_WORKSPACE before
+ * anything is enqueued; use ssd_fwd with a caller-owned workspace for those.
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *
+ * Set-up: the first call on each device (made with that device current) looks
+ * up the device address of the static array once and caches it; make that
+ * first call before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, and it keeps the last
+ * call's contents.  The kernels overwrite every intermediate they read, so
+ * nothing has to start at zero.  Calls that overlap on the GPU (on different
+ * streams, or from different host threads without ordering) race on the array
+ * and give wrong results: serialise them.
+ */
+ssd_status ssd_fwd_noalloc(const ssd_dims* d, const void* x, const float* dt, const float* A,
+                           const void* B, const void* C, const float* D,
+                           const float* init_state, void* y, float* final_state, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE"
           8: "SSD_ERR_ALIAS"}
 EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
-           "ssd_compute_out"]
+           "ssd_compute_out", "ssd_fwd_noalloc"]
 
 
 class SSDError(RuntimeError):
@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_fwd_pass_state.restype = ctypes.c_int
         lib.ssd_compute_out.argtypes = [dp] + [vp] * 9
         lib.ssd_compute_out.restype = ctypes.c_int
+        lib.ssd_fwd_noalloc.argtypes = [dp] + [vp] * 10
+        lib.ssd_fwd_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -191,3 +193,22 @@ def ssd_compute_out(x, B, C, Gcs, dtT, hiddens, D=None, chunk_size: int = 256):
     _check(lib.ssd_compute_out(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(C), _ptr(Gcs), _ptr(dtT),
                                _ptr(hiddens), _ptr(D), _ptr(y), _stream()))
     return y
+
+
+def ssd_fwd_noalloc(x, dt, A, B, C, D=None, init_state=None, chunk_size: int = 256,
+                    out=None, final_out=None):
+    """ssd_fwd without a workspace argument, for callers that cannot allocate
+    device memory: the library uses its own fixed 32 MiB device scratch array.
+
+    The caller passes every input and output buffer (``out`` for y and, if the
+    final state is wanted, ``final_out``); nothing is allocated here when both
+    are given.  Problems needing more scratch than the fixed array raise
+    SSD_ERR_WORKSPACE.  Calls on one device share the array, so calls that
+    overlap on the GPU must be serialised by the caller.
+    """
+    lib = load_library()
+    dims = dims_for(x, B, chunk_size)
+    y = out if out is not None else torch.empty_like(x)
+    _check(lib.ssd_fwd_noalloc(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                               _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_out), _stream()))
+    return y, final_out
