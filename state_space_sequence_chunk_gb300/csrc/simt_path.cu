@@ -249,7 +249,7 @@ cudaError_t launch_fwd_pass_state(const Problem& p, const void* x, const void* B
                                   const float* Gcs, const float* dtT, const float* init,
                                   void* hiddens, float* final_state, cudaStream_t stream) {
     if (p.dtype == SSD_BF16)
-        return launch_fps<__nv_bfloat16>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
+        return launch_fwd_pass_state_tc(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
     return launch_fps<float>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
 }
 
