@@ -143,6 +143,16 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
                            const float* Gcs, const float* dtT, const void* hiddens,
                            const float* D, void* y, void* stream);
 
+/*
+ * ssd_take_device_errors -- read and clear the device-side error words of the
+ * tensor-core kernels.  Every wait inside those kernels is bounded; a wait
+ * that gives up (it never should) sets a bit and the kernel ends early with
+ * undefined output instead of hanging.  Bit 0: fwd_pass_state, bit 1:
+ * compute_out.  Synchronises the current device; returns 0xFFFFFFFF if the
+ * words cannot be read.
+ */
+unsigned int ssd_take_device_errors(void);
+
 /* Size of the fixed device scratch buffer used by ssd_fwd_noalloc: 32 MiB. */
 #define SSD_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
 

@@ -32,7 +32,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE"
           8: "SSD_ERR_ALIAS"}
 EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
-           "ssd_compute_out", "ssd_fwd_noalloc"]
+           "ssd_compute_out", "ssd_fwd_noalloc", "ssd_take_device_errors"]
 
 
 class SSDError(RuntimeError):
@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_fwd_pass_state.restype = ctypes.c_int
         lib.ssd_compute_out.argtypes = [dp] + [vp] * 9
         lib.ssd_compute_out.restype = ctypes.c_int
+        lib.ssd_take_device_errors.argtypes = []
+        lib.ssd_take_device_errors.restype = ctypes.c_uint
         lib.ssd_fwd_noalloc.argtypes = [dp] + [vp] * 10
         lib.ssd_fwd_noalloc.restype = ctypes.c_int
         _lib = lib
@@ -118,6 +120,12 @@ def _ptr(t):
 
 def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def ssd_take_device_errors() -> int:
+    """Read and clear the kernels' device-side error bits (0 = no bounded wait
+    ever gave up).  Synchronises the device."""
+    return int(load_library().ssd_take_device_errors())
 
 
 def ssd_fwd_workspace_bytes(dims: Dims) -> int:

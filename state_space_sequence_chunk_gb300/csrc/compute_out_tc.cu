@@ -1,0 +1,552 @@
+// compute_out_tc.cu -- step 3 of the SSD forward pass on the tcgen05 tensor
+// cores (bf16 inputs, fp32 accumulation).
+//
+// "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA
+// CUDA Tile", section "Kernel 3: compute_out" (with "Step 2" and "Step 3"):
+// per (batch, chunk, head)
+//     Y = 2^{g} o (C h^T) + ((2^{g_i - g_j} [i >= j]) o (C B^T)) (dt o X) + D X
+// with the Q x Q matrix kept on chip and the causal mask applied as a select,
+// so the overflowing above-diagonal exponentials never reach the output.
+//
+// GB300 design (what differs from the pages' cuTile kernel):
+//  * Persistent CTAs, one per SM.  Work units (batch, chunk, head) are ordered
+//    so that the heads sharing one B/C group are adjacent; each CTA takes a
+//    contiguous, balanced range of units.  C B^T depends only on (batch,
+//    chunk, group), so it is computed once per group on the tensor core and
+//    kept in tensor memory as packed bf16, instead of once per head.
+//  * Queries are processed in 128-row blocks (the MMA's M).  For block I:
+//        acc  = C_I h^T                       (A = C from smem, B = h from smem)
+//        acc *= 2^{g_i}                       (row scale, in TMEM, by the SIMT warps)
+//        A_I  = (C B^T)_I o 2^{g_i - g_j} o dt_j, j <= i   (built by the SIMT warps
+//               directly into TMEM, bf16)
+//        acc += A_I X_{0..}                   (A from TMEM, B = X from smem)
+//        y    = acc + D x                     (epilogue, stored from registers)
+//    Two TMEM slots (block 0 / block 1 of a 256-token chunk, or alternate heads
+//    for shorter chunks) let one block's MMAs overlap the other's SIMT work.
+//  * x, h, C, B and the per-token g, dt vectors arrive by TMA / bulk copies
+//    into a stage ring; B only passes through the ring once per group.
+//
+// Warp roles (384 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
+// 2-3 idle, 4-7 SIMT warpgroup 0 (slot 0), 8-11 SIMT warpgroup 1 (slot 1).
+// A SIMT thread owns TMEM lane (query row) 32*(warp%4) + lane.
+//
+// Supported here: bf16, P <= 64, N <= 128, Q in {64, 128, 256}.
+#include <cuda.h>
+
+#include "sm100_ptx.cuh"
+#include "ssd_internal.cuh"
+#include "tma_host.cuh"
+
+namespace ssd {
+namespace {
+
+__device__ unsigned int g_co_error;  // bit 0: a bounded wait gave up
+
+constexpr int kThreads = 384;
+constexpr int kRowBytes = 128;
+constexpr int kSimtWarp0 = 4;
+constexpr int kSimtThreads = 256;
+
+template <int Q>
+struct CoCfg {
+    static constexpr int kBlocks = Q > 128 ? 2 : 1;        // 128-row query blocks per chunk
+    static constexpr int kBRows = Q < 128 ? Q : 128;        // rows of a key block
+    static constexpr int kCRows = Q < 128 ? 128 : Q;        // rows reserved per C atom
+    static constexpr int kNAtoms = 2;                       // N padded to 128 (two 64-wide atoms)
+    static constexpr int kCAtomBytes = kCRows * kRowBytes;
+    static constexpr int kCBytes = kNAtoms * kCAtomBytes;
+    static constexpr int kCBufs = Q > 128 ? 1 : 2;
+    static constexpr int kXBytes = Q * kRowBytes;           // x tile, P padded to 64
+    static constexpr int kHAtomBytes = 64 * kRowBytes;      // 64 rows of P x 64 of N
+    static constexpr int kHBytes = kNAtoms * kHAtomBytes;
+    static constexpr int kVecBytes = Q * 4;
+    static constexpr int kStageBytes = ((kXBytes + kHBytes + 2 * kVecBytes) + 1023) / 1024 * 1024;
+    static constexpr int kStages = Q > 128 ? 3 : 4;
+    static constexpr int kBSlots = Q > 128 ? 2 : 1;         // stage slots a B tile occupies
+    static constexpr int kBAtomBytes = kBRows * kRowBytes;
+    static constexpr int kBarBytes = 512;
+    static constexpr int kSmem = kCBufs * kCBytes + kStages * kStageBytes + kBarBytes + 1024;
+    // TMEM columns (512 allocated)
+    // layout, Q = 256: [0,192) CB blocks (0,0) (1,0) (1,1); [192,256) A slot 0;
+    //   [256,384) A slot 1; [384,448) acc slot 0; [448,512) acc slot 1;
+    //   fp32 scratch for C B^T: [256,384) and [384,512) (only while drained).
+    // layout, Q <= 128: [0,64) CB buffer 0; [64,128) CB buffer 1; [128,192) A slot 0;
+    //   [192,256) A slot 1; [256,320) acc slot 0; [320,384) acc slot 1; scratch [384,512).
+    static constexpr uint32_t kCbBase = 0;
+    static constexpr uint32_t kA0 = Q > 128 ? 192 : 128;
+    static constexpr uint32_t kA1 = Q > 128 ? 256 : 192;
+    static constexpr uint32_t kAcc0 = Q > 128 ? 384 : 256;
+    static constexpr uint32_t kAcc1 = Q > 128 ? 448 : 320;
+    static constexpr uint32_t kScratch = Q > 128 ? 256 : 384;
+};
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+
+// The units of a CTA: [u0, u1) of the list ordered (batch, chunk, head).
+struct UnitInfo {
+    int b, c, h, grp;
+};
+__device__ __forceinline__ UnitInfo unit_info(int u, int nc, int H, int hpg) {
+    UnitInfo r;
+    r.h = u % H;
+    const int bc = u / H;
+    r.c = bc % nc;
+    r.b = bc / nc;
+    r.grp = r.h / hpg;
+    return r;
+}
+__device__ __forceinline__ bool new_group(int u, int u0, int H, int hpg) {
+    return u == u0 || (u % H) % hpg == 0;
+}
+
+template <int Q>
+__global__ void __launch_bounds__(kThreads, 1)
+compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
+               const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_h,
+               const float* __restrict__ Gcs, const float* __restrict__ dtT,
+               const float* __restrict__ D, __nv_bfloat16* __restrict__ y, int L, int H, int P,
+               int nc, int Lp, int hpg, int units) {
+    using Cfg = CoCfg<Q>;
+    constexpr int NST = Cfg::kStages;
+    constexpr int NCB = Cfg::kCBufs;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* cbuf_ptr = smem;
+    uint8_t* stage_ptr = smem + NCB * Cfg::kCBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_ptr + NST * Cfg::kStageBytes);
+    // barrier map
+    uint64_t* b_full = bars;                 // [NST]  stage loaded (tx)
+    uint64_t* b_empty = b_full + NST;        // [NST]  stage released (256 SIMT arrivals)
+    uint64_t* b_grp = b_empty + NST;         // [NCB]  C + B of a group loaded (tx)
+    uint64_t* b_cfree = b_grp + NCB;         // [NCB]  last C h^T of a group done (commit)
+    uint64_t* b_cbfull = b_cfree + NCB;      // [2]    C B^T round done (commit)
+    uint64_t* b_cbconv = b_cbfull + 2;       // [2]    C B^T round converted (256 arrivals)
+    uint64_t* b_sdone = b_cbconv + 2;        // [2]    slot: C h^T done (commit)
+    uint64_t* b_ddone = b_sdone + 2;         // [2]    slot: A X done (commit)
+    uint64_t* b_aready = b_ddone + 2;        // [2]    slot: A built (128 arrivals)
+    uint64_t* b_scaled = b_aready + 2;       // [2]    slot: acc row-scaled (128 arrivals)
+    uint64_t* b_accfree = b_scaled + 2;      // [2]    slot: acc read by the epilogue (128)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(b_accfree + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int u0 = (int)((int64_t)blockIdx.x * units / gridDim.x);
+    const int u1 = (int)((int64_t)(blockIdx.x + 1) * units / gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(smem_u32(b_full + s), 1);
+            mbar_init(smem_u32(b_empty + s), kSimtThreads);
+        }
+        for (int s = 0; s < NCB; ++s) {
+            mbar_init(smem_u32(b_grp + s), 1);
+            mbar_init(smem_u32(b_cfree + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(b_cbfull + s), 1);
+            mbar_init(smem_u32(b_cbconv + s), kSimtThreads);
+            mbar_init(smem_u32(b_sdone + s), 1);
+            mbar_init(smem_u32(b_ddone + s), 1);
+            mbar_init(smem_u32(b_aready + s), 128);
+            mbar_init(smem_u32(b_scaled + s), 128);
+            mbar_init(smem_u32(b_accfree + s), 128);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    unsigned int* err = &g_co_error;
+
+    if (warp == 0) {
+        // ===================== TMA producer =====================
+        if (lane == 0) {
+            int sc = 0;   // stage ring counter
+            int gi = -1;  // group counter
+            for (int u = u0; u < u1; ++u) {
+                const UnitInfo ui = unit_info(u, nc, H, hpg);
+                if (new_group(u, u0, H, hpg)) {
+                    ++gi;
+                    const int cb = gi % NCB;
+                    // C buffer reuse: the previous group in it has finished its C h^T
+                    mbar_wait(smem_u32(b_cfree + cb), ((gi / NCB) & 1) ^ 1, err, 1u);
+                    // B passes through kBSlots stage slots
+                    int bslot[2];
+                    for (int j = 0; j < Cfg::kBSlots; ++j) {
+                        const int s = (sc + j) % NST, k = (sc + j) / NST;
+                        mbar_wait(smem_u32(b_empty + s), (k & 1) ^ 1, err, 1u);
+                        bslot[j] = s;
+                    }
+                    const uint32_t gbar = smem_u32(b_grp + cb);
+                    mbar_arrive_expect_tx(gbar, Cfg::kNAtoms * (Q * kRowBytes) +
+                                                    Cfg::kBSlots * Cfg::kNAtoms * Cfg::kBAtomBytes);
+                    const uint32_t cdst = smem_u32(cbuf_ptr + cb * Cfg::kCBytes);
+                    for (int a = 0; a < Cfg::kNAtoms; ++a)
+                        tma_load_4d(cdst + a * Cfg::kCAtomBytes, &tm_c, gbar, a * 64, ui.grp,
+                                    ui.c * Q, ui.b);
+                    for (int j = 0; j < Cfg::kBSlots; ++j) {
+                        const uint32_t bdst = smem_u32(stage_ptr + bslot[j] * Cfg::kStageBytes);
+                        for (int a = 0; a < Cfg::kNAtoms; ++a)
+                            tma_load_4d(bdst + a * Cfg::kBAtomBytes, &tm_b, gbar, a * 64, ui.grp,
+                                        ui.c * Q + j * 128, ui.b);
+                    }
+                    // keep the slots' "full" phases in step with the ring (the B
+                    // bytes themselves complete on the group barrier)
+                    for (int j = 0; j < Cfg::kBSlots; ++j) mbar_arrive(smem_u32(b_full + bslot[j]));
+                    sc += Cfg::kBSlots;
+                }
+                // head stage: x, h, g, dt
+                const int s = sc % NST, k = sc / NST;
+                mbar_wait(smem_u32(b_empty + s), (k & 1) ^ 1, err, 1u);
+                const uint32_t fb = smem_u32(b_full + s);
+                uint8_t* st = stage_ptr + s * Cfg::kStageBytes;
+                mbar_arrive_expect_tx(fb, Cfg::kXBytes + Cfg::kHBytes + 2 * Cfg::kVecBytes);
+                tma_load_4d(smem_u32(st), &tm_x, fb, 0, ui.h, ui.c * Q, ui.b);
+                const int bh = ui.b * H + ui.h;
+                for (int a = 0; a < Cfg::kNAtoms; ++a)
+                    tma_load_4d(smem_u32(st + Cfg::kXBytes + a * Cfg::kHAtomBytes), &tm_h, fb,
+                                a * 64, 0, bh * nc + ui.c, 0);
+                const int64_t vo = (int64_t)bh * Lp + (int64_t)ui.c * Q;
+                bulk_load(smem_u32(st + Cfg::kXBytes + Cfg::kHBytes), Gcs + vo, Cfg::kVecBytes, fb);
+                bulk_load(smem_u32(st + Cfg::kXBytes + Cfg::kHBytes + Cfg::kVecBytes), dtT + vo,
+                          Cfg::kVecBytes, fb);
+                ++sc;
+            }
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (lane == 0) {
+            constexpr uint32_t kIdescCB = make_idesc(1, 128, Cfg::kBRows, 0, 0);
+            constexpr uint32_t kIdescS = make_idesc(1, 128, 64, 0, 0);
+            constexpr uint32_t kIdescD = make_idesc(1, 128, 64, 0, 1);
+            int sc = 0, gi = -1, js = 0;  // stage, group, slot-job counters
+            int cbq = 0;                  // C buffer of the current group
+            for (int u = u0; u < u1; ++u) {
+                const bool ng = new_group(u, u0, H, hpg);
+                if (ng) {
+                    ++gi;
+                    cbq = gi % NCB;
+                    mbar_wait(smem_u32(b_grp + cbq), (gi / NCB) & 1, err, 1u);
+                    if (Q > 128) {
+                        // the C B^T scratch overlaps slot memory: drain both slots
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int uses = (js + 1 - s2) / 2;  // completed uses of slot s2
+                            if (uses > 0)
+                                mbar_wait(smem_u32(b_accfree + s2), (uses - 1) & 1, err, 1u);
+                        }
+                    } else {
+                        // scratch reuse: the previous group's conversion has read it
+                        mbar_wait(smem_u32(b_cbconv), (gi & 1) ^ 1, err, 1u);
+                    }
+                    tc_fence_after();
+                    const uint32_t cbase = smem_u32(cbuf_ptr + cbq * Cfg::kCBytes);
+                    // rounds of C B^T blocks (I, J): Q=256: {(0,0),(1,0)} then {(1,1)}
+                    const int rounds = Q > 128 ? 2 : 1;
+                    for (int r = 0; r < rounds; ++r) {
+                        if (r == 1) {
+                            mbar_wait(smem_u32(b_cbconv), gi & 1, err, 1u);
+                            tc_fence_after();
+                        }
+                        const int nblk = (Q > 128 && r == 0) ? 2 : 1;
+                        for (int q = 0; q < nblk; ++q) {
+                            const int I = (Q > 128) ? (r == 0 ? q : 1) : 0;
+                            const int J = (Q > 128) ? (r == 0 ? 0 : 1) : 0;
+                            const uint32_t bbase =
+                                smem_u32(stage_ptr + ((sc + J) % NST) * Cfg::kStageBytes);
+                            const uint32_t dcol = tmem + Cfg::kScratch + q * 128;
+                            for (int kk = 0; kk < 8; ++kk) {  // K = 128 state columns
+                                const uint64_t ad = smem_desc_sw128(
+                                    cbase + (kk / 4) * Cfg::kCAtomBytes + I * 128 * kRowBytes +
+                                        (kk % 4) * 32, 16, 8 * kRowBytes);
+                                const uint64_t bd = smem_desc_sw128(
+                                    bbase + (kk / 4) * Cfg::kBAtomBytes + (kk % 4) * 32, 16,
+                                    8 * kRowBytes);
+                                mma_f16_ss(dcol, ad, bd, kIdescCB, kk > 0 ? 1u : 0u);
+                            }
+                        }
+                        mma_commit(smem_u32(b_cbfull + r));
+                    }
+                    sc += Cfg::kBSlots;
+                }
+                const int s = sc % NST, k = sc / NST;
+                mbar_wait(smem_u32(b_full + s), k & 1, err, 1u);
+                tc_fence_after();
+                const uint32_t st = smem_u32(stage_ptr + s * Cfg::kStageBytes);
+                const uint32_t cbase = smem_u32(cbuf_ptr + cbq * Cfg::kCBytes);
+                // acc = C_I h^T for each block of this head
+                for (int I = 0; I < Cfg::kBlocks; ++I) {
+                    const int slot = (js + I) & 1, use = (js + I) >> 1;
+                    mbar_wait(smem_u32(b_accfree + slot), (use & 1) ^ 1, err, 1u);
+                    tc_fence_after();
+                    const uint32_t acc = tmem + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(
+                            cbase + (kk / 4) * Cfg::kCAtomBytes + I * 128 * kRowBytes + (kk % 4) * 32,
+                            16, 8 * kRowBytes);
+                        const uint64_t bd = smem_desc_sw128(
+                            st + Cfg::kXBytes + (kk / 4) * Cfg::kHAtomBytes + (kk % 4) * 32, 16,
+                            8 * kRowBytes);
+                        mma_f16_ss(acc, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(b_sdone + slot));
+                }
+                // the C buffer is free once the group's last C h^T is done
+                if (u + 1 == u1 || new_group(u + 1, u0, H, hpg)) mma_commit(smem_u32(b_cfree + cbq));
+                // acc += A_I X
+                for (int I = 0; I < Cfg::kBlocks; ++I) {
+                    const int slot = (js + I) & 1, use = (js + I) >> 1;
+                    mbar_wait(smem_u32(b_aready + slot), use & 1, err, 1u);
+                    mbar_wait(smem_u32(b_scaled + slot), use & 1, err, 1u);
+                    tc_fence_after();
+                    const uint32_t acc = tmem + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
+                    const uint32_t abase = tmem + (slot ? Cfg::kA1 : Cfg::kA0);
+                    const int ksteps = (Q > 128 ? (I + 1) * 128 : Q) / 16;
+                    for (int kk = 0; kk < ksteps; ++kk) {
+                        const uint64_t bd = smem_desc_sw128(st + kk * 16 * kRowBytes, 8 * kRowBytes,
+                                                            8 * kRowBytes);
+                        mma_f16_ts(acc, abase + kk * 8, bd, kIdescD, 1u);
+                    }
+                    mma_commit(smem_u32(b_ddone + slot));
+                }
+                js += Cfg::kBlocks;
+                ++sc;
+            }
+        }
+    } else if (warp >= kSimtWarp0) {
+        // ===================== SIMT warpgroups =====================
+        const int wg = (warp - kSimtWarp0) >> 2;         // 0 or 1
+        const int row = (warp & 3) * 32 + lane;         // TMEM lane / query row in block
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        int sc = 0, gi = -1, js = 0;
+        for (int u = u0; u < u1; ++u) {
+            const UnitInfo ui = unit_info(u, nc, H, hpg);
+            if (new_group(u, u0, H, hpg)) {
+                ++gi;
+                // convert C B^T (fp32 scratch) to packed bf16
+                const int rounds = Q > 128 ? 2 : 1;
+                const uint32_t cbdst = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
+                for (int r = 0; r < rounds; ++r) {
+                    mbar_wait(smem_u32(b_cbfull + r), gi & 1, err, 1u);
+                    tc_fence_after();
+                    // round 0 of Q=256: wg 0 converts block (0,0), wg 1 block (1,0);
+                    // otherwise both warpgroups take half of the block's columns.
+                    int q, c0, ncol, dcol;
+                    if (Q > 128 && r == 0) {
+                        q = wg; c0 = 0; ncol = 128; dcol = wg * 64;
+                    } else {
+                        q = 0; ncol = Cfg::kBRows / 2; c0 = wg * ncol;
+                        dcol = (Q > 128 ? 128 : 0) + c0 / 2;
+                    }
+                    for (int cc = 0; cc < ncol; cc += 32) {
+                        uint32_t v[32], o[16];
+                        tmem_ld_x32(tmem + lane_off + Cfg::kScratch + q * 128 + c0 + cc, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            o[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                        tmem_st_x16(tmem + lane_off + cbdst + dcol + cc / 2, o);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(b_cbconv + r));
+                }
+                // Both warpgroups read each other's halves of the last round: wait
+                // for the whole conversion.  (The MMA warp waits on round 0 of a
+                // 256-token chunk before it reuses the scratch for round 1.)
+                mbar_wait(smem_u32(b_cbconv + (rounds - 1)), gi & 1, err, 1u);
+                tc_fence_after();
+                // release the stage slots that carried B
+                for (int j = 0; j < Cfg::kBSlots; ++j) mbar_arrive(smem_u32(b_empty + (sc + j) % NST));
+                sc += Cfg::kBSlots;
+            }
+            const int s = sc % NST, k = sc / NST;
+            mbar_wait(smem_u32(b_full + s), k & 1, err, 1u);
+            const uint8_t* st = stage_ptr + s * Cfg::kStageBytes;
+            const float* gv = reinterpret_cast<const float*>(st + Cfg::kXBytes + Cfg::kHBytes);
+            const float* dv = gv + Q;
+            const uint32_t cbsrc = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
+            // which block of this head (if any) this warpgroup owns
+            int I = -1, slot = 0, use = 0;
+            if (Q > 128) {
+                I = wg; slot = (js + wg) & 1; use = (js + wg) >> 1;
+            } else if ((js & 1) == wg) {
+                I = 0; slot = js & 1; use = js >> 1;
+            }
+            if (I >= 0) {
+                const int i = I * 128 + row;               // query row in the chunk
+                const float gi_ = (i < Q) ? gv[i] : 0.f;
+                const uint32_t abase = tmem + lane_off + (slot ? Cfg::kA1 : Cfg::kA0);
+                const uint32_t acc = tmem + lane_off + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
+                // ---- build A_I: key columns j in [0, K_I) ----
+                const int KI = Q > 128 ? (I + 1) * 128 : Q;
+                for (int j0 = 0; j0 < KI; j0 += 32) {
+                    const int J = j0 / 128, jl0 = j0 % 128;
+                    uint32_t o[16];
+                    if (J == I && jl0 > row) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] = 0u;
+                    } else {
+                        // packed C B^T block (I, J): Q=256 blocks at 0 (0,0), 64 (1,0), 128 (1,1)
+                        const uint32_t blk = Q > 128 ? (I == 0 ? 0u : (J == 0 ? 64u : 128u)) : 0u;
+                        uint32_t v[16];
+                        tmem_ld_x16(tmem + lane_off + cbsrc + blk + jl0 / 2, v);
+                        tmem_wait_ld();
+                        const bool diag = (J == I);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int ja = j0 + 2 * e, jb = ja + 1;
+                            const float wa = exp2f(gi_ - gv[ja]) * dv[ja];
+                            const float wb = exp2f(gi_ - gv[jb]) * dv[jb];
+                            float va = bf16lo(v[e]) * wa, vb = bf16hi(v[e]) * wb;
+                            if (diag) {
+                                va = (jl0 + 2 * e <= row) ? va : 0.f;
+                                vb = (jl0 + 2 * e + 1 <= row) ? vb : 0.f;
+                            }
+                            o[e] = pack_bf16(va, vb);
+                        }
+                    }
+                    tmem_st_x16(abase + j0 / 2, o);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(b_aready + slot));
+                // ---- acc *= 2^{g_i} ----
+                mbar_wait(smem_u32(b_sdone + slot), use & 1, err, 1u);
+                tc_fence_after();
+                {
+                    const float sg = exp2f(gi_);
+                    uint32_t v[32];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        tmem_ld_x32(acc + h2 * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * sg);
+                        tmem_st_x32(acc + h2 * 32, v);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(b_scaled + slot));
+                // ---- epilogue: y = acc + D x ----
+                mbar_wait(smem_u32(b_ddone + slot), use & 1, err, 1u);
+                tc_fence_after();
+                uint32_t v[64];
+                {
+                    uint32_t t0[32], t1[32];
+                    tmem_ld_x32(acc, t0);
+                    tmem_ld_x32(acc + 32, t1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) { v[e] = t0[e]; v[32 + e] = t1[e]; }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(b_accfree + slot));
+                const int t = ui.c * Q + i;
+                if (i < Q && t < L) {
+                    const float dh = D ? D[ui.h] : 0.f;
+                    const uint8_t* xr = st + i * kRowBytes;
+                    __nv_bfloat16* yr = y + ((int64_t)(ui.b * L + t) * H + ui.h) * P;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        if (ch * 8 < P) {
+                            const uint4 xv = *reinterpret_cast<const uint4*>(xr + ((ch ^ (i & 7)) << 4));
+                            uint4 ov;
+                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                            uint32_t ow[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int p0 = ch * 8 + 2 * e;
+                                ow[e] = pack_bf16(__uint_as_float(v[p0]) + dh * bf16lo(xw[e]),
+                                                  __uint_as_float(v[p0 + 1]) + dh * bf16hi(xw[e]));
+                            }
+                            ov.x = ow[0]; ov.y = ow[1]; ov.z = ow[2]; ov.w = ow[3];
+                            *reinterpret_cast<uint4*>(yr + ch * 8) = ov;
+                        }
+                    }
+                }
+            }
+            mbar_arrive(smem_u32(b_empty + s));
+            js += Cfg::kBlocks;
+            ++sc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int Q>
+cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void* C,
+                     const float* Gcs, const float* dtT, const void* hid, const float* D, void* y,
+                     cudaStream_t stream) {
+    using Cfg = CoCfg<Q>;
+    CUtensorMap tx, tc, tb, th;
+    const uint64_t xd[4] = {(uint64_t)p.P, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
+    const uint64_t xs[3] = {(uint64_t)p.P * 2, (uint64_t)p.H * p.P * 2,
+                            (uint64_t)p.L * p.H * p.P * 2};
+    const uint64_t bd[4] = {(uint64_t)p.N, (uint64_t)p.G, (uint64_t)p.L, (uint64_t)p.b};
+    const uint64_t bs[3] = {(uint64_t)p.N * 2, (uint64_t)p.G * p.N * 2,
+                            (uint64_t)p.L * p.G * p.N * 2};
+    const uint64_t hd[4] = {(uint64_t)p.N, (uint64_t)p.P, (uint64_t)(p.b * p.H * p.nc), 1};
+    const uint64_t hs[3] = {(uint64_t)p.N * 2, (uint64_t)p.P * p.N * 2,
+                            (uint64_t)(p.b * p.H * p.nc) * p.P * p.N * 2};
+    const uint32_t box_x[4] = {64, 1, (uint32_t)Q, 1};
+    const uint32_t box_b[4] = {64, 1, (uint32_t)Cfg::kBRows, 1};
+    const uint32_t box_h[4] = {64, 64, 1, 1};
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!encode_tmap_4d(&tx, bf, x, xd, xs, box_x, sw) ||
+        !encode_tmap_4d(&tc, bf, C, bd, bs, box_x, sw) ||
+        !encode_tmap_4d(&tb, bf, B, bd, bs, box_b, sw) ||
+        !encode_tmap_4d(&th, bf, hid, hd, hs, box_h, sw))
+        return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    auto kern = compute_out_tc<Q>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t units = p.b * p.nc * p.H;
+    const int grid = (int)(units < sms ? units : sms);
+    kern<<<grid, kThreads, Cfg::kSmem, stream>>>(tx, tc, tb, th, Gcs, dtT, D, (__nv_bfloat16*)y,
+                                                 (int)p.L, (int)p.H, (int)p.P, (int)p.nc,
+                                                 (int)p.Lp, (int)p.hpg, (int)units);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool compute_out_tc_supports(const Problem& p) {
+    return p.dtype == SSD_BF16 && p.P <= 64 && p.N <= 128 && p.b * p.nc * p.H < (1LL << 31);
+}
+
+cudaError_t launch_compute_out_tc(const Problem& p, const void* x, const void* B, const void* C,
+                                  const float* Gcs, const float* dtT, const void* hiddens,
+                                  const float* D, void* y, cudaStream_t stream) {
+    switch (p.Q) {
+        case 64: return launch_q<64>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+        case 128: return launch_q<128>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+        default: return launch_q<256>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+    }
+}
+
+unsigned int take_compute_out_error() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_co_error, sizeof(v)) != cudaSuccess) return ~0u;
+    cudaMemcpyToSymbol(g_co_error, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace ssd

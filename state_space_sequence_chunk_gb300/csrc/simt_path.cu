@@ -256,6 +256,8 @@ cudaError_t launch_fwd_pass_state(const Problem& p, const void* x, const void* B
 cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, const void* C,
                                const float* Gcs, const float* dtT, const void* hiddens,
                                const float* D, void* y, cudaStream_t stream) {
+    if (compute_out_tc_supports(p))
+        return launch_compute_out_tc(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
     if (p.dtype == SSD_BF16)
         return launch_co<__nv_bfloat16>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
     return launch_co<float>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);

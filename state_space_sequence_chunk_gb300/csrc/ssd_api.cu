@@ -82,6 +82,16 @@ extern "C" {
 
 int ssd_abi_version(void) { return SSD_ABI_VERSION; }
 
+unsigned int ssd_take_device_errors(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return ~0u;
+    }
+    const unsigned int a = take_fwd_pass_state_error(), b = take_compute_out_error();
+    if (a == ~0u || b == ~0u) return ~0u;
+    return (a ? 1u : 0u) | (b ? 2u : 0u);
+}
+
 const char* ssd_status_string(ssd_status s) {
     switch (s) {
         case SSD_OK: return "ok";

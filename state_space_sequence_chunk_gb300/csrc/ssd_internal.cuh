@@ -38,9 +38,14 @@ cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, c
 cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void* B,
                                      const float* Gcs, const float* dtT, const float* init,
                                      void* hiddens, float* final_state, cudaStream_t stream);
+bool compute_out_tc_supports(const Problem& p);
+cudaError_t launch_compute_out_tc(const Problem& p, const void* x, const void* B, const void* C,
+                                  const float* Gcs, const float* dtT, const void* hiddens,
+                                  const float* D, void* y, cudaStream_t stream);
 // Read and clear the device-side error word of a kernel module (bit 0: a
 // bounded wait gave up).  Synchronous.
 unsigned int take_fwd_pass_state_error();
+unsigned int take_compute_out_error();
 
 // Element loads/stores shared by the kernels.
 __device__ __forceinline__ float to_f32(float v) { return v; }

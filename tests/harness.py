@@ -48,6 +48,7 @@ def gpu_fwd(dev: dict, chunk: int, **kw):
     y, fin = ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
                          dev["init_state"], chunk_size=chunk, **kw)
     torch.cuda.synchronize()
+    assert ssd.ssd_take_device_errors() == 0, "a bounded wait in a kernel gave up"
     return y.float().cpu().numpy(), (None if fin is None else fin.cpu().numpy())
 
 
