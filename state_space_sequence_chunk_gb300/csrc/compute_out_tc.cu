@@ -64,7 +64,7 @@ struct CoCfg {
     static constexpr int kStages = Q > 128 ? 3 : 4;
     static constexpr int kBSlots = Q > 128 ? 2 : 1;         // stage slots a B tile occupies
     static constexpr int kBAtomBytes = kBRows * kRowBytes;
-    static constexpr int kBarBytes = 512;
+    static constexpr int kBarBytes = 2048;  // barriers, TMEM holder, v_j tables
     static constexpr int kSmem = kCBufs * kCBytes + kStages * kStageBytes + kBarBytes + 1024;
     // TMEM columns (512 allocated)
     // layout, Q = 256: [0,192) CB blocks (0,0) (1,0) (1,1); [192,256) A slot 0;
@@ -85,6 +85,17 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&t);
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t v) {
+    return *reinterpret_cast<__nv_bfloat162*>(&v);
+}
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) {
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+// Barrier among `n` threads (a multiple of 32) on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // The units of a CTA: [u0, u1) of the list ordered (batch, chunk, head).
@@ -133,6 +144,8 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     uint64_t* b_scaled = b_aready + 2;       // [2]    slot: acc row-scaled (128 arrivals)
     uint64_t* b_accfree = b_scaled + 2;      // [2]    slot: acc read by the epilogue (128)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(b_accfree + 2);
+    // per-warpgroup, per-head-parity tables of the column factors v_j (bf16)
+    __nv_bfloat16* vtab = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(bars) + 512);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u0 = (int)((int64_t)blockIdx.x * units / gridDim.x);
@@ -152,7 +165,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             mbar_init(smem_u32(b_cbconv + s), kSimtThreads);
             mbar_init(smem_u32(b_sdone + s), 1);
             mbar_init(smem_u32(b_ddone + s), 1);
-            mbar_init(smem_u32(b_aready + s), 128);
+            mbar_init(smem_u32(b_aready + s), (Q > 128 && s == 1) ? 256 : 128);
             mbar_init(smem_u32(b_scaled + s), 128);
             mbar_init(smem_u32(b_accfree + s), 128);
         }
@@ -382,40 +395,79 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             if (I >= 0) {
                 const int i = I * 128 + row;               // query row in the chunk
                 const float gi_ = (i < Q) ? gv[i] : 0.f;
-                const uint32_t abase = tmem + lane_off + (slot ? Cfg::kA1 : Cfg::kA0);
                 const uint32_t acc = tmem + lane_off + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
-                // ---- build A_I: key columns j in [0, K_I) ----
-                const int KI = Q > 128 ? (I + 1) * 128 : Q;
-                for (int j0 = 0; j0 < KI; j0 += 32) {
-                    const int J = j0 / 128, jl0 = j0 % 128;
-                    uint32_t o[16];
-                    if (J == I && jl0 > row) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] = 0u;
-                    } else {
-                        // packed C B^T block (I, J): Q=256 blocks at 0 (0,0), 64 (1,0), 128 (1,1)
-                        const uint32_t blk = Q > 128 ? (I == 0 ? 0u : (J == 0 ? 64u : 128u)) : 0u;
-                        uint32_t v[16];
-                        tmem_ld_x16(tmem + lane_off + cbsrc + blk + jl0 / 2, v);
-                        tmem_wait_ld();
-                        const bool diag = (J == I);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int ja = j0 + 2 * e, jb = ja + 1;
-                            const float wa = exp2f(gi_ - gv[ja]) * dv[ja];
-                            const float wb = exp2f(gi_ - gv[jb]) * dv[jb];
-                            float va = bf16lo(v[e]) * wa, vb = bf16hi(v[e]) * wb;
-                            if (diag) {
-                                va = (jl0 + 2 * e <= row) ? va : 0.f;
-                                vb = (jl0 + 2 * e + 1 <= row) ? vb : 0.f;
-                            }
-                            o[e] = pack_bf16(va, vb);
-                        }
-                    }
-                    tmem_st_x16(abase + j0 / 2, o);
+                // ---- column factors v_j = 2^{g_e - g_j} dt_j, e = end of j's 32-key chunk,
+                //      for this warpgroup's keys [kv0, kv0 + nv) ----
+                const int kv0 = (Q > 128 && wg == 1) ? 128 : 0;
+                const int nv = Q > 128 ? 128 : Q;
+                __nv_bfloat16* vb = vtab + (wg * 2 + (use & 1)) * 128;
+                if (row < nv) {
+                    const int j = kv0 + row;
+                    vb[row] = __float2bfloat16_rn(exp2f(gv[j | 31] - gv[j]) * dv[j]);
                 }
-                tmem_wait_st();
-                tc_fence_before();
+                named_bar_sync(1 + wg, 128);
+                const uint32_t* vb32 = reinterpret_cast<const uint32_t*>(vb);
+                // ---- build A: keys [kb, ke) of query block Ib into A columns key/2 ----
+                auto build = [&](int Ib, int kb, int ke, uint32_t abase) {
+                    const int ib = Ib * 128 + row;
+                    const float gib = (ib < Q) ? gv[ib] : 0.f;
+                    const int dch = ib >> 5;              // key chunk holding the diagonal
+                    for (int k0 = kb; k0 < ke; k0 += 64) {
+                        uint32_t o[32];
+                        const int kc0 = k0 >> 5;
+                        if (kc0 > dch) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = 0u;
+                        } else {
+                            const int J = k0 >> 7, jl0 = k0 & 127;
+                            const uint32_t blk =
+                                Q > 128 ? (Ib == 0 ? 0u : (J == 0 ? 64u : 128u)) : 0u;
+                            uint32_t cbv[32];
+                            tmem_ld_x32(tmem + lane_off + cbsrc + blk + jl0 / 2, cbv);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const int kc = kc0 + hf, jb = k0 + 32 * hf;
+                                if (kc < dch) {
+                                    // whole chunk at or below the row: factorised decay,
+                                    // 2^{g_i - g_j} = 2^{g_i - g_e} 2^{g_e - g_j}, both <= 1
+                                    const float u = exp2f(gib - gv[jb + 31]);
+                                    const __nv_bfloat162 u2 = __floats2bfloat162_rn(u, u);
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) {
+                                        const __nv_bfloat162 c2 = as_bf162(cbv[16 * hf + e]);
+                                        const __nv_bfloat162 v2 = as_bf162(vb32[(jb - kv0) / 2 + e]);
+                                        o[16 * hf + e] = as_u32(__hmul2(__hmul2(c2, v2), u2));
+                                    }
+                                } else if (kc == dch) {
+                                    // diagonal chunk: exact exponent, masked by a select
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) {
+                                        const int ja = jb + 2 * e, jc = ja + 1;
+                                        const float wa = exp2f(gib - gv[ja]) * dv[ja];
+                                        const float wc = exp2f(gib - gv[jc]) * dv[jc];
+                                        const float va = (ja <= ib) ? bf16lo(cbv[16 * hf + e]) * wa : 0.f;
+                                        const float vc = (jc <= ib) ? bf16hi(cbv[16 * hf + e]) * wc : 0.f;
+                                        o[16 * hf + e] = pack_bf16(va, vc);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) o[16 * hf + e] = 0u;
+                                }
+                            }
+                        }
+                        tmem_st_x32(abase + k0 / 2, o);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                };
+                const uint32_t a_own = tmem + lane_off + (slot ? Cfg::kA1 : Cfg::kA0);
+                if (Q > 128) {
+                    if (wg == 0) build(0, 0, 128, a_own);
+                    else build(1, 128, 256, a_own);
+                } else {
+                    build(0, 0, Q, a_own);
+                }
                 mbar_arrive(smem_u32(b_aready + slot));
                 // ---- acc *= 2^{g_i} ----
                 mbar_wait(smem_u32(b_sdone + slot), use & 1, err, 1u);
@@ -435,6 +487,14 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(b_scaled + slot));
+                if (Q > 128 && wg == 0) {
+                    // keys [0, 128) of query block 1 (all below its diagonal), into A slot 1;
+                    // the previous head's block-1 product must have finished reading it
+                    if (use > 0) mbar_wait(smem_u32(b_ddone + 1), (use - 1) & 1, err, 1u);
+                    tc_fence_after();
+                    build(1, 0, 128, tmem + lane_off + Cfg::kA1);
+                    mbar_arrive(smem_u32(b_aready + 1));
+                }
                 // ---- epilogue: y = acc + D x ----
                 mbar_wait(smem_u32(b_ddone + slot), use & 1, err, 1u);
                 tc_fence_after();

@@ -49,7 +49,9 @@ struct FpsCfg {
     static constexpr int kStages = PP == 64 ? 4 : 3;
     static constexpr int kXBytes = kSub * PP * 2;         // x sub-tile
     static constexpr int kBBytes = kSub * 128 * 2;        // B sub-tile (128 state rows)
-    static constexpr int kStageBytes = kXBytes + kBBytes;
+    static constexpr int kVecOff = kXBytes + kBBytes;     // g[64], dt[64], last 4 g of the chunk
+    static constexpr int kVecBytes = 2 * kSub * 4 + 16;
+    static constexpr int kStageBytes = (kVecOff + kVecBytes + 1023) / 1024 * 1024;
     static constexpr int kTmemCols = 2 * PP;              // two accumulators
     static constexpr int kBarBytes = 256;
     static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
@@ -117,7 +119,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 const uint32_t xs = stage0 + s * Cfg::kStageBytes, bs = xs + Cfg::kXBytes;
                 const int c = i / nsub, sub = i % nsub;
                 const int t = c * Q + sub * kSub;
-                mbar_arrive_expect_tx(full(s), Cfg::kStageBytes);
+                mbar_arrive_expect_tx(full(s), Cfg::kXBytes + Cfg::kBBytes + Cfg::kVecBytes);
 #pragma unroll
                 for (int j = 0; j < PP / 64; ++j)
                     tma_load_4d(xs + j * kSub * kRowBytes, &tm_x, full(s), j * 64, h, t, b);
@@ -125,6 +127,11 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 for (int j = 0; j < 2; ++j)
                     tma_load_4d(bs + j * kSub * kRowBytes, &tm_b, full(s), mb * 128 + j * 64, grp,
                                 t, b);
+                const int64_t ro = (int64_t)bh * Lp;
+                const uint32_t vs = xs + Cfg::kVecOff;
+                bulk_load(vs, Gcs + ro + t, kSub * 4, full(s));
+                bulk_load(vs + kSub * 4, dtT + ro + t, kSub * 4, full(s));
+                bulk_load(vs + 2 * kSub * 4, Gcs + ro + (int64_t)c * Q + Q - 4, 16, full(s));
             }
         }
     } else if (warp == 1) {
@@ -156,17 +163,15 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         }
     } else if (warp == 2) {
         // ---------------- row scaler: x_q <- x_q * dt_q 2^{g_last - g_q} ----------------
-        const float* grow = Gcs + (int64_t)bh * Lp;
-        const float* drow = dtT + (int64_t)bh * Lp;
         for (int i = 0; i < total; ++i) {
             const int s = i % S, k = i / S;
-            const int c = i / nsub, sub = i % nsub;
-            const int t = c * Q + sub * kSub;
-            const float glast = grow[c * Q + Q - 1];
-            const float s0 = drow[t + lane] * exp2f(glast - grow[t + lane]);
-            const float s1 = drow[t + lane + 32] * exp2f(glast - grow[t + lane + 32]);
             mbar_wait(full(s), k & 1, &g_fps_error, 1u);
             uint8_t* xs = smem + s * Cfg::kStageBytes;
+            const float* gv = reinterpret_cast<const float*>(xs + Cfg::kVecOff);
+            const float* dv = gv + kSub;
+            const float glast = gv[2 * kSub + 3];
+            const float s0 = dv[lane] * exp2f(glast - gv[lane]);
+            const float s1 = dv[lane + 32] * exp2f(glast - gv[lane + 32]);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int r = lane + 32 * half;
@@ -200,14 +205,17 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         for (int p = 0; p < PP; ++p)
             Sr[p] = (init != nullptr && nok && p < P) ? init[sbase + (int64_t)p * N + n] : 0.f;
         const float* grow = Gcs + (int64_t)bh * Lp;
+        float gl_next = grow[Q - 1];  // g_last of the next chunk, loaded one chunk ahead
         for (int c = 0; c < nc; ++c) {
+            const float gl = gl_next;
+            if (c + 1 < nc) gl_next = grow[(int64_t)(c + 1) * Q + Q - 1];
             if (nok) {
                 __nv_bfloat16* hp = hiddens + ((int64_t)bh * nc + c) * P * N + n;
 #pragma unroll
                 for (int p = 0; p < PP; ++p)
                     if (p < P) hp[(int64_t)p * N] = __float2bfloat16_rn(Sr[p]);
             }
-            const float e = exp2f(grow[c * Q + Q - 1]);
+            const float e = exp2f(gl);
             const int acc = c & 1, use = c >> 1;
             mbar_wait(acc_full(acc), use & 1, &g_fps_error, 1u);
             tc_fence_after();
