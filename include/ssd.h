@@ -29,8 +29,10 @@
  *    Intermediates (chunk_cumsum / fwd_pass_state outputs):
  *              Gcs, dtT [b, H, Lp] (fp32; token-contiguous, padded to Lp;
  *                  Gcs is pre-scaled by log2(e); padded tokens carry dt = 0)
- *              hiddens [b, H, nc, P, N] (dims.dtype): the state before each
- *                  chunk's first token.
+ *              hiddens [b, H, nc, N, P] (dims.dtype): the state before each
+ *                  chunk's first token, stored transposed (row n holds the P
+ *                  values S[:, n]), the layout in which both the producing and
+ *                  the consuming kernel move whole contiguous rows.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *    asynchronous on that stream: no host synchronisation inside.
  *  - Errors: all arguments are validated on the host BEFORE anything is
@@ -124,7 +126,7 @@ ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A,
 /*
  * ssd_fwd_pass_state -- step 2 ("Kernel 2: fwd_pass_state").
  * For every (b, h), walking the chunks in order from S = init_state (or 0):
- *   hiddens[b, h, c] = S                                  (in dims.dtype)
+ *   hiddens[b, h, c] = S^T                                (in dims.dtype)
  *   S <- 2^{g_last} S + X_c^T (B_c o (dt_c 2^{g_last - g_c}))
  * where g = Gcs of chunk c and g_last its value at the chunk's last real token.
  * final_state (fp32, may be NULL, may equal init_state) receives the last S.

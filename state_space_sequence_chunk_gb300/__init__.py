@@ -180,13 +180,14 @@ def ssd_chunk_cumsum(dt, A, chunk_size: int, x_dtype=torch.bfloat16):
 
 def ssd_fwd_pass_state(x, B, Gcs, dtT, init_state=None, chunk_size: int = 256,
                        return_final_state: bool = True):
-    """Step 2: returns ``(hiddens [b, H, nc, P, N] in x.dtype, final_state)``."""
+    """Step 2: returns ``(hiddens [b, H, nc, N, P] in x.dtype, final_state)``;
+    hiddens[b, h, c] is the chunk-start state transposed."""
     lib = load_library()
     dims = dims_for(x, B, chunk_size)
     b, L, H, P = x.shape
     N = B.shape[3]
     nc = (L + chunk_size - 1) // chunk_size
-    hid = torch.empty((b, H, nc, P, N), dtype=x.dtype, device=x.device)
+    hid = torch.empty((b, H, nc, N, P), dtype=x.dtype, device=x.device)
     fin = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device) if return_final_state else None
     _check(lib.ssd_fwd_pass_state(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(Gcs), _ptr(dtT),
                                   _ptr(init_state), _ptr(hid), _ptr(fin), _stream()))

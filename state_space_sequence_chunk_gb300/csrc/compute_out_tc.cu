@@ -57,8 +57,7 @@ struct CoCfg {
     static constexpr int kCBytes = kNAtoms * kCAtomBytes;
     static constexpr int kCBufs = Q > 128 ? 1 : 2;
     static constexpr int kXBytes = Q * kRowBytes;           // x tile, P padded to 64
-    static constexpr int kHAtomBytes = 64 * kRowBytes;      // 64 rows of P x 64 of N
-    static constexpr int kHBytes = kNAtoms * kHAtomBytes;
+    static constexpr int kHBytes = 128 * kRowBytes;         // h^T: 128 rows of N x 64 of P
     static constexpr int kVecBytes = Q * 4;
     static constexpr int kStageBytes = ((kXBytes + kHBytes + 2 * kVecBytes) + 1023) / 1024 * 1024;
     static constexpr int kStages = Q > 128 ? 3 : 4;
@@ -223,9 +222,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 mbar_arrive_expect_tx(fb, Cfg::kXBytes + Cfg::kHBytes + 2 * Cfg::kVecBytes);
                 tma_load_4d(smem_u32(st), &tm_x, fb, 0, ui.h, ui.c * Q, ui.b);
                 const int bh = ui.b * H + ui.h;
-                for (int a = 0; a < Cfg::kNAtoms; ++a)
-                    tma_load_4d(smem_u32(st + Cfg::kXBytes + a * Cfg::kHAtomBytes), &tm_h, fb,
-                                a * 64, 0, bh * nc + ui.c, 0);
+                tma_load_4d(smem_u32(st + Cfg::kXBytes), &tm_h, fb, 0, 0, bh * nc + ui.c, 0);
                 const int64_t vo = (int64_t)bh * Lp + (int64_t)ui.c * Q;
                 bulk_load(smem_u32(st + Cfg::kXBytes + Cfg::kHBytes), Gcs + vo, Cfg::kVecBytes, fb);
                 bulk_load(smem_u32(st + Cfg::kXBytes + Cfg::kHBytes + Cfg::kVecBytes), dtT + vo,
@@ -237,7 +234,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // ===================== MMA issuer =====================
         if (lane == 0) {
             constexpr uint32_t kIdescCB = make_idesc(1, 128, Cfg::kBRows, 0, 0);
-            constexpr uint32_t kIdescS = make_idesc(1, 128, 64, 0, 0);
+            constexpr uint32_t kIdescS = make_idesc(1, 128, 64, 0, 1);  // B = h, MN-major
             constexpr uint32_t kIdescD = make_idesc(1, 128, 64, 0, 1);
             int sc = 0, gi = -1, js = 0;  // stage, group, slot-job counters
             int cbq = 0;                  // C buffer of the current group
@@ -303,9 +300,9 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         const uint64_t ad = smem_desc_sw128(
                             cbase + (kk / 4) * Cfg::kCAtomBytes + I * 128 * kRowBytes + (kk % 4) * 32,
                             16, 8 * kRowBytes);
-                        const uint64_t bd = smem_desc_sw128(
-                            st + Cfg::kXBytes + (kk / 4) * Cfg::kHAtomBytes + (kk % 4) * 32, 16,
-                            8 * kRowBytes);
+                        // B = h^T tile [n][p]: MN-major (p contiguous), K = 16 state rows
+                        const uint64_t bd = smem_desc_sw128(st + Cfg::kXBytes + kk * 16 * kRowBytes,
+                                                            8 * kRowBytes, 8 * kRowBytes);
                         mma_f16_ss(acc, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(smem_u32(b_sdone + slot));
@@ -339,6 +336,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         int sc = 0, gi = -1, js = 0;
         for (int u = u0; u < u1; ++u) {
+            __syncwarp();  // the previous unit's per-row stores may have diverged
             const UnitInfo ui = unit_info(u, nc, H, hpg);
             if (new_group(u, u0, H, hpg)) {
                 ++gi;
@@ -358,6 +356,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         dcol = (Q > 128 ? 128 : 0) + c0 / 2;
                     }
                     for (int cc = 0; cc < ncol; cc += 32) {
+                        __syncwarp();
                         uint32_t v[32], o[16];
                         tmem_ld_x32(tmem + lane_off + Cfg::kScratch + q * 128 + c0 + cc, v);
                         tmem_wait_ld();
@@ -413,6 +412,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const float gib = (ib < Q) ? gv[ib] : 0.f;
                     const int dch = ib >> 5;              // key chunk holding the diagonal
                     for (int k0 = kb; k0 < ke; k0 += 64) {
+                        __syncwarp();  // warp-collective TMEM access below
                         uint32_t o[32];
                         const int kc0 = k0 >> 5;
                         if (kc0 > dch) {
@@ -477,6 +477,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     uint32_t v[32];
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
+                        __syncwarp();
                         tmem_ld_x32(acc + h2 * 32, v);
                         tmem_wait_ld();
 #pragma unroll
@@ -501,6 +502,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 uint32_t v[64];
                 {
                     uint32_t t0[32], t1[32];
+                    __syncwarp();
                     tmem_ld_x32(acc, t0);
                     tmem_ld_x32(acc + 32, t1);
                     tmem_wait_ld();
@@ -541,6 +543,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -558,12 +561,12 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     const uint64_t bd[4] = {(uint64_t)p.N, (uint64_t)p.G, (uint64_t)p.L, (uint64_t)p.b};
     const uint64_t bs[3] = {(uint64_t)p.N * 2, (uint64_t)p.G * p.N * 2,
                             (uint64_t)p.L * p.G * p.N * 2};
-    const uint64_t hd[4] = {(uint64_t)p.N, (uint64_t)p.P, (uint64_t)(p.b * p.H * p.nc), 1};
-    const uint64_t hs[3] = {(uint64_t)p.N * 2, (uint64_t)p.P * p.N * 2,
-                            (uint64_t)(p.b * p.H * p.nc) * p.P * p.N * 2};
+    const uint64_t hd[4] = {(uint64_t)p.P, (uint64_t)p.N, (uint64_t)(p.b * p.H * p.nc), 1};
+    const uint64_t hs[3] = {(uint64_t)p.P * 2, (uint64_t)p.N * p.P * 2,
+                            (uint64_t)(p.b * p.H * p.nc) * p.N * p.P * 2};
     const uint32_t box_x[4] = {64, 1, (uint32_t)Q, 1};
     const uint32_t box_b[4] = {64, 1, (uint32_t)Cfg::kBRows, 1};
-    const uint32_t box_h[4] = {64, 64, 1, 1};
+    const uint32_t box_h[4] = {64, 128, 1, 1};
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
     if (!encode_tmap_4d(&tx, bf, x, xd, xs, box_x, sw) ||

@@ -14,17 +14,20 @@
 //    rendering, "Mamba-2性能优化" (swapping the A/B operands), describes the same
 //    B^T A^T = (A B)^T swap for Blackwell.
 //  * Every chunk's product D_c = B_c^T (s o X_c) goes into a FRESH TMEM
-//    accumulator (two, used alternately), and the epilogue warps fold it into
-//    the running state held in registers, S <- 2^{g_last} S + D_c.  The
-//    tensor core never waits for the previous chunk's state: only the cheap
-//    register update is serial.
-//  * x and B stream in 64-token sub-chunks through a multi-stage TMA ring
+//    accumulator, and the epilogue warps fold it into the running state kept
+//    in a second TMEM region, S <- 2^{g_last} S + D_c.  The tensor core never
+//    waits for the previous chunk's state, only for the epilogue to have read
+//    the accumulator; keeping S in TMEM keeps registers low enough for four
+//    CTAs per SM, so that a full batch*head grid is resident at once.
+//  * x and B stream in 32-token sub-chunks through a multi-stage TMA ring
 //    (128-byte swizzle, token-major rows, read as MN-major operands).  The
 //    per-token scale s_q = dt_q 2^{g_last - g_q} is applied to the x rows in
-//    shared memory by one warp (a row is contiguous in the swizzled tile).
+//    shared memory (a row is contiguous in the swizzled tile).
 //
-// Warp roles (224 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
-// 2 row scaler, 3..6 epilogue (TMEM lane quarter = warp % 4).
+// Warp roles (192 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
+// 2..5 state warps (row scaling of every stage, and the state update at each
+// chunk boundary; TMEM lane quarter = warp % 4).  TMEM: columns
+// [0, PP) accumulator, [PP, 2 PP) state S^T (lane = state row n, column = p).
 //
 // CTA = (128-row block of N, batch * head).  N and P are padded to the
 // 64-element swizzle atom by the TMA's zero fill; padded rows/columns are
@@ -40,19 +43,20 @@ namespace {
 
 __device__ unsigned int g_fps_error;  // bit 0: a bounded wait gave up
 
-constexpr int kSub = 64;            // tokens per pipeline stage
+constexpr int kSub = 32;            // tokens per pipeline stage
 constexpr int kRowBytes = 128;      // one swizzle row (64 bf16)
-constexpr int kThreads = 224;
+constexpr int kThreads = 192;
 
 template <int PP>
 struct FpsCfg {
-    static constexpr int kStages = PP == 64 ? 4 : 3;
+    static constexpr int kStages = 5;
+    static constexpr int kMinBlocks = PP == 64 ? 3 : 2;   // CTAs per SM (TMEM: 2*PP each)
     static constexpr int kXBytes = kSub * PP * 2;         // x sub-tile
     static constexpr int kBBytes = kSub * 128 * 2;        // B sub-tile (128 state rows)
-    static constexpr int kVecOff = kXBytes + kBBytes;     // g[64], dt[64], last 4 g of the chunk
+    static constexpr int kVecOff = kXBytes + kBBytes;     // g[kSub], dt[kSub], last 4 g of the chunk
     static constexpr int kVecBytes = 2 * kSub * 4 + 16;
     static constexpr int kStageBytes = (kVecOff + kVecBytes + 1023) / 1024 * 1024;
-    static constexpr int kTmemCols = 2 * PP;              // two accumulators
+    static constexpr int kTmemCols = 2 * PP;              // accumulator + state
     static constexpr int kBarBytes = 256;
     static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
     static constexpr uint32_t kIdesc = make_idesc(1, 128, PP, 1, 1);
@@ -64,9 +68,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&t);
 }
+__device__ __forceinline__ uint32_t mul_bf162(uint32_t a, __nv_bfloat162 b) {
+    __nv_bfloat162 t = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), b);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
 
 template <int PP>
-__global__ void __launch_bounds__(kThreads, PP == 64 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, FpsCfg<PP>::kMinBlocks)
 fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                   const float* __restrict__ Gcs, const float* __restrict__ dtT, const float* init,
                   __nv_bfloat16* __restrict__ hiddens, float* final_state, int H, int P, int N,
@@ -81,9 +89,9 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto scaled = [&](int s) { return smem_u32(bars + S + s); };
     auto empty = [&](int s) { return smem_u32(bars + 2 * S + s); };
-    auto acc_full = [&](int j) { return smem_u32(bars + 3 * S + j); };
-    auto acc_empty = [&](int j) { return smem_u32(bars + 3 * S + 2 + j); };
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 4);
+    const uint32_t acc_full = smem_u32(bars + 3 * S);
+    const uint32_t acc_empty = smem_u32(bars + 3 * S + 1);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 2);
 
     const int mb = blockIdx.x, bh = blockIdx.y;
     const int b = bh / H, h = bh % H, grp = h / hpg;
@@ -94,13 +102,11 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(scaled(s), 32);
+            mbar_init(scaled(s), 128);
             mbar_init(empty(s), 1);
         }
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(acc_full(j), 1);
-            mbar_init(acc_empty(j), 128);
-        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 128);
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
@@ -140,8 +146,8 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             for (int i = 0; i < total; ++i) {
                 const int s = i % S, k = i / S;
                 const int c = i / nsub, sub = i % nsub;
-                const int acc = c & 1, use = c >> 1;
-                if (sub == 0) mbar_wait(acc_empty(acc), (use & 1) ^ 1, &g_fps_error, 1u);
+                // the epilogue has read the previous chunk's product
+                if (sub == 0) mbar_wait(acc_empty, (c & 1) ^ 1, &g_fps_error, 1u);
                 mbar_wait(scaled(s), k & 1, &g_fps_error, 1u);
                 tc_fence_after();
                 const uint32_t xs = stage0 + s * Cfg::kStageBytes, bs = xs + Cfg::kXBytes;
@@ -154,91 +160,132 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     // B = s o X_c: N = PP columns of P, K = 16 tokens, MN-major.
                     const uint64_t bdesc = smem_desc_sw128(xs + kk * 16 * kRowBytes,
                                                            kSub * kRowBytes, 8 * kRowBytes);
-                    mma_f16_ss(tmem + acc * PP, adesc, bdesc, Cfg::kIdesc,
-                               (sub > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_ss(tmem, adesc, bdesc, Cfg::kIdesc, (sub > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(empty(s));
-                if (sub == nsub - 1) mma_commit(acc_full(acc));
+                if (sub == nsub - 1) mma_commit(acc_full);
             }
         }
-    } else if (warp == 2) {
-        // ---------------- row scaler: x_q <- x_q * dt_q 2^{g_last - g_q} ----------------
+    } else {
+        // ---------------- state warps (2..5): row scaling and the state update ----------------
+        // Each thread owns TMEM lane (state row n) 32*(warp%4) + lane.  The warps
+        // scale every stage's x rows (128 threads, two 16-byte vectors each) and,
+        // at each chunk boundary, fold the finished chunk product into S.
+        const int quarter = warp & 3;
+        const int tid = threadIdx.x - 64;  // 0..127
+        const int n = mb * 128 + quarter * 32 + lane;
+        const bool nok = n < N;
+        const uint32_t acc_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t st_addr = acc_addr + PP;
+        const int64_t sbase = (int64_t)bh * P * N;
+        // S^T row n <- init_state[b, h, :, n] (or 0)
+#pragma unroll
+        for (int j = 0; j < PP / 16; ++j) {
+            __syncwarp();
+            uint32_t r[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int p = 16 * j + q;
+                r[q] = __float_as_uint((init != nullptr && nok && p < P)
+                                           ? init[sbase + (int64_t)p * N + n] : 0.f);
+            }
+            tmem_st_x16(st_addr + 16 * j, r);
+        }
+        tmem_wait_st();
+        const float* grow = Gcs + (int64_t)bh * Lp;
+        // S <- 2^{g_last(c)} S + D_c, storing the chunk-start S^T to hiddens[c]
+        auto chunk_update = [&](int c, float gl) {
+            const float e = exp2f(gl);
+            // hiddens[b, h, c] is stored transposed: row n holds S[:, n] (P values)
+            __nv_bfloat16* hp = hiddens + (((int64_t)bh * nc + c) * N + n) * P;
+            mbar_wait(acc_full, c & 1, &g_fps_error, 1u);
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < PP / 16; ++j) {
+                // tcgen05.ld/st are warp-collective: every lane runs them, and the
+                // warp is reconverged after the per-lane stores below
+                __syncwarp();
+                uint32_t d[16], sv[16];
+                tmem_ld_x16(acc_addr + 16 * j, d);
+                tmem_ld_x16(st_addr + 16 * j, sv);
+                tmem_wait_ld();
+                uint32_t nw[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    nw[q] = __float_as_uint(fmaf(e, __uint_as_float(sv[q]), __uint_as_float(d[q])));
+                tmem_st_x16(st_addr + 16 * j, nw);
+                // chunk-start state (before this chunk's update) -> hiddens[c]:
+                // 16 contiguous bf16 of row n per slice (P is a multiple of 16)
+                if (nok && 16 * j < P) {
+                    uint4 w0, w1;
+                    w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
+                    w0.y = pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3]));
+                    w0.z = pack_bf16(__uint_as_float(sv[4]), __uint_as_float(sv[5]));
+                    w0.w = pack_bf16(__uint_as_float(sv[6]), __uint_as_float(sv[7]));
+                    w1.x = pack_bf16(__uint_as_float(sv[8]), __uint_as_float(sv[9]));
+                    w1.y = pack_bf16(__uint_as_float(sv[10]), __uint_as_float(sv[11]));
+                    w1.z = pack_bf16(__uint_as_float(sv[12]), __uint_as_float(sv[13]));
+                    w1.w = pack_bf16(__uint_as_float(sv[14]), __uint_as_float(sv[15]));
+                    uint4* dst = reinterpret_cast<uint4*>(hp + 16 * j);
+                    dst[0] = w0;
+                    dst[1] = w1;
+                }
+            }
+            __syncwarp();
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+        };
+        float gl_prev = 0.f;
         for (int i = 0; i < total; ++i) {
             const int s = i % S, k = i / S;
+            const int c = i / nsub, sub = i % nsub;
+            if (sub == 0 && c > 0) chunk_update(c - 1, gl_prev);
+            // ---- row scaling of stage i: x_q <- x_q * dt_q 2^{g_last - g_q} ----
             mbar_wait(full(s), k & 1, &g_fps_error, 1u);
             uint8_t* xs = smem + s * Cfg::kStageBytes;
             const float* gv = reinterpret_cast<const float*>(xs + Cfg::kVecOff);
             const float* dv = gv + kSub;
             const float glast = gv[2 * kSub + 3];
-            const float s0 = dv[lane] * exp2f(glast - gv[lane]);
-            const float s1 = dv[lane + 32] * exp2f(glast - gv[lane + 32]);
+            if (sub == nsub - 1) gl_prev = glast;
+            constexpr int kVecs = kSub * (PP / 64) * 8;   // 16-byte vectors in the x sub-tile
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int r = lane + 32 * half;
-                const float sc = half ? s1 : s0;
-#pragma unroll
-                for (int j = 0; j < PP / 64; ++j) {
-                    uint4* row = reinterpret_cast<uint4*>(xs + j * kSub * kRowBytes + r * kRowBytes);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        uint4 v = row[q];
-                        v.x = pack_bf16(bf16lo(v.x) * sc, bf16hi(v.x) * sc);
-                        v.y = pack_bf16(bf16lo(v.y) * sc, bf16hi(v.y) * sc);
-                        v.z = pack_bf16(bf16lo(v.z) * sc, bf16hi(v.z) * sc);
-                        v.w = pack_bf16(bf16lo(v.w) * sc, bf16hi(v.w) * sc);
-                        row[q] = v;
-                    }
-                }
+            for (int v = tid; v < kVecs; v += 128) {
+                const int box = v / (kSub * 8), r = (v / 8) % kSub, q = v % 8;
+                // the row scale rounded to bf16 once, then packed bf16x2 products
+                const __nv_bfloat162 s2 = __float2bfloat162_rn(dv[r] * exp2f(glast - gv[r]));
+                uint4* ptr = reinterpret_cast<uint4*>(xs + box * kSub * kRowBytes + r * kRowBytes) + q;
+                uint4 w = *ptr;
+                w.x = mul_bf162(w.x, s2);
+                w.y = mul_bf162(w.y, s2);
+                w.z = mul_bf162(w.z, s2);
+                w.w = mul_bf162(w.w, s2);
+                *ptr = w;
             }
             fence_proxy_async_smem();
             mbar_arrive(scaled(s));
         }
-    } else {
-        // ---------------- epilogue: the serial state update ----------------
-        const int quarter = warp & 3;
-        const int n = mb * 128 + quarter * 32 + lane;
-        const bool nok = n < N;
-        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        float Sr[PP];
-        const int64_t sbase = (int64_t)bh * P * N;
-#pragma unroll
-        for (int p = 0; p < PP; ++p)
-            Sr[p] = (init != nullptr && nok && p < P) ? init[sbase + (int64_t)p * N + n] : 0.f;
-        const float* grow = Gcs + (int64_t)bh * Lp;
-        float gl_next = grow[Q - 1];  // g_last of the next chunk, loaded one chunk ahead
-        for (int c = 0; c < nc; ++c) {
-            const float gl = gl_next;
-            if (c + 1 < nc) gl_next = grow[(int64_t)(c + 1) * Q + Q - 1];
-            if (nok) {
-                __nv_bfloat16* hp = hiddens + ((int64_t)bh * nc + c) * P * N + n;
-#pragma unroll
-                for (int p = 0; p < PP; ++p)
-                    if (p < P) hp[(int64_t)p * N] = __float2bfloat16_rn(Sr[p]);
-            }
-            const float e = exp2f(gl);
-            const int acc = c & 1, use = c >> 1;
-            mbar_wait(acc_full(acc), use & 1, &g_fps_error, 1u);
-            tc_fence_after();
+        if (nc > 0) chunk_update(nc - 1, gl_prev);
+        if (final_state != nullptr) {  // uniform: all lanes load, valid lanes store
 #pragma unroll
             for (int j = 0; j < PP / 16; ++j) {
-                uint32_t r[16];
-                tmem_ld_x16(lane_addr + acc * PP + 16 * j, r);
+                __syncwarp();
+                uint32_t sv[16];
+                tmem_ld_x16(st_addr + 16 * j, sv);
                 tmem_wait_ld();
+                if (nok) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) Sr[16 * j + q] = fmaf(e, Sr[16 * j + q], __uint_as_float(r[q]));
+                    for (int q = 0; q < 16; ++q)
+                        if (16 * j + q < P)
+                            final_state[sbase + (int64_t)(16 * j + q) * N + n] = __uint_as_float(sv[q]);
+                }
             }
-            tc_fence_before();
-            mbar_arrive(acc_empty(acc));
-        }
-        if (final_state != nullptr && nok) {
-#pragma unroll
-            for (int p = 0; p < PP; ++p)
-                if (p < P) final_state[sbase + (int64_t)p * N + n] = Sr[p];
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
     }

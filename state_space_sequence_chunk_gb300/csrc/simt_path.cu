@@ -49,10 +49,11 @@ fwd_pass_state_simt(const T* __restrict__ x, const T* __restrict__ B,
 
     for (int c = 0; c < nc; ++c) {
         // chunk-start state
-        T* hrow = hiddens + ((((int64_t)bidx * H + h) * nc + c) * P + p) * N;
+        // chunk-start state, stored transposed: hiddens[b, h, c, n, p]
+        T* hrow = hiddens + (((int64_t)bidx * H + h) * nc + c) * (int64_t)N * P + p;
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-            if (k < nper) hrow[nl + 16 * k] = from_f32<T>(S[k]);
+            if (k < nper) hrow[(int64_t)(nl + 16 * k) * P] = from_f32<T>(S[k]);
 
         const int t0 = c * Q;
         const float glast = grow[t0 + Q - 1];  // padded tokens repeat the last real value
@@ -147,7 +148,7 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
         __syncthreads();
         for (int i = tid; i < P * 32; i += kThreads) {
             const int pp = i / 32, nn = i % 32;
-            hs[pp * 33 + nn] = (n0 + nn < N) ? to_f32(hbase[(int64_t)pp * N + n0 + nn]) : 0.f;
+            hs[pp * 33 + nn] = (n0 + nn < N) ? to_f32(hbase[(int64_t)(n0 + nn) * P + pp]) : 0.f;
         }
         __syncthreads();
         const int nlim = min(32, N - n0);

@@ -53,23 +53,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for phase `parity` of the barrier to complete, giving up after about
 // `kWaitLimitCycles` SM cycles.  On giving up, bit `code` is set in *err and
-// false is returned, so that no wait in these kernels can hang the GPU.  Once
-// *err is non-zero every later wait gives up at once, so a broken schedule
-// ends the kernel quickly instead of timing out wait after wait.
+// false is returned, so that no wait in these kernels can hang the GPU.  The
+// fast path touches only the barrier and the SM clock; a wait that has lasted
+// longer than `kWaitSlowCycles` (far beyond any healthy pipeline handoff) also
+// polls *err, so that once one wait has given up every other wait in the
+// kernel ends within microseconds instead of timing out on its own.
 constexpr long long kWaitLimitCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr long long kWaitSlowCycles = 200000LL;       // ~100 us
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
                                           unsigned int code) {
     if (mbar_try_wait(bar, parity)) return true;
-    volatile unsigned int* verr = err;
-    if (*verr != 0u) return false;
     const long long t0 = clock64();
     unsigned int spins = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if ((++spins & 63u) == 0u) {
-            if (*verr != 0u) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
-                atomicOr(err, code);
-                return false;
+        if ((++spins & 15u) == 0u) {
+            const long long dt = clock64() - t0;
+            if (dt > kWaitSlowCycles) {
+                if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
+                if (dt > kWaitLimitCycles) {
+                    atomicOr(err, code);
+                    return false;
+                }
             }
         }
     }
