@@ -26,9 +26,10 @@
 //  * x, h, C, B and the per-token g, dt vectors arrive by TMA / bulk copies
 //    into a stage ring; B only passes through the ring once per group.
 //
-// Warp roles (384 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
-// 2-3 idle, 4-7 SIMT warpgroup 0 (slot 0), 8-11 SIMT warpgroup 1 (slot 1).
-// A SIMT thread owns TMEM lane (query row) 32*(warp%4) + lane.
+// Warp roles (640 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
+// 2-3 idle, 4-19 four SIMT warpgroups: warpgroup w serves TMEM slot (w & 1)
+// and half (w >> 1) of the key and output columns.  A SIMT thread owns TMEM
+// lane (query row) 32*(warp%4) + lane.
 //
 // Supported here: bf16, P <= 64, N <= 128, Q in {64, 128, 256}.
 #include <cuda.h>
@@ -42,10 +43,10 @@ namespace {
 
 __device__ unsigned int g_co_error;  // bit 0: a bounded wait gave up
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;
 constexpr int kRowBytes = 128;
 constexpr int kSimtWarp0 = 4;
-constexpr int kSimtThreads = 256;
+constexpr int kSimtThreads = 512;   // 16 SIMT warps
 
 template <int Q>
 struct CoCfg {
@@ -63,7 +64,7 @@ struct CoCfg {
     static constexpr int kStages = Q > 128 ? 3 : 4;
     static constexpr int kBSlots = Q > 128 ? 2 : 1;         // stage slots a B tile occupies
     static constexpr int kBAtomBytes = kBRows * kRowBytes;
-    static constexpr int kBarBytes = 2048;  // barriers, TMEM holder, v_j tables
+    static constexpr int kBarBytes = 3072;  // barriers, TMEM holder, v_j tables
     static constexpr int kSmem = kCBufs * kCBytes + kStages * kStageBytes + kBarBytes + 1024;
     // TMEM columns (512 allocated)
     // layout, Q = 256: [0,192) CB blocks (0,0) (1,0) (1,1); [192,256) A slot 0;
@@ -161,12 +162,12 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(b_cbfull + s), 1);
-            mbar_init(smem_u32(b_cbconv + s), kSimtThreads);
+            mbar_init(smem_u32(b_cbconv + s), 256);
             mbar_init(smem_u32(b_sdone + s), 1);
             mbar_init(smem_u32(b_ddone + s), 1);
-            mbar_init(smem_u32(b_aready + s), (Q > 128 && s == 1) ? 256 : 128);
-            mbar_init(smem_u32(b_scaled + s), 128);
-            mbar_init(smem_u32(b_accfree + s), 128);
+            mbar_init(smem_u32(b_aready + s), 256);
+            mbar_init(smem_u32(b_scaled + s), 256);
+            mbar_init(smem_u32(b_accfree + s), 256);
         }
         fence_mbar_init();
     }
@@ -331,8 +332,12 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
     } else if (warp >= kSimtWarp0) {
         // ===================== SIMT warpgroups =====================
-        const int wg = (warp - kSimtWarp0) >> 2;         // 0 or 1
-        const int row = (warp & 3) * 32 + lane;         // TMEM lane / query row in block
+        // Four warpgroups; warpgroup w serves TMEM slot / query block (w & 1) and
+        // half (w >> 1) of its key columns and output columns, so two threads
+        // share every query row and twice as many warps hide the latencies.
+        const int w = (warp - kSimtWarp0) >> 2;          // 0..3
+        const int sel = w & 1, half = w >> 1;
+        const int row = (warp & 3) * 32 + lane;          // TMEM lane / query row in block
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         int sc = 0, gi = -1, js = 0;
         for (int u = u0; u < u1; ++u) {
@@ -340,38 +345,40 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const UnitInfo ui = unit_info(u, nc, H, hpg);
             if (new_group(u, u0, H, hpg)) {
                 ++gi;
-                // convert C B^T (fp32 scratch) to packed bf16
                 const int rounds = Q > 128 ? 2 : 1;
-                const uint32_t cbdst = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
-                for (int r = 0; r < rounds; ++r) {
-                    mbar_wait(smem_u32(b_cbfull + r), gi & 1, err, 1u);
-                    tc_fence_after();
-                    // round 0 of Q=256: wg 0 converts block (0,0), wg 1 block (1,0);
-                    // otherwise both warpgroups take half of the block's columns.
-                    int q, c0, ncol, dcol;
-                    if (Q > 128 && r == 0) {
-                        q = wg; c0 = 0; ncol = 128; dcol = wg * 64;
-                    } else {
-                        q = 0; ncol = Cfg::kBRows / 2; c0 = wg * ncol;
-                        dcol = (Q > 128 ? 128 : 0) + c0 / 2;
-                    }
-                    for (int cc = 0; cc < ncol; cc += 32) {
-                        __syncwarp();
-                        uint32_t v[32], o[16];
-                        tmem_ld_x32(tmem + lane_off + Cfg::kScratch + q * 128 + c0 + cc, v);
-                        tmem_wait_ld();
+                if (half == 0) {
+                    // convert C B^T (fp32 scratch) to packed bf16 (warpgroups 0 and 1)
+                    const uint32_t cbdst = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
+                    for (int r = 0; r < rounds; ++r) {
+                        mbar_wait(smem_u32(b_cbfull + r), gi & 1, err, 1u);
+                        tc_fence_after();
+                        // round 0 of Q=256: warpgroup 0 converts block (0,0), 1 block (1,0);
+                        // otherwise the two take half of the block's columns each.
+                        int q, c0, ncol, dcol;
+                        if (Q > 128 && r == 0) {
+                            q = sel; c0 = 0; ncol = 128; dcol = sel * 64;
+                        } else {
+                            q = 0; ncol = Cfg::kBRows / 2; c0 = sel * ncol;
+                            dcol = (Q > 128 ? 128 : 0) + c0 / 2;
+                        }
+                        for (int cc = 0; cc < ncol; cc += 32) {
+                            __syncwarp();
+                            uint32_t v[32], o[16];
+                            tmem_ld_x32(tmem + lane_off + Cfg::kScratch + q * 128 + c0 + cc, v);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            o[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                        tmem_st_x16(tmem + lane_off + cbdst + dcol + cc / 2, o);
+                            for (int e = 0; e < 16; ++e)
+                                o[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                            tmem_st_x16(tmem + lane_off + cbdst + dcol + cc / 2, o);
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(b_cbconv + r));
                     }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(b_cbconv + r));
                 }
-                // Both warpgroups read each other's halves of the last round: wait
-                // for the whole conversion.  (The MMA warp waits on round 0 of a
-                // 256-token chunk before it reuses the scratch for round 1.)
+                // every warpgroup reads the whole packed C B^T: wait for the conversion
+                // (the MMA warp waits on round 0 of a 256-token chunk before it reuses
+                // the scratch for round 1)
                 mbar_wait(smem_u32(b_cbconv + (rounds - 1)), gi & 1, err, 1u);
                 tc_fence_after();
                 // release the stage slots that carried B
@@ -384,131 +391,100 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const float* gv = reinterpret_cast<const float*>(st + Cfg::kXBytes + Cfg::kHBytes);
             const float* dv = gv + Q;
             const uint32_t cbsrc = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
-            // which block of this head (if any) this warpgroup owns
+            // the query block of this head (if any) that this warpgroup works on
             int I = -1, slot = 0, use = 0;
             if (Q > 128) {
-                I = wg; slot = (js + wg) & 1; use = (js + wg) >> 1;
-            } else if ((js & 1) == wg) {
-                I = 0; slot = js & 1; use = js >> 1;
+                I = sel; slot = sel; use = js >> 1;
+            } else if ((js & 1) == sel) {
+                I = 0; slot = sel; use = js >> 1;
             }
             if (I >= 0) {
                 const int i = I * 128 + row;               // query row in the chunk
                 const float gi_ = (i < Q) ? gv[i] : 0.f;
                 const uint32_t acc = tmem + lane_off + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
-                // ---- column factors v_j = 2^{g_e - g_j} dt_j, e = end of j's 32-key chunk,
-                //      for this warpgroup's keys [kv0, kv0 + nv) ----
-                const int kv0 = (Q > 128 && wg == 1) ? 128 : 0;
-                const int nv = Q > 128 ? 128 : Q;
-                __nv_bfloat16* vb = vtab + (wg * 2 + (use & 1)) * 128;
-                if (row < nv) {
-                    const int j = kv0 + row;
+                const uint32_t abase = tmem + lane_off + (slot ? Cfg::kA1 : Cfg::kA0);
+                // this warpgroup's keys [kb, ke) of block I
+                const int KI = Q > 128 ? (I + 1) * 128 : Q;
+                const int kmid = (Q > 128 && I == 1) ? 128 : KI / 2;
+                const int kb = half ? kmid : 0, ke = half ? KI : kmid;
+                // ---- column factors v_j = 2^{g_e - g_j} dt_j, e = end of j's 32-key chunk ----
+                __nv_bfloat16* vb = vtab + (w * 2 + (use & 1)) * 128;
+                if (row < ke - kb) {
+                    const int j = kb + row;
                     vb[row] = __float2bfloat16_rn(exp2f(gv[j | 31] - gv[j]) * dv[j]);
                 }
-                named_bar_sync(1 + wg, 128);
+                named_bar_sync(1 + w, 128);
                 const uint32_t* vb32 = reinterpret_cast<const uint32_t*>(vb);
-                // ---- build A: keys [kb, ke) of query block Ib into A columns key/2 ----
-                auto build = [&](int Ib, int kb, int ke, uint32_t abase) {
-                    const int ib = Ib * 128 + row;
-                    const float gib = (ib < Q) ? gv[ib] : 0.f;
-                    const int dch = ib >> 5;              // key chunk holding the diagonal
-                    for (int k0 = kb; k0 < ke; k0 += 64) {
+                // ---- build A_I for keys [kb, ke): 32 keys (16 packed columns) at a time ----
+                {
+                    const int dch = i >> 5;   // key chunk holding the diagonal (warp-uniform)
+                    for (int j0 = kb; j0 < ke; j0 += 32) {
                         __syncwarp();  // warp-collective TMEM access below
-                        uint32_t o[32];
-                        const int kc0 = k0 >> 5;
-                        if (kc0 > dch) {
+                        const int kc = j0 >> 5;
+                        uint32_t o[16];
+                        if (kc > dch) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = 0u;
+                            for (int e = 0; e < 16; ++e) o[e] = 0u;
                         } else {
-                            const int J = k0 >> 7, jl0 = k0 & 127;
-                            const uint32_t blk =
-                                Q > 128 ? (Ib == 0 ? 0u : (J == 0 ? 64u : 128u)) : 0u;
-                            uint32_t cbv[32];
-                            tmem_ld_x32(tmem + lane_off + cbsrc + blk + jl0 / 2, cbv);
+                            const int J = j0 >> 7, jl0 = j0 & 127;
+                            const uint32_t blk = Q > 128 ? (I == 0 ? 0u : (J == 0 ? 64u : 128u)) : 0u;
+                            uint32_t cbv[16];
+                            tmem_ld_x16(tmem + lane_off + cbsrc + blk + jl0 / 2, cbv);
                             tmem_wait_ld();
+                            if (kc < dch) {
+                                // whole chunk at or below the row: factorised decay,
+                                // 2^{g_i - g_j} = 2^{g_i - g_e} 2^{g_e - g_j}, both <= 1
+                                const float uu = exp2f(gi_ - gv[j0 + 31]);
+                                const __nv_bfloat162 u2 = __floats2bfloat162_rn(uu, uu);
 #pragma unroll
-                            for (int hf = 0; hf < 2; ++hf) {
-                                const int kc = kc0 + hf, jb = k0 + 32 * hf;
-                                if (kc < dch) {
-                                    // whole chunk at or below the row: factorised decay,
-                                    // 2^{g_i - g_j} = 2^{g_i - g_e} 2^{g_e - g_j}, both <= 1
-                                    const float u = exp2f(gib - gv[jb + 31]);
-                                    const __nv_bfloat162 u2 = __floats2bfloat162_rn(u, u);
+                                for (int e = 0; e < 16; ++e) {
+                                    const __nv_bfloat162 c2 = as_bf162(cbv[e]);
+                                    const __nv_bfloat162 v2 = as_bf162(vb32[(j0 - kb) / 2 + e]);
+                                    o[e] = as_u32(__hmul2(__hmul2(c2, v2), u2));
+                                }
+                            } else {
+                                // diagonal chunk: exact exponent, masked by a select
 #pragma unroll
-                                    for (int e = 0; e < 16; ++e) {
-                                        const __nv_bfloat162 c2 = as_bf162(cbv[16 * hf + e]);
-                                        const __nv_bfloat162 v2 = as_bf162(vb32[(jb - kv0) / 2 + e]);
-                                        o[16 * hf + e] = as_u32(__hmul2(__hmul2(c2, v2), u2));
-                                    }
-                                } else if (kc == dch) {
-                                    // diagonal chunk: exact exponent, masked by a select
-#pragma unroll
-                                    for (int e = 0; e < 16; ++e) {
-                                        const int ja = jb + 2 * e, jc = ja + 1;
-                                        const float wa = exp2f(gib - gv[ja]) * dv[ja];
-                                        const float wc = exp2f(gib - gv[jc]) * dv[jc];
-                                        const float va = (ja <= ib) ? bf16lo(cbv[16 * hf + e]) * wa : 0.f;
-                                        const float vc = (jc <= ib) ? bf16hi(cbv[16 * hf + e]) * wc : 0.f;
-                                        o[16 * hf + e] = pack_bf16(va, vc);
-                                    }
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < 16; ++e) o[16 * hf + e] = 0u;
+                                for (int e = 0; e < 16; ++e) {
+                                    const int ja = j0 + 2 * e, jc = ja + 1;
+                                    const float wa = exp2f(gi_ - gv[ja]) * dv[ja];
+                                    const float wc = exp2f(gi_ - gv[jc]) * dv[jc];
+                                    const float va = (ja <= i) ? bf16lo(cbv[e]) * wa : 0.f;
+                                    const float vc = (jc <= i) ? bf16hi(cbv[e]) * wc : 0.f;
+                                    o[e] = pack_bf16(va, vc);
                                 }
                             }
                         }
-                        tmem_st_x32(abase + k0 / 2, o);
+                        tmem_st_x16(abase + j0 / 2, o);
                     }
+                    __syncwarp();
                     tmem_wait_st();
                     tc_fence_before();
-                };
-                const uint32_t a_own = tmem + lane_off + (slot ? Cfg::kA1 : Cfg::kA0);
-                if (Q > 128) {
-                    if (wg == 0) build(0, 0, 128, a_own);
-                    else build(1, 128, 256, a_own);
-                } else {
-                    build(0, 0, Q, a_own);
                 }
                 mbar_arrive(smem_u32(b_aready + slot));
-                // ---- acc *= 2^{g_i} ----
+                // ---- acc *= 2^{g_i} (this warpgroup's 32 columns) ----
                 mbar_wait(smem_u32(b_sdone + slot), use & 1, err, 1u);
                 tc_fence_after();
                 {
                     const float sg = exp2f(gi_);
                     uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld_x32(acc + half * 32, v);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        __syncwarp();
-                        tmem_ld_x32(acc + h2 * 32, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * sg);
-                        tmem_st_x32(acc + h2 * 32, v);
-                    }
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * sg);
+                    tmem_st_x32(acc + half * 32, v);
                     tmem_wait_st();
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(b_scaled + slot));
-                if (Q > 128 && wg == 0) {
-                    // keys [0, 128) of query block 1 (all below its diagonal), into A slot 1;
-                    // the previous head's block-1 product must have finished reading it
-                    if (use > 0) mbar_wait(smem_u32(b_ddone + 1), (use - 1) & 1, err, 1u);
-                    tc_fence_after();
-                    build(1, 0, 128, tmem + lane_off + Cfg::kA1);
-                    mbar_arrive(smem_u32(b_aready + 1));
-                }
-                // ---- epilogue: y = acc + D x ----
+                // ---- epilogue: y = acc + D x (this warpgroup's 32 columns) ----
                 mbar_wait(smem_u32(b_ddone + slot), use & 1, err, 1u);
                 tc_fence_after();
-                uint32_t v[64];
-                {
-                    uint32_t t0[32], t1[32];
-                    __syncwarp();
-                    tmem_ld_x32(acc, t0);
-                    tmem_ld_x32(acc + 32, t1);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) { v[e] = t0[e]; v[32 + e] = t1[e]; }
-                }
+                uint32_t v[32];
+                __syncwarp();
+                tmem_ld_x32(acc + half * 32, v);
+                tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(smem_u32(b_accfree + slot));
                 const int t = ui.c * Q + i;
@@ -517,18 +493,19 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const uint8_t* xr = st + i * kRowBytes;
                     __nv_bfloat16* yr = y + ((int64_t)(ui.b * L + t) * H + ui.h) * P;
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int ch = half * 4 + c4;
                         if (ch * 8 < P) {
                             const uint4 xv = *reinterpret_cast<const uint4*>(xr + ((ch ^ (i & 7)) << 4));
-                            uint4 ov;
                             const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
                             uint32_t ow[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const int p0 = ch * 8 + 2 * e;
+                                const int p0 = c4 * 8 + 2 * e;
                                 ow[e] = pack_bf16(__uint_as_float(v[p0]) + dh * bf16lo(xw[e]),
                                                   __uint_as_float(v[p0 + 1]) + dh * bf16hi(xw[e]));
                             }
+                            uint4 ov;
                             ov.x = ow[0]; ov.y = ow[1]; ov.z = ow[2]; ov.w = ow[3];
                             *reinterpret_cast<uint4*>(yr + ch * 8) = ov;
                         }
