@@ -386,6 +386,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 sc += Cfg::kBSlots;
             }
             const int s = sc % NST, k = sc / NST;
+            const float dh = D ? __ldg(D + ui.h) : 0.f;   // issued early, used in the epilogue
             mbar_wait(smem_u32(b_full + s), k & 1, err, 1u);
             const uint8_t* st = stage_ptr + s * Cfg::kStageBytes;
             const float* gv = reinterpret_cast<const float*>(st + Cfg::kXBytes + Cfg::kHBytes);
@@ -489,7 +490,6 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 mbar_arrive(smem_u32(b_accfree + slot));
                 const int t = ui.c * Q + i;
                 if (i < Q && t < L) {
-                    const float dh = D ? D[ui.h] : 0.f;
                     const uint8_t* xr = st + i * kRowBytes;
                     __nv_bfloat16* yr = y + ((int64_t)(ui.b * L + t) * H + ui.h) * P;
 #pragma unroll
