@@ -10,10 +10,10 @@
 //
 // One CTA owns (batch, chunk, 32 heads).  The dt tile is read row by row
 // (32 consecutive heads per warp load, coalesced), transposed through shared
-// memory, then each warp scans whole head columns: every lane sums a run of
-// Q/32 consecutive tokens serially and a warp-shuffle scan adds the lane
-// offsets.  Tokens past seqlen read as dt = 0, so the padded tail of the last
-// chunk repeats the value at the last real token.
+// memory, then each warp scans whole head columns in 32-token blocks with
+// warp shuffles, carrying the running total between blocks.  Tokens past
+// seqlen read as dt = 0, and the padded tail of the last chunk takes exactly
+// the value at the last real token.
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -31,7 +31,9 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = c * Q;
 
-    // coalesced load of the [Q, 32] dt tile (zero outside [0, L) x [0, H))
+    // coalesced load of the [Q, 32] dt tile (zero outside [0, L) x [0, H)),
+    // unrolled so that each warp keeps several independent loads in flight
+#pragma unroll 8
     for (int t = warp; t < Q; t += kThreads / 32) {
         const int tg = t0 + t, h = h0 + lane;
         float v = 0.f;
@@ -40,54 +42,36 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     }
     __syncthreads();
 
-    const int per_lane = Q >> 5;  // Q in {64, 128, 256} -> 2, 4 or 8 tokens per lane
+    // Each warp scans whole head columns.  Lane l takes tokens l, l + 32, ...:
+    // the column reads are conflict-free and every store is a coalesced
+    // 128-byte row.  A 32-token block is scanned with warp shuffles and the
+    // running total of the earlier blocks is carried in a register.
+    const int tl = L - 1 - t0;  // local index of the chunk's last real token
     for (int j = warp; j < kHeadsPerCta; j += kThreads / 32) {
         const int h = h0 + j;
         if (h >= H) break;
         const float a = A[h];
-        float run = 0.f;
-        float vals[8];
+        float* grow = Gcs + ((int64_t)b * H + h) * Lp + t0;
+        float* drow = dtT + ((int64_t)b * H + h) * Lp + t0;
+        float carry = 0.f, last = 0.f;
+        for (int k = 0; k < Q; k += 32) {
+            const int t = k + lane;
+            const float d = tile[t][j];
+            float v = a * d;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (k < per_lane) {
-                const float v = tile[lane * per_lane + k][j];
-                run += a * v;
-                vals[k] = run;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += o;
             }
-        }
-        // inclusive warp scan of the lane totals -> exclusive offset per lane
-        float incl = run;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        const float excl = incl - run;
-        float out[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) out[k] = (vals[k] + excl) * kLog2e;
-        if (t0 + Q > L) {
+            float out = (carry + v) * kLog2e;
+            carry += __shfl_sync(0xffffffffu, v, 31);
             // ragged last chunk: the padded slots take exactly the value at the
             // last real token, so that g_last (read at the chunk's last slot) is
             // bit-identical to it
-            const int last = L - 1 - t0, src_lane = last / per_lane, src_k = last % per_lane;
-            float v = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k == src_k) v = out[k];
-            v = __shfl_sync(0xffffffffu, v, src_lane);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (t0 + lane * per_lane + k > L - 1) out[k] = v;
-        }
-        float* grow = Gcs + ((int64_t)b * H + h) * Lp + t0 + lane * per_lane;
-        float* drow = dtT + ((int64_t)b * H + h) * Lp + t0 + lane * per_lane;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (k < per_lane) {
-                grow[k] = out[k];
-                drow[k] = tile[lane * per_lane + k][j];
-            }
+            if (tl >= k && tl < k + 32) last = __shfl_sync(0xffffffffu, out, tl - k);
+            if (t > tl) out = last;
+            grow[t] = out;
+            drow[t] = d;
         }
     }
 }
