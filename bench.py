@@ -103,11 +103,18 @@ def dram_traffic_record():
     return rec
 
 
-def source_digest() -> str:
+KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "fwd_pass_state": "fwd_pass_state_tc.cu",
+                  "compute_out": "compute_out_tc.cu"}
+
+
+def source_digest(kernel: str) -> str:
+    """Digest of one kernel's source file and the shared headers: a recorded
+    DRAM-traffic figure is valid only while this digest is unchanged."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "state_space_sequence_chunk_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = [KERNEL_SOURCES[kernel]] + sorted(n for n in os.listdir(csrc) if n.endswith(".cuh"))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -413,7 +420,7 @@ def main():
         achieved = model[dom] / (kms[dom] * 1e-3) / 1e9
         traffic = None
         rec = dram_traffic_record().get((dom, w.name))
-        if rec is not None and rec[1] == source_digest():
+        if rec is not None and rec[1] == source_digest(dom):
             traffic = rec[0]
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
