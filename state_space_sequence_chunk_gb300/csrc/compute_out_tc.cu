@@ -27,9 +27,9 @@
 //    into a stage ring; B only passes through the ring once per group.
 //
 // Warp roles (640 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
-// 2-3 idle, 4-19 four SIMT warpgroups: warpgroup w serves TMEM slot (w & 1)
-// and half (w >> 1) of the key and output columns.  A SIMT thread owns TMEM
-// lane (query row) 32*(warp%4) + lane.
+// 2-3 idle, 4-11 two builder warpgroups (C B^T conversion, decay-weighted
+// operands), 12-19 two epilogue warpgroups (slot 0 / slot 1: row scale and
+// y).  A SIMT thread owns TMEM lane (query row) 32*(warp%4) + lane.
 //
 // Supported here: bf16, P <= 64, N <= 128, Q in {64, 128, 256}.
 #include <cuda.h>
@@ -165,9 +165,9 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             mbar_init(smem_u32(b_cbconv + s), 256);
             mbar_init(smem_u32(b_sdone + s), 1);
             mbar_init(smem_u32(b_ddone + s), 1);
-            mbar_init(smem_u32(b_aready + s), 256);
-            mbar_init(smem_u32(b_scaled + s), 256);
-            mbar_init(smem_u32(b_accfree + s), 256);
+            mbar_init(smem_u32(b_aready + s), (Q > 128 && s == 0) ? 128 : 256);
+            mbar_init(smem_u32(b_scaled + s), 128);
+            mbar_init(smem_u32(b_accfree + s), 128);
         }
         fence_mbar_init();
     }
@@ -332,11 +332,14 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
     } else if (warp >= kSimtWarp0) {
         // ===================== SIMT warpgroups =====================
-        // Four warpgroups; warpgroup w serves TMEM slot / query block (w & 1) and
-        // half (w >> 1) of its key columns and output columns, so two threads
-        // share every query row and twice as many warps hide the latencies.
+        // Warpgroups 0 and 1 are builders: they convert C B^T once per group and
+        // build the decay-weighted operands A of every head.  Warpgroups 2 and 3
+        // serve TMEM slots 0 and 1: the 2^{g_i} row scale of the accumulator and
+        // the y epilogue.  The builders of head h+1 thus run while the epilogue
+        // of head h drains; only the MMA that reads an operand region orders them.
         const int w = (warp - kSimtWarp0) >> 2;          // 0..3
-        const int sel = w & 1, half = w >> 1;
+        const bool builder = w < 2;
+        const int sel = w & 1;
         const int row = (warp & 3) * 32 + lane;          // TMEM lane / query row in block
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         int sc = 0, gi = -1, js = 0;
@@ -346,14 +349,14 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             if (new_group(u, u0, H, hpg)) {
                 ++gi;
                 const int rounds = Q > 128 ? 2 : 1;
-                if (half == 0) {
-                    // convert C B^T (fp32 scratch) to packed bf16 (warpgroups 0 and 1)
+                if (builder) {
+                    // convert C B^T (fp32 scratch) to packed bf16
                     const uint32_t cbdst = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
                     for (int r = 0; r < rounds; ++r) {
                         mbar_wait(smem_u32(b_cbfull + r), gi & 1, err, 1u);
                         tc_fence_after();
-                        // round 0 of Q=256: warpgroup 0 converts block (0,0), 1 block (1,0);
-                        // otherwise the two take half of the block's columns each.
+                        // round 0 of Q=256: builder 0 converts block (0,0), builder 1
+                        // block (1,0); otherwise each takes half of the block's columns
                         int q, c0, ncol, dcol;
                         if (Q > 128 && r == 0) {
                             q = sel; c0 = 0; ncol = 128; dcol = sel * 64;
@@ -375,50 +378,40 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         tc_fence_before();
                         mbar_arrive(smem_u32(b_cbconv + r));
                     }
+                    // both builders read the whole packed C B^T
+                    mbar_wait(smem_u32(b_cbconv + (rounds - 1)), gi & 1, err, 1u);
+                    tc_fence_after();
                 }
-                // every warpgroup reads the whole packed C B^T: wait for the conversion
-                // (the MMA warp waits on round 0 of a 256-token chunk before it reuses
-                // the scratch for round 1)
-                mbar_wait(smem_u32(b_cbconv + (rounds - 1)), gi & 1, err, 1u);
-                tc_fence_after();
                 // release the stage slots that carried B
                 for (int j = 0; j < Cfg::kBSlots; ++j) mbar_arrive(smem_u32(b_empty + (sc + j) % NST));
                 sc += Cfg::kBSlots;
             }
             const int s = sc % NST, k = sc / NST;
-            const float dh = D ? __ldg(D + ui.h) : 0.f;   // issued early, used in the epilogue
+            const float dh = (!builder && D) ? __ldg(D + ui.h) : 0.f;  // issued early
             mbar_wait(smem_u32(b_full + s), k & 1, err, 1u);
             const uint8_t* st = stage_ptr + s * Cfg::kStageBytes;
             const float* gv = reinterpret_cast<const float*>(st + Cfg::kXBytes + Cfg::kHBytes);
             const float* dv = gv + Q;
-            const uint32_t cbsrc = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
-            // the query block of this head (if any) that this warpgroup works on
-            int I = -1, slot = 0, use = 0;
-            if (Q > 128) {
-                I = sel; slot = sel; use = js >> 1;
-            } else if ((js & 1) == sel) {
-                I = 0; slot = sel; use = js >> 1;
-            }
-            if (I >= 0) {
-                const int i = I * 128 + row;               // query row in the chunk
-                const float gi_ = (i < Q) ? gv[i] : 0.f;
-                const uint32_t acc = tmem + lane_off + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
-                const uint32_t abase = tmem + lane_off + (slot ? Cfg::kA1 : Cfg::kA0);
-                // this warpgroup's keys [kb, ke) of block I
-                const int KI = Q > 128 ? (I + 1) * 128 : Q;
-                const int kmid = (Q > 128 && I == 1) ? 128 : KI / 2;
-                const int kb = half ? kmid : 0, ke = half ? KI : kmid;
-                // ---- column factors v_j = 2^{g_e - g_j} dt_j, e = end of j's 32-key chunk ----
-                __nv_bfloat16* vb = vtab + (w * 2 + (use & 1)) * 128;
-                if (row < ke - kb) {
-                    const int j = kb + row;
-                    vb[row] = __float2bfloat16_rn(exp2f(gv[j | 31] - gv[j]) * dv[j]);
-                }
-                named_bar_sync(1 + w, 128);
-                const uint32_t* vb32 = reinterpret_cast<const uint32_t*>(vb);
-                // ---- build A_I for keys [kb, ke): 32 keys (16 packed columns) at a time ----
+            const int use = js >> 1;   // use count of the slot(s) this head occupies
+            if (builder) {
+                const uint32_t cbsrc = Q > 128 ? Cfg::kCbBase : Cfg::kCbBase + (gi & 1) * 64;
+                // ---- column factors v_j = 2^{g_e - g_j} dt_j (e = end of j's 32-key
+                //      chunk) for every key of the chunk, shared by both builders ----
+                // double-buffered by head parity: a builder may still read the
+                // previous head's table while the other writes this one
+                __nv_bfloat16* vb = vtab + ((js / Cfg::kBlocks) & 1) * 256;
                 {
+                    const int j = sel * 128 + row;
+                    if (j < Q) vb[j] = __float2bfloat16_rn(exp2f(gv[j | 31] - gv[j]) * dv[j]);
+                }
+                named_bar_sync(1, 256);
+                const uint32_t* vb32 = reinterpret_cast<const uint32_t*>(vb);
+                // ---- build A for query block I, keys [kb, ke), 32 keys at a time ----
+                auto build = [&](int I, int kb, int ke, int slot) {
+                    const int i = I * 128 + row;               // query row in the chunk
+                    const float gi_ = (i < Q) ? gv[i] : 0.f;
                     const int dch = i >> 5;   // key chunk holding the diagonal (warp-uniform)
+                    const uint32_t abase = tmem + lane_off + (slot ? Cfg::kA1 : Cfg::kA0);
                     for (int j0 = kb; j0 < ke; j0 += 32) {
                         __syncwarp();  // warp-collective TMEM access below
                         const int kc = j0 >> 5;
@@ -440,7 +433,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                                 for (int e = 0; e < 16; ++e) {
                                     const __nv_bfloat162 c2 = as_bf162(cbv[e]);
-                                    const __nv_bfloat162 v2 = as_bf162(vb32[(j0 - kb) / 2 + e]);
+                                    const __nv_bfloat162 v2 = as_bf162(vb32[j0 / 2 + e]);
                                     o[e] = as_u32(__hmul2(__hmul2(c2, v2), u2));
                                 }
                             } else {
@@ -461,53 +454,85 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     __syncwarp();
                     tmem_wait_st();
                     tc_fence_before();
+                    mbar_arrive(smem_u32(b_aready + slot));
+                };
+                // the previous A X product on a slot must be done before its A is rewritten
+                auto a_free = [&](int slot) {
+                    if (use > 0) mbar_wait(smem_u32(b_ddone + slot), (use - 1) & 1, err, 1u);
+                    tc_fence_after();
+                };
+                if (Q > 128) {
+                    // block 0: keys [0,128); block 1: keys [0,256); split for balance
+                    if (sel == 0) {
+                        a_free(0);
+                        build(0, 0, 128, 0);
+                        a_free(1);
+                        build(1, 0, 64, 1);
+                    } else {
+                        a_free(1);
+                        build(1, 64, 256, 1);
+                    }
+                } else {
+                    const int slot = js & 1;
+                    a_free(slot);
+                    build(0, sel * (Q / 2), (sel + 1) * (Q / 2), slot);
                 }
-                mbar_arrive(smem_u32(b_aready + slot));
-                // ---- acc *= 2^{g_i} (this warpgroup's 32 columns) ----
-                mbar_wait(smem_u32(b_sdone + slot), use & 1, err, 1u);
-                tc_fence_after();
-                {
-                    const float sg = exp2f(gi_);
-                    uint32_t v[32];
+            } else {
+                const int es = sel;    // this warpgroup's TMEM slot
+                const int I = Q > 128 ? es : (((js & 1) == es) ? 0 : -1);
+                if (I >= 0) {
+                    const int i = I * 128 + row;
+                    const uint32_t acc = tmem + lane_off + (es ? Cfg::kAcc1 : Cfg::kAcc0);
+                    // ---- acc *= 2^{g_i} ----
+                    mbar_wait(smem_u32(b_sdone + es), use & 1, err, 1u);
+                    tc_fence_after();
+                    {
+                        const float sg = exp2f((i < Q) ? gv[i] : 0.f);
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            uint32_t v[32];
+                            __syncwarp();
+                            tmem_ld_x32(acc + h2 * 32, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * sg);
+                            tmem_st_x32(acc + h2 * 32, v);
+                        }
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(b_scaled + es));
+                    // ---- epilogue: y = acc + D x ----
+                    mbar_wait(smem_u32(b_ddone + es), use & 1, err, 1u);
+                    tc_fence_after();
+                    uint32_t v0[32], v1[32];
                     __syncwarp();
-                    tmem_ld_x32(acc + half * 32, v);
+                    tmem_ld_x32(acc, v0);
+                    tmem_ld_x32(acc + 32, v1);
                     tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(b_accfree + es));
+                    const int t = ui.c * Q + i;
+                    if (i < Q && t < L) {
+                        const uint8_t* xr = st + i * kRowBytes;
+                        __nv_bfloat16* yr = y + ((int64_t)(ui.b * L + t) * H + ui.h) * P;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * sg);
-                    tmem_st_x32(acc + half * 32, v);
-                    tmem_wait_st();
-                }
-                tc_fence_before();
-                mbar_arrive(smem_u32(b_scaled + slot));
-                // ---- epilogue: y = acc + D x (this warpgroup's 32 columns) ----
-                mbar_wait(smem_u32(b_ddone + slot), use & 1, err, 1u);
-                tc_fence_after();
-                uint32_t v[32];
-                __syncwarp();
-                tmem_ld_x32(acc + half * 32, v);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(smem_u32(b_accfree + slot));
-                const int t = ui.c * Q + i;
-                if (i < Q && t < L) {
-                    const uint8_t* xr = st + i * kRowBytes;
-                    __nv_bfloat16* yr = y + ((int64_t)(ui.b * L + t) * H + ui.h) * P;
+                        for (int ch = 0; ch < 8; ++ch) {
+                            if (ch * 8 < P) {
+                                const uint4 xv = *reinterpret_cast<const uint4*>(xr + ((ch ^ (i & 7)) << 4));
+                                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                                uint32_t ow[4];
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int ch = half * 4 + c4;
-                        if (ch * 8 < P) {
-                            const uint4 xv = *reinterpret_cast<const uint4*>(xr + ((ch ^ (i & 7)) << 4));
-                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                            uint32_t ow[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int p0 = c4 * 8 + 2 * e;
-                                ow[e] = pack_bf16(__uint_as_float(v[p0]) + dh * bf16lo(xw[e]),
-                                                  __uint_as_float(v[p0 + 1]) + dh * bf16hi(xw[e]));
+                                for (int e = 0; e < 4; ++e) {
+                                    const int p0 = ch * 8 + 2 * e;
+                                    const uint32_t* vv = p0 < 32 ? v0 : v1;
+                                    ow[e] = pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
+                                                      __uint_as_float(vv[(p0 & 31) + 1]) + dh * bf16hi(xw[e]));
+                                }
+                                uint4 ov;
+                                ov.x = ow[0]; ov.y = ow[1]; ov.z = ow[2]; ov.w = ow[3];
+                                *reinterpret_cast<uint4*>(yr + ch * 8) = ov;
                             }
-                            uint4 ov;
-                            ov.x = ow[0]; ov.y = ow[1]; ov.z = ow[2]; ov.w = ow[3];
-                            *reinterpret_cast<uint4*>(yr + ch * 8) = ov;
                         }
                     }
                 }
