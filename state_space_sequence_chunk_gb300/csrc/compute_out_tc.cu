@@ -119,6 +119,7 @@ template <int Q>
 __global__ void __launch_bounds__(kThreads, 1)
 compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_h,
+               const __grid_constant__ CUtensorMap tm_y,
                const float* __restrict__ Gcs, const float* __restrict__ dtT,
                const float* __restrict__ D, __nv_bfloat16* __restrict__ y, int L, int H, int P,
                int nc, int Lp, int hpg, int units) {
@@ -512,28 +513,42 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(smem_u32(b_accfree + es));
-                    const int t = ui.c * Q + i;
-                    if (i < Q && t < L) {
+                    // y rows go to shared memory in the 128-byte-swizzled layout of the
+                    // tensor map, then one thread stores the 128-row block with TMA
+                    // (rows past seqlen and columns past headdim are clipped by it).
+                    // Block 0 of a 256-token chunk stages in the stage's h tile (free
+                    // once both C h^T products are done); otherwise each row
+                    // overwrites its own x row (free once the last A X product is
+                    // done, which the d_done wait above covers).
+                    uint8_t* stage_rw = stage_ptr + s * Cfg::kStageBytes;
+                    uint8_t* ybuf = (Q > 128 && I == 0) ? stage_rw + Cfg::kXBytes : stage_rw + I * 128 * kRowBytes;
+                    if (i < Q) {
                         const uint8_t* xr = st + i * kRowBytes;
-                        __nv_bfloat16* yr = y + ((int64_t)(ui.b * L + t) * H + ui.h) * P;
+                        uint8_t* yr = ybuf + row * kRowBytes;
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
-                            if (ch * 8 < P) {
-                                const uint4 xv = *reinterpret_cast<const uint4*>(xr + ((ch ^ (i & 7)) << 4));
-                                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                                uint32_t ow[4];
+                            const int off = (ch ^ (i & 7)) << 4;   // (row & 7) == (i & 7)
+                            const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
+                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                            uint32_t ow[4];
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int p0 = ch * 8 + 2 * e;
-                                    const uint32_t* vv = p0 < 32 ? v0 : v1;
-                                    ow[e] = pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
-                                                      __uint_as_float(vv[(p0 & 31) + 1]) + dh * bf16hi(xw[e]));
-                                }
-                                uint4 ov;
-                                ov.x = ow[0]; ov.y = ow[1]; ov.z = ow[2]; ov.w = ow[3];
-                                *reinterpret_cast<uint4*>(yr + ch * 8) = ov;
+                            for (int e = 0; e < 4; ++e) {
+                                const int p0 = ch * 8 + 2 * e;
+                                const uint32_t* vv = p0 < 32 ? v0 : v1;
+                                ow[e] = pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
+                                                  __uint_as_float(vv[(p0 & 31) + 1]) + dh * bf16hi(xw[e]));
                             }
+                            uint4 ov;
+                            ov.x = ow[0]; ov.y = ow[1]; ov.z = ow[2]; ov.w = ow[3];
+                            *reinterpret_cast<uint4*>(yr + off) = ov;
                         }
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(2 + es, 128);
+                    if (row == 0) {
+                        tma_store_4d(&tm_y, smem_u32(ybuf), 0, ui.h, ui.c * Q + I * 128, ui.b);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();   // the stage is released only after this read
                     }
                 }
             }
@@ -556,7 +571,7 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
                      const float* Gcs, const float* dtT, const void* hid, const float* D, void* y,
                      cudaStream_t stream) {
     using Cfg = CoCfg<Q>;
-    CUtensorMap tx, tc, tb, th;
+    CUtensorMap tx, tc, tb, th, ty;
     const uint64_t xd[4] = {(uint64_t)p.P, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
     const uint64_t xs[3] = {(uint64_t)p.P * 2, (uint64_t)p.H * p.P * 2,
                             (uint64_t)p.L * p.H * p.P * 2};
@@ -574,7 +589,8 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     if (!encode_tmap_4d(&tx, bf, x, xd, xs, box_x, sw) ||
         !encode_tmap_4d(&tc, bf, C, bd, bs, box_x, sw) ||
         !encode_tmap_4d(&tb, bf, B, bd, bs, box_b, sw) ||
-        !encode_tmap_4d(&th, bf, hid, hd, hs, box_h, sw))
+        !encode_tmap_4d(&th, bf, hid, hd, hs, box_h, sw) ||
+        !encode_tmap_4d(&ty, bf, y, xd, xs, box_b, sw))
         return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -585,7 +601,7 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     if (e != cudaSuccess) return e;
     const int64_t units = p.b * p.nc * p.H;
     const int grid = (int)(units < sms ? units : sms);
-    kern<<<grid, kThreads, Cfg::kSmem, stream>>>(tx, tc, tb, th, Gcs, dtT, D, (__nv_bfloat16*)y,
+    kern<<<grid, kThreads, Cfg::kSmem, stream>>>(tx, tc, tb, th, ty, Gcs, dtT, D, (__nv_bfloat16*)y,
                                                  (int)p.L, (int)p.H, (int)p.P, (int)p.nc,
                                                  (int)p.Lp, (int)p.hpg, (int)units);
     return cudaGetLastError();
