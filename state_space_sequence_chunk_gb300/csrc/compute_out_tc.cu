@@ -273,15 +273,14 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             const uint32_t bbase =
                                 smem_u32(stage_ptr + ((sc + J) % NST) * Cfg::kStageBytes);
                             const uint32_t dcol = tmem + Cfg::kScratch + q * 128;
-                            for (int kk = 0; kk < 8; ++kk) {  // K = 128 state columns
-                                const uint64_t ad = smem_desc_sw128(
-                                    cbase + (kk / 4) * Cfg::kCAtomBytes + I * 128 * kRowBytes +
-                                        (kk % 4) * 32, 16, 8 * kRowBytes);
-                                const uint64_t bd = smem_desc_sw128(
-                                    bbase + (kk / 4) * Cfg::kBAtomBytes + (kk % 4) * 32, 16,
-                                    8 * kRowBytes);
-                                mma_f16_ss(dcol, ad, bd, kIdescCB, kk > 0 ? 1u : 0u);
-                            }
+                            const uint64_t ad0 = smem_desc_sw128(cbase + I * 128 * kRowBytes, 16, 8 * kRowBytes);
+                            const uint64_t bd0 = smem_desc_sw128(bbase, 16, 8 * kRowBytes);
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)  // K = 128 state columns
+                                mma_f16_ss(dcol,
+                                           ad0 + (uint64_t)(((kk / 4) * Cfg::kCAtomBytes + (kk % 4) * 32) >> 4),
+                                           bd0 + (uint64_t)(((kk / 4) * Cfg::kBAtomBytes + (kk % 4) * 32) >> 4),
+                                           kIdescCB, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(smem_u32(b_cbfull + r));
                     }
@@ -298,15 +297,15 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     mbar_wait(smem_u32(b_accfree + slot), (use & 1) ^ 1, err, 1u);
                     tc_fence_after();
                     const uint32_t acc = tmem + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(
-                            cbase + (kk / 4) * Cfg::kCAtomBytes + I * 128 * kRowBytes + (kk % 4) * 32,
-                            16, 8 * kRowBytes);
-                        // B = h^T tile [n][p]: MN-major (p contiguous), K = 16 state rows
-                        const uint64_t bd = smem_desc_sw128(st + Cfg::kXBytes + kk * 16 * kRowBytes,
-                                                            8 * kRowBytes, 8 * kRowBytes);
-                        mma_f16_ss(acc, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-                    }
+                    // descriptors built once; the K steps add compile-time offsets to
+                    // the start-address field (addr >> 4, no carry below 256 KB)
+                    const uint64_t ad0 = smem_desc_sw128(cbase + I * 128 * kRowBytes, 16, 8 * kRowBytes);
+                    // B = h^T tile [n][p]: MN-major (p contiguous), K = 16 state rows
+                    const uint64_t bd0 = smem_desc_sw128(st + Cfg::kXBytes, 8 * kRowBytes, 8 * kRowBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_f16_ss(acc, ad0 + (uint64_t)(((kk / 4) * Cfg::kCAtomBytes + (kk % 4) * 32) >> 4),
+                                   bd0 + (uint64_t)((kk * 16 * kRowBytes) >> 4), kIdescS, kk > 0 ? 1u : 0u);
                     mma_commit(smem_u32(b_sdone + slot));
                 }
                 // the C buffer is free once the group's last C h^T is done
@@ -320,11 +319,12 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const uint32_t acc = tmem + (slot ? Cfg::kAcc1 : Cfg::kAcc0);
                     const uint32_t abase = tmem + (slot ? Cfg::kA1 : Cfg::kA0);
                     const int ksteps = (Q > 128 ? (I + 1) * 128 : Q) / 16;
-                    for (int kk = 0; kk < ksteps; ++kk) {
-                        const uint64_t bd = smem_desc_sw128(st + kk * 16 * kRowBytes, 8 * kRowBytes,
-                                                            8 * kRowBytes);
-                        mma_f16_ts(acc, abase + kk * 8, bd, kIdescD, 1u);
-                    }
+                    const uint64_t bd0 = smem_desc_sw128(st, 8 * kRowBytes, 8 * kRowBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk)
+                        if (kk < ksteps)
+                            mma_f16_ts(acc, abase + kk * 8, bd0 + (uint64_t)((kk * 16 * kRowBytes) >> 4),
+                                       kIdescD, 1u);
                     mma_commit(smem_u32(b_ddone + slot));
                 }
                 js += Cfg::kBlocks;

@@ -151,17 +151,17 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 mbar_wait(scaled(s), k & 1, &g_fps_error, 1u);
                 tc_fence_after();
                 const uint32_t xs = stage0 + s * Cfg::kStageBytes, bs = xs + Cfg::kXBytes;
+                // A = B_c^T: M = 128 state rows (two 64-row swizzle atoms, kSub*128
+                // bytes apart), K = 16 tokens, MN-major.  B = s o X_c: N = PP columns
+                // of P, K = 16 tokens, MN-major.  Descriptors are built once; a K
+                // step adds a compile-time offset to the start-address field.
+                const uint64_t ad0 = smem_desc_sw128(bs, kSub * kRowBytes, 8 * kRowBytes);
+                const uint64_t bd0 = smem_desc_sw128(xs, kSub * kRowBytes, 8 * kRowBytes);
 #pragma unroll
-                for (int kk = 0; kk < kSub / 16; ++kk) {
-                    // A = B_c^T: M = 128 state rows (two 64-row swizzle atoms,
-                    // kSub*128 bytes apart), K = 16 tokens, MN-major.
-                    const uint64_t adesc = smem_desc_sw128(bs + kk * 16 * kRowBytes,
-                                                           kSub * kRowBytes, 8 * kRowBytes);
-                    // B = s o X_c: N = PP columns of P, K = 16 tokens, MN-major.
-                    const uint64_t bdesc = smem_desc_sw128(xs + kk * 16 * kRowBytes,
-                                                           kSub * kRowBytes, 8 * kRowBytes);
-                    mma_f16_ss(tmem, adesc, bdesc, Cfg::kIdesc, (sub > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kSub / 16; ++kk)
+                    mma_f16_ss(tmem, ad0 + (uint64_t)((kk * 16 * kRowBytes) >> 4),
+                               bd0 + (uint64_t)((kk * 16 * kRowBytes) >> 4), Cfg::kIdesc,
+                               (sub > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(empty(s));
                 if (sub == nsub - 1) mma_commit(acc_full);
             }
