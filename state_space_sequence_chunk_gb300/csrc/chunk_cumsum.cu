@@ -8,10 +8,11 @@
 // that the two later kernels read it with contiguous (TMA-able) loads; dt is
 // transposed into the same layout in the same pass.
 //
-// One CTA owns (batch, chunk, 32 heads).  The dt tile is read row by row
-// (32 consecutive heads per warp load, coalesced), transposed through shared
-// memory, then each warp scans whole head columns in 32-token blocks with
-// warp shuffles, carrying the running total between blocks.  Tokens past
+// One CTA owns (batch, chunk, 8 heads) -- a grid of nc * H/8 * batch CTAs, so
+// that enough loads are in flight.  The dt tile is read as 32-byte runs of 8
+// consecutive heads per token, transposed through shared memory, then each of
+// the 8 warps scans one head column in 32-token blocks with warp shuffles,
+// carrying the running total between blocks.  Tokens past
 // seqlen read as dt = 0, and the padded tail of the last chunk takes exactly
 // the value at the last real token.
 #include "ssd_internal.cuh"
@@ -19,7 +20,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kHeadsPerCta = 32;
+constexpr int kHeadsPerCta = 8;
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads)
@@ -27,18 +28,20 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
                     float* __restrict__ Gcs, float* __restrict__ dtT,
                     int L, int H, int Q, int Lp) {
     __shared__ float tile[256][kHeadsPerCta + 1];
+    static_assert(kThreads / 32 == kHeadsPerCta, "one warp per head column");
     const int c = blockIdx.x, h0 = blockIdx.y * kHeadsPerCta, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = c * Q;
 
-    // coalesced load of the [Q, 32] dt tile (zero outside [0, L) x [0, H)),
-    // unrolled so that each warp keeps several independent loads in flight
+    // load of the [Q, 8] dt tile (zero outside [0, L) x [0, H)): thread i reads
+    // head i % 8 of token i / 8, so a warp covers 4 tokens x 8 heads per load
 #pragma unroll 8
-    for (int t = warp; t < Q; t += kThreads / 32) {
-        const int tg = t0 + t, h = h0 + lane;
+    for (int i = threadIdx.x; i < Q * kHeadsPerCta; i += kThreads) {
+        const int t = i / kHeadsPerCta, hh = i % kHeadsPerCta;
+        const int tg = t0 + t, h = h0 + hh;
         float v = 0.f;
         if (tg < L && h < H) v = dt[((int64_t)b * L + tg) * H + h];
-        tile[t][lane] = v;
+        tile[t][hh] = v;
     }
     __syncthreads();
 

@@ -24,9 +24,9 @@
 //    per-token scale s_q = dt_q 2^{g_last - g_q} is applied to the x rows in
 //    shared memory (a row is contiguous in the swizzled tile).
 //
-// Warp roles (192 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
-// 2..5 state warps (row scaling of every stage, and the state update at each
-// chunk boundary; TMEM lane quarter = warp % 4).  TMEM: columns
+// Warp roles (256 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
+// 2..3 row scalers, 4..7 state warps (the state update at each chunk
+// boundary; TMEM lane quarter = warp % 4).  TMEM: columns
 // [0, PP) accumulator, [PP, 2 PP) state S^T (lane = state row n, column = p).
 //
 // CTA = (128-row block of N, batch * head).  N and P are padded to the
@@ -45,7 +45,7 @@ __device__ unsigned int g_fps_error;  // bit 0: a bounded wait gave up
 
 constexpr int kSub = 32;            // tokens per pipeline stage
 constexpr int kRowBytes = 128;      // one swizzle row (64 bf16)
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
 
 template <int PP>
 struct FpsCfg {
@@ -102,7 +102,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(scaled(s), 128);
+            mbar_init(scaled(s), 64);
             mbar_init(empty(s), 1);
         }
         mbar_init(acc_full, 1);
@@ -166,13 +166,38 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 if (sub == nsub - 1) mma_commit(acc_full);
             }
         }
+    } else if (warp < 4) {
+        // ---------------- scaler warps (2, 3): x_q <- x_q * dt_q 2^{g_last - g_q} ----------------
+        const int tid = threadIdx.x - 64;  // 0..63
+        for (int i = 0; i < total; ++i) {
+            const int s = i % S, k = i / S;
+            mbar_wait(full(s), k & 1, &g_fps_error, 1u);
+            uint8_t* xs = smem + s * Cfg::kStageBytes;
+            const float* gv = reinterpret_cast<const float*>(xs + Cfg::kVecOff);
+            const float* dv = gv + kSub;
+            const float glast = gv[2 * kSub + 3];
+            constexpr int kVecs = kSub * (PP / 64) * 8;   // 16-byte vectors in the x sub-tile
+#pragma unroll
+            for (int v = tid; v < kVecs; v += 64) {
+                const int box = v / (kSub * 8), r = (v / 8) % kSub, q = v % 8;
+                // the row scale rounded to bf16 once, then packed bf16x2 products
+                const __nv_bfloat162 s2 = __float2bfloat162_rn(dv[r] * exp2f(glast - gv[r]));
+                uint4* ptr = reinterpret_cast<uint4*>(xs + box * kSub * kRowBytes + r * kRowBytes) + q;
+                uint4 w = *ptr;
+                w.x = mul_bf162(w.x, s2);
+                w.y = mul_bf162(w.y, s2);
+                w.z = mul_bf162(w.z, s2);
+                w.w = mul_bf162(w.w, s2);
+                *ptr = w;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(scaled(s));
+        }
     } else {
-        // ---------------- state warps (2..5): row scaling and the state update ----------------
-        // Each thread owns TMEM lane (state row n) 32*(warp%4) + lane.  The warps
-        // scale every stage's x rows (128 threads, two 16-byte vectors each) and,
-        // at each chunk boundary, fold the finished chunk product into S.
+        // ---------------- state warps (4..7): the state update ----------------
+        // Each thread owns TMEM lane (state row n) 32*(warp%4) + lane and, at each
+        // chunk boundary, folds the finished chunk product into S.
         const int quarter = warp & 3;
-        const int tid = threadIdx.x - 64;  // 0..127
         const int n = mb * 128 + quarter * 32 + lane;
         const bool nok = n < N;
         const uint32_t acc_addr = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -192,7 +217,6 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             tmem_st_x16(st_addr + 16 * j, r);
         }
         tmem_wait_st();
-        const float* grow = Gcs + (int64_t)bh * Lp;
         // S <- 2^{g_last(c)} S + D_c, storing the chunk-start S^T to hiddens[c]
         auto chunk_update = [&](int c, float gl) {
             const float e = exp2f(gl);
@@ -236,36 +260,13 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             tc_fence_before();
             mbar_arrive(acc_empty);
         };
-        float gl_prev = 0.f;
-        for (int i = 0; i < total; ++i) {
-            const int s = i % S, k = i / S;
-            const int c = i / nsub, sub = i % nsub;
-            if (sub == 0 && c > 0) chunk_update(c - 1, gl_prev);
-            // ---- row scaling of stage i: x_q <- x_q * dt_q 2^{g_last - g_q} ----
-            mbar_wait(full(s), k & 1, &g_fps_error, 1u);
-            uint8_t* xs = smem + s * Cfg::kStageBytes;
-            const float* gv = reinterpret_cast<const float*>(xs + Cfg::kVecOff);
-            const float* dv = gv + kSub;
-            const float glast = gv[2 * kSub + 3];
-            if (sub == nsub - 1) gl_prev = glast;
-            constexpr int kVecs = kSub * (PP / 64) * 8;   // 16-byte vectors in the x sub-tile
-#pragma unroll
-            for (int v = tid; v < kVecs; v += 128) {
-                const int box = v / (kSub * 8), r = (v / 8) % kSub, q = v % 8;
-                // the row scale rounded to bf16 once, then packed bf16x2 products
-                const __nv_bfloat162 s2 = __float2bfloat162_rn(dv[r] * exp2f(glast - gv[r]));
-                uint4* ptr = reinterpret_cast<uint4*>(xs + box * kSub * kRowBytes + r * kRowBytes) + q;
-                uint4 w = *ptr;
-                w.x = mul_bf162(w.x, s2);
-                w.y = mul_bf162(w.y, s2);
-                w.z = mul_bf162(w.z, s2);
-                w.w = mul_bf162(w.w, s2);
-                *ptr = w;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(scaled(s));
+        const float* gl_src = Gcs + (int64_t)bh * Lp + Q - 1;   // g_last of each chunk
+        float gl_next = gl_src[0];
+        for (int c = 0; c < nc; ++c) {
+            const float gl = gl_next;
+            if (c + 1 < nc) gl_next = gl_src[(int64_t)(c + 1) * Q];
+            chunk_update(c, gl);
         }
-        if (nc > 0) chunk_update(nc - 1, gl_prev);
         if (final_state != nullptr) {  // uniform: all lanes load, valid lanes store
 #pragma unroll
             for (int j = 0; j < PP / 16; ++j) {
