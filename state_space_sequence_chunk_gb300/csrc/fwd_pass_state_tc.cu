@@ -24,8 +24,8 @@
 //    per-token scale s_q = dt_q 2^{g_last - g_q} is applied to the x rows in
 //    shared memory (a row is contiguous in the swizzled tile).
 //
-// Warp roles (256 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
-// 2..3 row scalers, 4..7 state warps (the state update at each chunk
+// Warp roles (320 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
+// 2..5 row scalers, 6..9 state warps (the state update at each chunk
 // boundary; TMEM lane quarter = warp % 4).  TMEM: columns
 // [0, PP) accumulator, [PP, 2 PP) state S^T (lane = state row n, column = p).
 //
@@ -45,7 +45,8 @@ __device__ unsigned int g_fps_error;  // bit 0: a bounded wait gave up
 
 constexpr int kSub = 32;            // tokens per pipeline stage
 constexpr int kRowBytes = 128;      // one swizzle row (64 bf16)
-constexpr int kThreads = 256;
+constexpr int kScalerWarps = 4;
+constexpr int kThreads = 32 * (2 + kScalerWarps + 4);
 
 template <int PP>
 struct FpsCfg {
@@ -102,7 +103,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(scaled(s), 64);
+            mbar_init(scaled(s), 32 * kScalerWarps);
             mbar_init(empty(s), 1);
         }
         mbar_init(acc_full, 1);
@@ -166,9 +167,9 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 if (sub == nsub - 1) mma_commit(acc_full);
             }
         }
-    } else if (warp < 4) {
-        // ---------------- scaler warps (2, 3): x_q <- x_q * dt_q 2^{g_last - g_q} ----------------
-        const int tid = threadIdx.x - 64;  // 0..63
+    } else if (warp < 2 + kScalerWarps) {
+        // ---------------- scaler warps: x_q <- x_q * dt_q 2^{g_last - g_q} ----------------
+        const int tid = threadIdx.x - 64;
         for (int i = 0; i < total; ++i) {
             const int s = i % S, k = i / S;
             mbar_wait(full(s), k & 1, &g_fps_error, 1u);
@@ -178,7 +179,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             const float glast = gv[2 * kSub + 3];
             constexpr int kVecs = kSub * (PP / 64) * 8;   // 16-byte vectors in the x sub-tile
 #pragma unroll
-            for (int v = tid; v < kVecs; v += 64) {
+            for (int v = tid; v < kVecs; v += 32 * kScalerWarps) {
                 const int box = v / (kSub * 8), r = (v / 8) % kSub, q = v % 8;
                 // the row scale rounded to bf16 once, then packed bf16x2 products
                 const __nv_bfloat162 s2 = __float2bfloat162_rn(dv[r] * exp2f(glast - gv[r]));
@@ -194,7 +195,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             mbar_arrive(scaled(s));
         }
     } else {
-        // ---------------- state warps (4..7): the state update ----------------
+        // ---------------- state warps (the last four): the state update ----------------
         // Each thread owns TMEM lane (state row n) 32*(warp%4) + lane and, at each
         // chunk boundary, folds the finished chunk product into S.
         const int quarter = warp & 3;
