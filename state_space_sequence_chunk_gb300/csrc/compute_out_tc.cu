@@ -64,7 +64,7 @@ struct CoCfg {
     static constexpr int kStages = Q > 128 ? 3 : 4;
     static constexpr int kBSlots = Q > 128 ? 2 : 1;         // stage slots a B tile occupies
     static constexpr int kBAtomBytes = kBRows * kRowBytes;
-    static constexpr int kBarBytes = 3072;  // barriers, TMEM holder, v_j tables
+    static constexpr int kBarBytes = 4096;  // barriers, TMEM holder, v_j tables
     static constexpr int kSmem = kCBufs * kCBytes + kStages * kStageBytes + kBarBytes + 1024;
     // TMEM columns (512 allocated)
     // layout, Q = 256: [0,192) CB blocks (0,0) (1,0) (1,1); [192,256) A slot 0;
@@ -147,6 +147,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(b_accfree + 2);
     // per-warpgroup, per-head-parity tables of the column factors v_j (bf16)
     __nv_bfloat16* vtab = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(bars) + 512);
+    float* vtabf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 1536);  // fp32 copy
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u0 = (int)((int64_t)blockIdx.x * units / gridDim.x);
@@ -401,9 +402,14 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 // double-buffered by head parity: a builder may still read the
                 // previous head's table while the other writes this one
                 __nv_bfloat16* vb = vtab + ((js / Cfg::kBlocks) & 1) * 256;
+                float* vf = vtabf + ((js / Cfg::kBlocks) & 1) * 256;
                 {
                     const int j = sel * 128 + row;
-                    if (j < Q) vb[j] = __float2bfloat16_rn(exp2f(gv[j | 31] - gv[j]) * dv[j]);
+                    if (j < Q) {
+                        const float vj = exp2f(gv[j | 31] - gv[j]) * dv[j];
+                        vb[j] = __float2bfloat16_rn(vj);
+                        vf[j] = vj;
+                    }
                 }
                 named_bar_sync(1, 256);
                 const uint32_t* vb32 = reinterpret_cast<const uint32_t*>(vb);
@@ -426,10 +432,16 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             uint32_t cbv[16];
                             tmem_ld_x16(tmem + lane_off + cbsrc + blk + jl0 / 2, cbv);
                             tmem_wait_ld();
+                            // Factorised decay 2^{g_i - g_j} = 2^{g_i - g_e} 2^{g_e - g_j} with
+                            // e the chunk's last key: below the diagonal chunk both factors
+                            // are <= 1.  On the diagonal chunk the row factor may exceed 1
+                            // (by at most the chunk's decay span), so the factorised form is
+                            // used there only when that span is small enough to stay far from
+                            // overflow; the entries above the diagonal are dropped by a
+                            // select.  Otherwise the exact per-element exponent is used.
+                            const float span = gv[j0] - gv[j0 + 31];   // >= 0, warp-uniform
+                            const float uu = exp2f(gi_ - gv[j0 + 31]);
                             if (kc < dch) {
-                                // whole chunk at or below the row: factorised decay,
-                                // 2^{g_i - g_j} = 2^{g_i - g_e} 2^{g_e - g_j}, both <= 1
-                                const float uu = exp2f(gi_ - gv[j0 + 31]);
                                 const __nv_bfloat162 u2 = __floats2bfloat162_rn(uu, uu);
 #pragma unroll
                                 for (int e = 0; e < 16; ++e) {
@@ -437,8 +449,25 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                     const __nv_bfloat162 v2 = as_bf162(vb32[j0 / 2 + e]);
                                     o[e] = as_u32(__hmul2(__hmul2(c2, v2), u2));
                                 }
+                            } else if (span < 64.f) {
+                                // diagonal chunk, moderate decay span: the same factors in
+                                // fp32 (one rounding, as for the exact form), masked by a select
+                                const float4* vq = reinterpret_cast<const float4*>(vf + j0);
+#pragma unroll
+                                for (int e4 = 0; e4 < 8; ++e4) {
+                                    const float4 vv = vq[e4];
+                                    const int ja = j0 + 4 * e4;
+                                    const uint32_t c01 = cbv[2 * e4], c23 = cbv[2 * e4 + 1];
+                                    const float a0 = (ja <= i) ? bf16lo(c01) * (vv.x * uu) : 0.f;
+                                    const float a1 = (ja + 1 <= i) ? bf16hi(c01) * (vv.y * uu) : 0.f;
+                                    const float a2 = (ja + 2 <= i) ? bf16lo(c23) * (vv.z * uu) : 0.f;
+                                    const float a3 = (ja + 3 <= i) ? bf16hi(c23) * (vv.w * uu) : 0.f;
+                                    o[2 * e4] = pack_bf16(a0, a1);
+                                    o[2 * e4 + 1] = pack_bf16(a2, a3);
+                                }
                             } else {
-                                // diagonal chunk: exact exponent, masked by a select
+                                // diagonal chunk with a large decay span: exact exponent,
+                                // masked by a select
 #pragma unroll
                                 for (int e = 0; e < 16; ++e) {
                                     const int ja = j0 + 2 * e, jc = ja + 1;
