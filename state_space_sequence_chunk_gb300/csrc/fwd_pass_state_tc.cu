@@ -69,10 +69,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&t);
 }
-__device__ __forceinline__ uint32_t mul_bf162(uint32_t a, __nv_bfloat162 b) {
-    __nv_bfloat162 t = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), b);
-    return *reinterpret_cast<uint32_t*>(&t);
-}
 
 template <int PP>
 __global__ void __launch_bounds__(kThreads, FpsCfg<PP>::kMinBlocks)
@@ -181,14 +177,15 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
 #pragma unroll
             for (int v = tid; v < kVecs; v += 32 * kScalerWarps) {
                 const int box = v / (kSub * 8), r = (v / 8) % kSub, q = v % 8;
-                // the row scale rounded to bf16 once, then packed bf16x2 products
-                const __nv_bfloat162 s2 = __float2bfloat162_rn(dv[r] * exp2f(glast - gv[r]));
+                // fp32 products, one rounding to bf16 (as the pages' cast of the
+                // scaled operand)
+                const float sc = dv[r] * exp2f(glast - gv[r]);
                 uint4* ptr = reinterpret_cast<uint4*>(xs + box * kSub * kRowBytes + r * kRowBytes) + q;
                 uint4 w = *ptr;
-                w.x = mul_bf162(w.x, s2);
-                w.y = mul_bf162(w.y, s2);
-                w.z = mul_bf162(w.z, s2);
-                w.w = mul_bf162(w.w, s2);
+                w.x = pack_bf16(bf16lo(w.x) * sc, bf16hi(w.x) * sc);
+                w.y = pack_bf16(bf16lo(w.y) * sc, bf16hi(w.y) * sc);
+                w.z = pack_bf16(bf16lo(w.z) * sc, bf16hi(w.z) * sc);
+                w.w = pack_bf16(bf16lo(w.w) * sc, bf16hi(w.w) * sc);
                 *ptr = w;
             }
             fence_proxy_async_smem();
