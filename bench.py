@@ -348,6 +348,7 @@ def main():
     off = (gb + 255) // 256 * 256
     dtT = ws[off:off + gb].view(torch.float32)
     hid = ws[2 * off:2 * off + hb]
+    scr = ws[2 * off + (hb + 255) // 256 * 256:]   # fwd_pass_state scratch (the rest)
     P = ctypes.c_void_p
     ptr = lambda t: None if t is None else P(t.data_ptr())
     st = P(stream.cuda_stream)
@@ -355,7 +356,8 @@ def main():
                                                          ptr(gcs), ptr(dtT), st),
             "fwd_pass_state": lambda: lib.ssd_fwd_pass_state(ctypes.byref(dims), ptr(x), ptr(B),
                                                              ptr(gcs), ptr(dtT), ptr(init),
-                                                             ptr(hid), ptr(fin), st),
+                                                             ptr(hid), ptr(fin), ptr(scr),
+                                                             ctypes.c_size_t(scr.numel()), st),
             "compute_out": lambda: lib.ssd_compute_out(ctypes.byref(dims), ptr(x), ptr(B),
                                                        ptr(C), ptr(gcs), ptr(dtT), ptr(hid),
                                                        ptr(D), ptr(y), st)}

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 1
+#define SSD_ABI_VERSION 2
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
@@ -86,7 +86,8 @@ int ssd_abi_version(void);
 const char* ssd_status_string(ssd_status s);
 
 /* Bytes of device workspace that ssd_fwd needs for `d` (the Gcs, dtT and
- * hiddens intermediates, each 256-byte aligned); 0 if `d` is invalid or empty. */
+ * hiddens intermediates and fwd_pass_state's scratch, each 256-byte aligned);
+ * 0 if `d` is invalid or empty. */
 size_t ssd_fwd_workspace_bytes(const ssd_dims* d);
 
 /* Byte sizes of the two intermediate kinds: Gcs (== dtT) and hiddens.  Returns
@@ -106,7 +107,9 @@ ssd_status ssd_intermediate_bytes(const ssd_dims* d, size_t* gcs_bytes, size_t* 
  *                       overlap with an input is SSD_ERR_ALIAS.
  *   workspace           device scratch of >= ssd_fwd_workspace_bytes(d) bytes,
  *                       owned by the caller; its contents on entry do not
- *                       matter and on exit hold Gcs, dtT and hiddens.
+ *                       matter and on exit hold Gcs, dtT and hiddens (in that
+ *                       order, each 256-byte aligned) and fwd_pass_state's
+ *                       scratch.
  */
 ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const float* A,
                    const void* B, const void* C, const float* D, const float* init_state,
@@ -123,6 +126,12 @@ ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const floa
 ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A,
                             float* Gcs, float* dtT, void* stream);
 
+/* Bytes of device scratch that ssd_fwd_pass_state needs for `d`: for bf16, a
+ * two-slot fp32 state buffer per (batch, head, 128-row block of N), through
+ * which the units of one head's chunk sequence hand the state on, and a small
+ * control block; 0 for fp32, or if `d` is invalid or empty. */
+size_t ssd_fwd_pass_state_scratch_bytes(const ssd_dims* d);
+
 /*
  * ssd_fwd_pass_state -- step 2 ("Kernel 2: fwd_pass_state").
  * For every (b, h), walking the chunks in order from S = init_state (or 0):
@@ -130,10 +139,16 @@ ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A,
  *   S <- 2^{g_last} S + X_c^T (B_c o (dt_c 2^{g_last - g_c}))
  * where g = Gcs of chunk c and g_last its value at the chunk's last real token.
  * final_state (fp32, may be NULL, may equal init_state) receives the last S.
+ * scratch: device memory of >= ssd_fwd_pass_state_scratch_bytes(d) bytes
+ * (NULL allowed when that is 0), owned by the caller, contents on entry
+ * irrelevant (the call clears what it needs on `stream` first); it must not
+ * overlap any other argument (SSD_ERR_ALIAS), and a smaller size is
+ * SSD_ERR_WORKSPACE.  Two calls that overlap on the GPU must not share it.
  */
 ssd_status ssd_fwd_pass_state(const ssd_dims* d, const void* x, const void* B,
                               const float* Gcs, const float* dtT, const float* init_state,
-                              void* hiddens, float* final_state, void* stream);
+                              void* hiddens, float* final_state, void* scratch,
+                              size_t scratch_bytes, void* stream);
 
 /*
  * ssd_compute_out -- step 3 ("Kernel 3: compute_out").  For every (b, chunk, h):

@@ -32,7 +32,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE"
           8: "SSD_ERR_ALIAS"}
 EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
-           "ssd_compute_out", "ssd_fwd_noalloc", "ssd_take_device_errors"]
+           "ssd_fwd_pass_state_scratch_bytes", "ssd_compute_out", "ssd_fwd_noalloc",
+           "ssd_take_device_errors"]
 
 
 class SSDError(RuntimeError):
@@ -77,7 +78,9 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_fwd.restype = ctypes.c_int
         lib.ssd_chunk_cumsum.argtypes = [dp] + [vp] * 5
         lib.ssd_chunk_cumsum.restype = ctypes.c_int
-        lib.ssd_fwd_pass_state.argtypes = [dp] + [vp] * 8
+        lib.ssd_fwd_pass_state.argtypes = [dp] + [vp] * 8 + [sz, vp]
+        lib.ssd_fwd_pass_state_scratch_bytes.argtypes = [dp]
+        lib.ssd_fwd_pass_state_scratch_bytes.restype = sz
         lib.ssd_fwd_pass_state.restype = ctypes.c_int
         lib.ssd_compute_out.argtypes = [dp] + [vp] * 9
         lib.ssd_compute_out.restype = ctypes.c_int
@@ -179,9 +182,11 @@ def ssd_chunk_cumsum(dt, A, chunk_size: int, x_dtype=torch.bfloat16):
 
 
 def ssd_fwd_pass_state(x, B, Gcs, dtT, init_state=None, chunk_size: int = 256,
-                       return_final_state: bool = True):
+                       return_final_state: bool = True, scratch=None):
     """Step 2: returns ``(hiddens [b, H, nc, N, P] in x.dtype, final_state)``;
-    hiddens[b, h, c] is the chunk-start state transposed."""
+    hiddens[b, h, c] is the chunk-start state transposed.  ``scratch`` (uint8
+    device tensor of at least ssd_fwd_pass_state_scratch_bytes) is allocated
+    here when not given."""
     lib = load_library()
     dims = dims_for(x, B, chunk_size)
     b, L, H, P = x.shape
@@ -189,8 +194,13 @@ def ssd_fwd_pass_state(x, B, Gcs, dtT, init_state=None, chunk_size: int = 256,
     nc = (L + chunk_size - 1) // chunk_size
     hid = torch.empty((b, H, nc, N, P), dtype=x.dtype, device=x.device)
     fin = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device) if return_final_state else None
+    need = int(lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(dims)))
+    if scratch is None and need > 0:
+        scratch = torch.empty(need, dtype=torch.uint8, device=x.device)
+    nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
     _check(lib.ssd_fwd_pass_state(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(Gcs), _ptr(dtT),
-                                  _ptr(init_state), _ptr(hid), _ptr(fin), _stream()))
+                                  _ptr(init_state), _ptr(hid), _ptr(fin), _ptr(scratch), nbytes,
+                                  _stream()))
     return hid, fin
 
 

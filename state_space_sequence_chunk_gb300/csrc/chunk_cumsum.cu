@@ -26,8 +26,11 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
 chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
                     float* __restrict__ Gcs, float* __restrict__ dtT,
-                    int L, int H, int Q, int Lp) {
+                    int L, int H, int Q, int Lp, unsigned int* zero_ptr, int zero_words) {
     __shared__ float tile[256][kHeadsPerCta + 1];
+    // the first CTA also clears the next kernel's control block
+    if (zero_ptr != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < zero_words; i += kThreads) zero_ptr[i] = 0u;
     static_assert(kThreads / 32 == kHeadsPerCta, "one warp per head column");
     const int c = blockIdx.x, h0 = blockIdx.y * kHeadsPerCta, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,11 +85,13 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
 }  // namespace
 
 cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* Gcs,
-                                float* dtT, cudaStream_t stream) {
+                                float* dtT, unsigned int* zero_ptr, int zero_words,
+                                cudaStream_t stream) {
     dim3 grid((unsigned)p.nc, (unsigned)((p.H + kHeadsPerCta - 1) / kHeadsPerCta),
               (unsigned)p.b);
     chunk_cumsum_kernel<<<grid, kThreads, 0, stream>>>(dt, A, Gcs, dtT, (int)p.L, (int)p.H,
-                                                        (int)p.Q, (int)p.Lp);
+                                                        (int)p.Q, (int)p.Lp, zero_ptr,
+                                                        zero_words);
     return cudaGetLastError();
 }
 

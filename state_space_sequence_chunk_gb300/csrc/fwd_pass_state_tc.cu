@@ -13,26 +13,39 @@
 //    state dimension N is the MMA's M (128 TMEM lanes).  The zhiding.cn
 //    rendering, "Mamba-2性能优化" (swapping the A/B operands), describes the same
 //    B^T A^T = (A B)^T swap for Blackwell.
-//  * Every chunk's product D_c = B_c^T (s o X_c) goes into a FRESH TMEM
-//    accumulator, and the epilogue warps fold it into the running state kept
-//    in a second TMEM region, S <- 2^{g_last} S + D_c.  The tensor core never
-//    waits for the previous chunk's state, only for the epilogue to have read
-//    the accumulator; keeping S in TMEM keeps registers low enough for four
-//    CTAs per SM, so that a full batch*head grid is resident at once.
-//  * x and B stream in 32-token sub-chunks through a multi-stage TMA ring
-//    (128-byte swizzle, token-major rows, read as MN-major operands).  The
-//    per-token scale s_q = dt_q 2^{g_last - g_q} is applied to the x rows in
-//    shared memory (a row is contiguous in the swizzled tile).
+//  * A chain is the state block that one CTA carries: (batch, head, 128-row
+//    block of N, 64-column block of P).  Its chunks are walked in order.  So
+//    that every SM gets the same work whatever the number of chains (batch *
+//    head rarely divides evenly over 152 SMs), the chains x chunks work units,
+//    laid out chain after chain, are cut into one equal contiguous range per
+//    resident CTA.  A range holds the tail of one chain, whole chains and the
+//    head of another.  A CTA walks its head piece first and publishes the
+//    state at its end (fp32, in a two-slot buffer per chain kept in L2), then
+//    its whole chains, then its tail piece, which starts from the state that
+//    the previous range's CTA published.  Ranges are longer than chains
+//    whenever there is more work than CTAs per chain, so that state is ready
+//    long before it is needed; every wait is bounded anyway, and ranges are
+//    handed out in dispatch order, so a waited-for CTA is always running.
+//  * The chunk products D_c = B_c^T (s o X_c) need no state, so the tensor core
+//    runs ahead through three TMEM accumulators while the fold warps apply
+//    hiddens[c] = S, S <- 2^{g_last} S + D_c, with S in a fourth TMEM slot.
+//  * x and B stream in 64-token sub-chunks through a 4-stage TMA ring
+//    (128-byte swizzle, token-major rows, read as MN-major operands); g and dt
+//    of a chunk arrive once per chunk in a separate two-slot ring.  Few, large
+//    copies matter: the TMA issue cost per copy, not the bytes, bounded the
+//    rate of smaller stages.  The per-token scale s_q = dt_q 2^{g_last - g_q}
+//    is applied to the x rows in shared memory (a row is contiguous in the
+//    swizzled tile).
 //
-// Warp roles (320 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
-// 2..5 row scalers, 6..9 state warps (the state update at each chunk
-// boundary; TMEM lane quarter = warp % 4).  TMEM: columns
-// [0, PP) accumulator, [PP, 2 PP) state S^T (lane = state row n, column = p).
+// Warp roles (384 threads, two CTAs per SM): 0 TMA producer, 1 MMA issuer (and
+// TMEM owner), 2..7 row scalers, 8..11 fold warps (TMEM lane quarter =
+// warp % 4).  TMEM: three accumulator slots and the state, 64 columns each.
 //
-// CTA = (128-row block of N, batch * head).  N and P are padded to the
-// 64-element swizzle atom by the TMA's zero fill; padded rows/columns are
-// computed and never stored.
+// N and P are padded to the 64-element swizzle atom by the TMA's zero fill;
+// padded rows/columns are computed and never stored.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "sm100_ptx.cuh"
 #include "ssd_internal.cuh"
@@ -43,24 +56,38 @@ namespace {
 
 __device__ unsigned int g_fps_error;  // bit 0: a bounded wait gave up
 
-constexpr int kSub = 32;            // tokens per pipeline stage
+constexpr int kSub = 64;            // tokens per pipeline stage
 constexpr int kRowBytes = 128;      // one swizzle row (64 bf16)
-constexpr int kScalerWarps = 4;
-constexpr int kThreads = 32 * (2 + kScalerWarps + 4);
+constexpr int kCols = 64;           // state columns (of P) per chain
+constexpr int kScalerWarps = 6;
+constexpr int kFoldWarps = 4;
+constexpr int kThreads = 32 * (2 + kScalerWarps + kFoldWarps);
+constexpr int kAccSlots = 3;        // TMEM accumulators (chunk products in flight)
+constexpr int kStages = 4;
+constexpr int kVecSlots = 2;        // per-chunk g / dt buffers
+constexpr int kMinBlocks = 2;       // CTAs per SM
+// Register cap: two 384-thread CTAs per SM stay below the register file's
+// limit (per SM sub-partition, three warps of each CTA).
+constexpr int kMaxRegs = 80;
+constexpr int kXBytes = kSub * kCols * 2;          // x sub-tile
+constexpr int kBBytes = kSub * 128 * 2;            // B sub-tile (128 state rows)
+constexpr int kStageBytes = kXBytes + kBBytes;     // multiple of 1024
+constexpr int kMaxQ = 256;
+constexpr int kVecSlotBytes = 2 * kMaxQ * 4;       // g[Q], dt[Q] of one chunk
+constexpr int kStateCol = kAccSlots * kCols;       // TMEM column of the running state
+constexpr int kTmemCols = 256;                     // 3 accumulators + the state, power of two
+constexpr int kBarBytes = 512;
+constexpr int kSmem = kStages * kStageBytes + kVecSlots * kVecSlotBytes + kBarBytes + 1024;
+constexpr uint32_t kIdesc = make_idesc(1, 128, kCols, 1, 1);
+constexpr int kSlotFloats = 128 * kCols;           // one state slot of the hand-off buffer
+static_assert(kStateCol + kCols <= kTmemCols, "TMEM layout");
+static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 
-template <int PP>
-struct FpsCfg {
-    static constexpr int kStages = 5;
-    static constexpr int kMinBlocks = PP == 64 ? 3 : 2;   // CTAs per SM (TMEM: 2*PP each)
-    static constexpr int kXBytes = kSub * PP * 2;         // x sub-tile
-    static constexpr int kBBytes = kSub * 128 * 2;        // B sub-tile (128 state rows)
-    static constexpr int kVecOff = kXBytes + kBBytes;     // g[kSub], dt[kSub], last 4 g of the chunk
-    static constexpr int kVecBytes = 2 * kSub * 4 + 16;
-    static constexpr int kStageBytes = (kVecOff + kVecBytes + 1023) / 1024 * 1024;
-    static constexpr int kTmemCols = 2 * PP;              // accumulator + state
-    static constexpr int kBarBytes = 256;
-    static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
-    static constexpr uint32_t kIdesc = make_idesc(1, 128, PP, 1, 1);
+struct FpsParams {
+    int H, P, N, Q, nc, Lp, hpg;
+    int nmb, npb, nchains;   // row blocks of N, column blocks of P, chains
+    int W;                   // work units: nchains * nc (< 2^31, checked on the host)
+    int G;                   // CTAs (ranges)
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -70,31 +97,79 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
-template <int PP>
-__global__ void __launch_bounds__(kThreads, FpsCfg<PP>::kMinBlocks)
+// The work range of range index k and the order of its pieces.  Units are
+// numbered chain * nc + chunk; range k is [k W / G, (k+1) W / G).
+struct Range {
+    int lo, hi;
+    int ch_first, ch_last;
+    bool first_is_tail;   // the first chain's piece starts mid-chain (waits for a state)
+    bool last_is_head;    // the last chain's piece ends mid-chain (publishes a state)
+    __device__ int pieces() const { return ch_last - ch_first + 1; }
+    // chain of the i-th piece in processing order: head piece, whole chains, tail piece
+    __device__ int chain_at(int i) const {
+        if (ch_first == ch_last) return ch_first;
+        if (last_is_head) {
+            if (i == 0) return ch_last;
+            --i;
+        }
+        const int mid_lo = ch_first + (first_is_tail ? 1 : 0);
+        const int mid_hi = ch_last - (last_is_head ? 1 : 0);
+        return i <= mid_hi - mid_lo ? mid_lo + i : ch_first;
+    }
+};
+__device__ __forceinline__ Range range_of(int k, const FpsParams& q) {
+    Range r;
+    r.lo = (int)((long long)k * q.W / q.G);
+    r.hi = (int)((long long)(k + 1) * q.W / q.G);
+    r.ch_first = r.lo / q.nc;
+    r.ch_last = (r.hi - 1) / q.nc;
+    r.first_is_tail = r.lo > r.ch_first * q.nc;
+    r.last_is_head = r.hi < (r.ch_last + 1) * q.nc;
+    return r;
+}
+// One piece: chunks [c0, c1) of chain ch = (bh*nmb + mb)*npb + pb.
+struct Piece {
+    int ch, bh, mb, pb, c0, c1;
+};
+__device__ __forceinline__ Piece piece_of(const Range& r, int i, const FpsParams& q) {
+    Piece u;
+    u.ch = r.chain_at(i);
+    const int base = u.ch * q.nc;
+    u.c0 = max(r.lo - base, 0);
+    u.c1 = min(r.hi - base, q.nc);
+    const int rb = u.ch / q.npb;
+    u.pb = u.ch - rb * q.npb;
+    u.bh = rb / q.nmb;
+    u.mb = rb - u.bh * q.nmb;
+    return u;
+}
+
+__global__ void __maxnreg__(kMaxRegs)
 fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                   const float* __restrict__ Gcs, const float* __restrict__ dtT, const float* init,
-                  __nv_bfloat16* __restrict__ hiddens, float* final_state, int H, int P, int N,
-                  int Q, int nc, int Lp, int hpg) {
-    using Cfg = FpsCfg<PP>;
-    constexpr int S = Cfg::kStages;
+                  __nv_bfloat16* __restrict__ hiddens, float* final_state, float* ring,
+                  unsigned int* ctrl, const FpsParams q) {
+    constexpr int S = kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
+    uint8_t* vecs = smem + S * kStageBytes;   // kVecSlots x (g[Q], dt[Q])
+    uint64_t* bars = reinterpret_cast<uint64_t*>(vecs + kVecSlots * kVecSlotBytes);
     // barrier indices
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto scaled = [&](int s) { return smem_u32(bars + S + s); };
     auto empty = [&](int s) { return smem_u32(bars + 2 * S + s); };
-    const uint32_t acc_full = smem_u32(bars + 3 * S);
-    const uint32_t acc_empty = smem_u32(bars + 3 * S + 1);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 2);
+    auto acc_full = [&](int k) { return smem_u32(bars + 3 * S + k); };
+    auto acc_empty = [&](int k) { return smem_u32(bars + 3 * S + kAccSlots + k); };
+    auto vec_full = [&](int v) { return smem_u32(bars + 3 * S + 2 * kAccSlots + v); };
+    auto vec_empty = [&](int v) { return smem_u32(bars + 3 * S + 2 * kAccSlots + kVecSlots + v); };
+    const uint32_t fold_done = smem_u32(bars + 3 * S + 2 * kAccSlots + 2 * kVecSlots);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 2 * kAccSlots + 2 * kVecSlots + 1);
+    int* range_id = reinterpret_cast<int*>(tmem_holder + 1);
 
-    const int mb = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / H, h = bh % H, grp = h / hpg;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nsub = Q / kSub;
-    const int total = nc * nsub;
+    const int nsub = q.Q / kSub;
+    unsigned int* flags = ctrl + kCtrlFlagOffset;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -102,182 +177,281 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             mbar_init(scaled(s), 32 * kScalerWarps);
             mbar_init(empty(s), 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 128);
+        for (int k = 0; k < kAccSlots; ++k) {
+            mbar_init(acc_full(k), 1);
+            mbar_init(acc_empty(k), 32 * kFoldWarps);
+        }
+        for (int v = 0; v < kVecSlots; ++v) {
+            mbar_init(vec_full(v), 1);
+            mbar_init(vec_empty(v), 32 * kScalerWarps);
+        }
+        mbar_init(fold_done, kFoldWarps);
         fence_mbar_init();
+        // ranges in dispatch order: the range before this one belongs to a CTA
+        // that is already running
+        *range_id = (int)atomicAdd(ctrl, 1u);
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const uint32_t stage0 = smem_u32(smem);
+    const int rk = *range_id;
+    const Range rg = range_of(rk, q);
+    const int nchunks = rg.hi - rg.lo;
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            for (int i = 0; i < total; ++i) {
-                const int s = i % S, k = i / S;
-                mbar_wait(empty(s), (k & 1) ^ 1, &g_fps_error, 1u);
-                const uint32_t xs = stage0 + s * Cfg::kStageBytes, bs = xs + Cfg::kXBytes;
-                const int c = i / nsub, sub = i % nsub;
-                const int t = c * Q + sub * kSub;
-                mbar_arrive_expect_tx(full(s), Cfg::kXBytes + Cfg::kBBytes + Cfg::kVecBytes);
+            int i = 0;   // stage counter
+            int cv = 0;  // chunk counter (g / dt ring position)
+            bool ok = true;
+            for (int pi = 0; pi < rg.pieces() && ok; ++pi) {
+                const Piece u = piece_of(rg, pi, q);
+                const int b = u.bh / q.H, h = u.bh - b * q.H, grp = h / q.hpg;
+                const int64_t ro = (int64_t)u.bh * q.Lp;
+                for (int c = u.c0; c < u.c1 && ok; ++c, ++cv) {
+                    // g and dt of the chunk, once per chunk
+                    const int vslot = cv % kVecSlots;
+                    if (!mbar_wait(vec_empty(vslot), ((cv / kVecSlots) & 1) ^ 1, &g_fps_error, 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vs = smem_u32(vecs + vslot * kVecSlotBytes);
+                    mbar_arrive_expect_tx(vec_full(vslot), 2 * q.Q * 4);
+                    bulk_load(vs, Gcs + ro + (int64_t)c * q.Q, q.Q * 4, vec_full(vslot));
+                    bulk_load(vs + kMaxQ * 4, dtT + ro + (int64_t)c * q.Q, q.Q * 4, vec_full(vslot));
+                    for (int sub = 0; sub < nsub; ++sub, ++i) {
+                        const int s = i % S, k = i / S;
+                        if (!mbar_wait(empty(s), (k & 1) ^ 1, &g_fps_error, 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t xs = stage0 + s * kStageBytes, bs = xs + kXBytes;
+                        const int tok = c * q.Q + sub * kSub;
+                        mbar_arrive_expect_tx(full(s), kXBytes + kBBytes);
+                        tma_load_4d(xs, &tm_x, full(s), u.pb * kCols, h, tok, b);
 #pragma unroll
-                for (int j = 0; j < PP / 64; ++j)
-                    tma_load_4d(xs + j * kSub * kRowBytes, &tm_x, full(s), j * 64, h, t, b);
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    tma_load_4d(bs + j * kSub * kRowBytes, &tm_b, full(s), mb * 128 + j * 64, grp,
-                                t, b);
-                const int64_t ro = (int64_t)bh * Lp;
-                const uint32_t vs = xs + Cfg::kVecOff;
-                bulk_load(vs, Gcs + ro + t, kSub * 4, full(s));
-                bulk_load(vs + kSub * 4, dtT + ro + t, kSub * 4, full(s));
-                bulk_load(vs + 2 * kSub * 4, Gcs + ro + (int64_t)c * Q + Q - 4, 16, full(s));
+                        for (int jb = 0; jb < 2; ++jb)
+                            tma_load_4d(bs + jb * kSub * kRowBytes, &tm_b, full(s),
+                                        u.mb * 128 + jb * 64, grp, tok, b);
+                    }
+                }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- MMA issuer: one chunk product per accumulator slot ----------------
         if (lane == 0) {
-            for (int i = 0; i < total; ++i) {
-                const int s = i % S, k = i / S;
-                const int c = i / nsub, sub = i % nsub;
-                // the epilogue has read the previous chunk's product
-                if (sub == 0) mbar_wait(acc_empty, (c & 1) ^ 1, &g_fps_error, 1u);
-                mbar_wait(scaled(s), k & 1, &g_fps_error, 1u);
-                tc_fence_after();
-                const uint32_t xs = stage0 + s * Cfg::kStageBytes, bs = xs + Cfg::kXBytes;
-                // A = B_c^T: M = 128 state rows (two 64-row swizzle atoms, kSub*128
-                // bytes apart), K = 16 tokens, MN-major.  B = s o X_c: N = PP columns
-                // of P, K = 16 tokens, MN-major.  Descriptors are built once; a K
-                // step adds a compile-time offset to the start-address field.
-                const uint64_t ad0 = smem_desc_sw128(bs, kSub * kRowBytes, 8 * kRowBytes);
-                const uint64_t bd0 = smem_desc_sw128(xs, kSub * kRowBytes, 8 * kRowBytes);
+            int i = 0;
+            for (int qc = 0; qc < nchunks; ++qc) {
+                const int slot = qc % kAccSlots;
+                bool ok = true;
+                for (int sub = 0; sub < nsub; ++sub, ++i) {
+                    const int s = i % S, k = i / S;
+                    if (!mbar_wait(scaled(s), k & 1, &g_fps_error, 1u)) { ok = false; break; }
+                    // the fold warps have read this slot's previous product
+                    if (sub == 0 &&
+                        !mbar_wait(acc_empty(slot), ((qc / kAccSlots) & 1) ^ 1, &g_fps_error, 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = stage0 + s * kStageBytes, bs = xs + kXBytes;
+                    // A = B_c^T: M = 128 state rows (two 64-row swizzle atoms, kSub*128
+                    // bytes apart), K = 16 tokens, MN-major.  B = s o X_c: N = 64 columns
+                    // of P, K = 16 tokens, MN-major.  A K step adds a compile-time offset
+                    // to the start-address field.
+                    const uint64_t ad0 = smem_desc_sw128(bs, kSub * kRowBytes, 8 * kRowBytes);
+                    const uint64_t bd0 = smem_desc_sw128(xs, kSub * kRowBytes, 8 * kRowBytes);
 #pragma unroll
-                for (int kk = 0; kk < kSub / 16; ++kk)
-                    mma_f16_ss(tmem, ad0 + (uint64_t)((kk * 16 * kRowBytes) >> 4),
-                               bd0 + (uint64_t)((kk * 16 * kRowBytes) >> 4), Cfg::kIdesc,
-                               (sub > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(empty(s));
-                if (sub == nsub - 1) mma_commit(acc_full);
+                    for (int kk = 0; kk < kSub / 16; ++kk)
+                        mma_f16_ss(tmem + slot * kCols, ad0 + (uint64_t)((kk * 16 * kRowBytes) >> 4),
+                                   bd0 + (uint64_t)((kk * 16 * kRowBytes) >> 4), kIdesc,
+                                   (sub > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(empty(s));
+                    if (sub == nsub - 1) mma_commit(acc_full(slot));
+                }
+                if (!ok) break;
             }
         }
     } else if (warp < 2 + kScalerWarps) {
         // ---------------- scaler warps: x_q <- x_q * dt_q 2^{g_last - g_q} ----------------
+        // 16-byte vectors of the stage's x tile (kSub rows x 8) dealt round-robin.
         const int tid = threadIdx.x - 64;
-        for (int i = 0; i < total; ++i) {
+        constexpr int kVecs = kSub * 8;
+        constexpr int kPer = (kVecs + 32 * kScalerWarps - 1) / (32 * kScalerWarps);
+        const int nstages = nchunks * nsub;
+        for (int i = 0; i < nstages; ++i) {
             const int s = i % S, k = i / S;
-            mbar_wait(full(s), k & 1, &g_fps_error, 1u);
-            uint8_t* xs = smem + s * Cfg::kStageBytes;
-            const float* gv = reinterpret_cast<const float*>(xs + Cfg::kVecOff);
-            const float* dv = gv + kSub;
-            const float glast = gv[2 * kSub + 3];
-            constexpr int kVecs = kSub * (PP / 64) * 8;   // 16-byte vectors in the x sub-tile
+            const int cv = i / nsub, sub = i - cv * nsub, vslot = cv % kVecSlots;
+            if (!mbar_wait(full(s), k & 1, &g_fps_error, 1u)) break;
+            if (sub == 0 && !mbar_wait(vec_full(vslot), (cv / kVecSlots) & 1, &g_fps_error, 1u)) break;
+            const float* gchunk = reinterpret_cast<const float*>(vecs + vslot * kVecSlotBytes);
+            const float* gv = gchunk + sub * kSub;
+            const float* dv = gv + kMaxQ;
+            const float glast = gchunk[q.Q - 1];
+            uint8_t* xs = smem + s * kStageBytes;
 #pragma unroll
-            for (int v = tid; v < kVecs; v += 32 * kScalerWarps) {
-                const int box = v / (kSub * 8), r = (v / 8) % kSub, q = v % 8;
-                // fp32 products, one rounding to bf16 (as the pages' cast of the
-                // scaled operand)
-                const float sc = dv[r] * exp2f(glast - gv[r]);
-                uint4* ptr = reinterpret_cast<uint4*>(xs + box * kSub * kRowBytes + r * kRowBytes) + q;
-                uint4 w = *ptr;
-                w.x = pack_bf16(bf16lo(w.x) * sc, bf16hi(w.x) * sc);
-                w.y = pack_bf16(bf16lo(w.y) * sc, bf16hi(w.y) * sc);
-                w.z = pack_bf16(bf16lo(w.z) * sc, bf16hi(w.z) * sc);
-                w.w = pack_bf16(bf16lo(w.w) * sc, bf16hi(w.w) * sc);
-                *ptr = w;
+            for (int kq = 0; kq < kPer; ++kq) {
+                const int v = tid + kq * 32 * kScalerWarps;
+                if (v < kVecs) {
+                    const int r = v >> 3;
+                    // fp32 scale, one rounding to bf16 per product (as the pages'
+                    // cast of the scaled operand)
+                    const float sc = dv[r] * exp2f(glast - gv[r]);
+                    uint4* ptr = reinterpret_cast<uint4*>(xs + r * kRowBytes) + (v & 7);
+                    uint4 w = *ptr;
+                    w.x = pack_bf16(bf16lo(w.x) * sc, bf16hi(w.x) * sc);
+                    w.y = pack_bf16(bf16lo(w.y) * sc, bf16hi(w.y) * sc);
+                    w.z = pack_bf16(bf16lo(w.z) * sc, bf16hi(w.z) * sc);
+                    w.w = pack_bf16(bf16lo(w.w) * sc, bf16hi(w.w) * sc);
+                    *ptr = w;
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(scaled(s));
+            if (sub == nsub - 1) mbar_arrive(vec_empty(vslot));
         }
     } else {
-        // ---------------- state warps (the last four): the state update ----------------
-        // Each thread owns TMEM lane (state row n) 32*(warp%4) + lane and, at each
-        // chunk boundary, folds the finished chunk product into S.
+        // ---------------- fold warps: hiddens[c] = S, S <- 2^{g_last} S + D_c ----------------
+        // Thread = TMEM lane = state row n of the chain's 128-row block.  The
+        // running state S^T lives in TMEM columns [kStateCol, kStateCol + 64).  A
+        // hand-off slot holds S^T as [16][128 rows][4] fp32, so that a warp's
+        // float4 accesses cover 512 contiguous bytes.  Every exit from this loop
+        // is warp-uniform: the warp-collective TMEM accesses and __syncwarp calls
+        // never wait for a lane that has left.
         const int quarter = warp & 3;
-        const int n = mb * 128 + quarter * 32 + lane;
-        const bool nok = n < N;
-        const uint32_t acc_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t st_addr = acc_addr + PP;
-        const int64_t sbase = (int64_t)bh * P * N;
-        // S^T row n <- init_state[b, h, :, n] (or 0)
+        const int rl = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t st_addr = lane_base + kStateCol;
+        int qc = 0;  // chunk counter (accumulator ring position)
+        for (int pi = 0; pi < rg.pieces(); ++pi) {
+            const Piece u = piece_of(rg, pi, q);
+            const int n = u.mb * 128 + rl;
+            const bool nok = n < q.N;
+            const int p0 = u.pb * kCols;
+            const int64_t sbase = (int64_t)u.bh * q.P * q.N;
+            const float* grow = Gcs + (int64_t)u.bh * q.Lp + q.Q - 1;   // g_last of chunk c: grow[c*Q]
+            float gl_next = grow[(int64_t)u.c0 * q.Q];
+            // the piece's initial state -> TMEM
+            if (u.c0 == 0) {
+                const float* ip = init + sbase + (int64_t)p0 * q.N + n;
+                const int pl = (init != nullptr && nok) ? q.P - p0 : 0;   // valid columns
 #pragma unroll
-        for (int j = 0; j < PP / 16; ++j) {
-            __syncwarp();
-            uint32_t r[16];
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    uint32_t v[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const int p = 16 * j + q;
-                r[q] = __float_as_uint((init != nullptr && nok && p < P)
-                                           ? init[sbase + (int64_t)p * N + n] : 0.f);
-            }
-            tmem_st_x16(st_addr + 16 * j, r);
-        }
-        tmem_wait_st();
-        // S <- 2^{g_last(c)} S + D_c, storing the chunk-start S^T to hiddens[c]
-        auto chunk_update = [&](int c, float gl) {
-            const float e = exp2f(gl);
-            // hiddens[b, h, c] is stored transposed: row n holds S[:, n] (P values)
-            __nv_bfloat16* hp = hiddens + (((int64_t)bh * nc + c) * N + n) * P;
-            mbar_wait(acc_full, c & 1, &g_fps_error, 1u);
-            tc_fence_after();
+                    for (int k = 0; k < 16; ++k)
+                        v[k] = __float_as_uint(16 * jj + k < pl ? ip[(int64_t)(16 * jj + k) * q.N] : 0.f);
+                    __syncwarp();
+                    tmem_st_x16(st_addr + 16 * jj, v);
+                }
+            } else {
+                // the state published by the CTA of the previous range
+                bool ok = true;
+                if (lane == 0) ok = flag_wait_geq(flags + u.ch, (unsigned)u.c0, &g_fps_error, 1u);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                (void)ld_acquire_gpu(flags + u.ch);  // this lane's own acquire of the hand-off
+                const float* src = ring + ((int64_t)u.ch * 2 + ((rk - 1) & 1)) * kSlotFloats;
 #pragma unroll
-            for (int j = 0; j < PP / 16; ++j) {
-                // tcgen05.ld/st are warp-collective: every lane runs them, and the
-                // warp is reconverged after the per-lane stores below
-                __syncwarp();
-                uint32_t d[16], sv[16];
-                tmem_ld_x16(acc_addr + 16 * j, d);
-                tmem_ld_x16(st_addr + 16 * j, sv);
-                tmem_wait_ld();
-                uint32_t nw[16];
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    uint32_t v[16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    nw[q] = __float_as_uint(fmaf(e, __uint_as_float(sv[q]), __uint_as_float(d[q])));
-                tmem_st_x16(st_addr + 16 * j, nw);
-                // chunk-start state (before this chunk's update) -> hiddens[c]:
-                // 16 contiguous bf16 of row n per slice (P is a multiple of 16)
-                if (nok && 16 * j < P) {
-                    uint4 w0, w1;
-                    w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
-                    w0.y = pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3]));
-                    w0.z = pack_bf16(__uint_as_float(sv[4]), __uint_as_float(sv[5]));
-                    w0.w = pack_bf16(__uint_as_float(sv[6]), __uint_as_float(sv[7]));
-                    w1.x = pack_bf16(__uint_as_float(sv[8]), __uint_as_float(sv[9]));
-                    w1.y = pack_bf16(__uint_as_float(sv[10]), __uint_as_float(sv[11]));
-                    w1.z = pack_bf16(__uint_as_float(sv[12]), __uint_as_float(sv[13]));
-                    w1.w = pack_bf16(__uint_as_float(sv[14]), __uint_as_float(sv[15]));
-                    uint4* dst = reinterpret_cast<uint4*>(hp + 16 * j);
-                    dst[0] = w0;
-                    dst[1] = w1;
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float4 f = __ldcg(reinterpret_cast<const float4*>(src + ((4 * jj + q4) * 128 + rl) * 4));
+                        v[4 * q4] = __float_as_uint(f.x); v[4 * q4 + 1] = __float_as_uint(f.y);
+                        v[4 * q4 + 2] = __float_as_uint(f.z); v[4 * q4 + 3] = __float_as_uint(f.w);
+                    }
+                    __syncwarp();
+                    tmem_st_x16(st_addr + 16 * jj, v);
                 }
             }
-            __syncwarp();
             tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-        };
-        const float* gl_src = Gcs + (int64_t)bh * Lp + Q - 1;   // g_last of each chunk
-        float gl_next = gl_src[0];
-        for (int c = 0; c < nc; ++c) {
-            const float gl = gl_next;
-            if (c + 1 < nc) gl_next = gl_src[(int64_t)(c + 1) * Q];
-            chunk_update(c, gl);
-        }
-        if (final_state != nullptr) {  // uniform: all lanes load, valid lanes store
+            bool ok = true;
+            for (int c = u.c0; c < u.c1; ++c, ++qc) {
+                const float e = exp2f(gl_next);
+                if (c + 1 < u.c1) gl_next = grow[(int64_t)(c + 1) * q.Q];
+                const int slot = qc % kAccSlots;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(acc_full(slot), (qc / kAccSlots) & 1, &g_fps_error, 1u))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t acc = lane_base + slot * kCols;
+                __nv_bfloat16* hp = hiddens + (((int64_t)u.bh * q.nc + c) * q.N + n) * q.P + p0;
 #pragma unroll
-            for (int j = 0; j < PP / 16; ++j) {
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    __syncwarp();
+                    uint32_t sv[16], d[16];
+                    tmem_ld_x16(st_addr + 16 * jj, sv);
+                    tmem_ld_x16(acc + 16 * jj, d);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        d[k] = __float_as_uint(fmaf(e, __uint_as_float(sv[k]), __uint_as_float(d[k])));
+                    tmem_st_x16(st_addr + 16 * jj, d);
+                    // chunk-start state S -> hiddens[c] (row n holds S[:, n]): 16
+                    // contiguous bf16 per slice (P is a multiple of 16)
+                    if (nok && p0 + 16 * jj < q.P) {
+                        uint4 w0, w1;
+                        w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
+                        w0.y = pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3]));
+                        w0.z = pack_bf16(__uint_as_float(sv[4]), __uint_as_float(sv[5]));
+                        w0.w = pack_bf16(__uint_as_float(sv[6]), __uint_as_float(sv[7]));
+                        w1.x = pack_bf16(__uint_as_float(sv[8]), __uint_as_float(sv[9]));
+                        w1.y = pack_bf16(__uint_as_float(sv[10]), __uint_as_float(sv[11]));
+                        w1.z = pack_bf16(__uint_as_float(sv[12]), __uint_as_float(sv[13]));
+                        w1.w = pack_bf16(__uint_as_float(sv[14]), __uint_as_float(sv[15]));
+                        uint4* hdst = reinterpret_cast<uint4*>(hp + 16 * jj);
+                        hdst[0] = w0;
+                        hdst[1] = w1;
+                    }
+                }
+                __syncwarp();
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(acc_empty(slot));
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+            // the piece's final state: to final_state, or published for the next range
+            const bool last = u.c1 == q.nc;
+            float* dst = ring + ((int64_t)u.ch * 2 + (rk & 1)) * kSlotFloats;
+            const int pl = nok ? q.P - p0 : 0;
+#pragma unroll
+            for (int jj = 0; jj < kCols / 16; ++jj) {
                 __syncwarp();
                 uint32_t sv[16];
-                tmem_ld_x16(st_addr + 16 * j, sv);
+                tmem_ld_x16(st_addr + 16 * jj, sv);
                 tmem_wait_ld();
-                if (nok) {
+                if (!last) {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        if (16 * j + q < P)
-                            final_state[sbase + (int64_t)(16 * j + q) * N + n] = __uint_as_float(sv[q]);
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        __stcg(reinterpret_cast<float4*>(dst + ((4 * jj + q4) * 128 + rl) * 4),
+                               make_float4(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1]),
+                                           __uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])));
+                } else if (final_state != nullptr) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (16 * jj + k < pl)
+                            final_state[sbase + (int64_t)(p0 + 16 * jj + k) * q.N + n] = __uint_as_float(sv[k]);
                 }
+            }
+            if (!last) {
+                // publish: every fold warp's stores, then one release of the chain's
+                // flag (a range publishes at most once)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(fold_done);
+                bool okp = true;
+                if (rl == 0) {
+                    okp = mbar_wait(fold_done, 0, &g_fps_error, 1u);
+                    if (okp) {
+                        __threadfence();
+                        st_release_gpu(flags + u.ch, (unsigned)u.c1);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, okp, 0)) break;
             }
         }
     }
@@ -286,15 +460,61 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     if (warp == 1) {
         __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
         tc_fence_after();
-        tmem_dealloc(tmem, Cfg::kTmemCols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int PP>
-cudaError_t launch_pp(const Problem& p, const void* x, const void* B, const float* Gcs,
-                      const float* dtT, const float* init, void* hid, float* fin,
-                      cudaStream_t stream) {
-    using Cfg = FpsCfg<PP>;
+int64_t chains(const Problem& p) { return p.b * p.H * ((p.N + 127) / 128) * ((p.P + 63) / 64); }
+size_t ring_bytes(const Problem& p) {
+    return round_up256((size_t)chains(p) * 2 * kSlotFloats * sizeof(float));
+}
+size_t ctrl_bytes(const Problem& p) {
+    return round_up256((size_t)(kCtrlFlagOffset + chains(p)) * sizeof(unsigned int));
+}
+
+// Resident CTA slots of the current device, from the SM count and this
+// kernel's per-CTA needs (shared memory, registers, TMEM), cached per device.
+// (The occupancy calculator reports one CTA per SM for this kernel, while two
+// run side by side.)
+cudaError_t resident_ctas(int* out) {
+    static int cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) {
+        *out = cached[dev];
+        return cudaSuccess;
+    }
+    int sms = 0, smem_sm = 0, regs_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) !=
+            cudaSuccess)
+        return e;
+    int per_sm = std::min(smem_sm / (kSmem + 1024), 512 / kTmemCols);
+    per_sm = std::min(per_sm, regs_sm / (kThreads * kMaxRegs));
+    per_sm = std::max(1, std::min(per_sm, kMinBlocks));
+    *out = sms * per_sm;
+    if (dev >= 0 && dev < 64) cached[dev] = *out;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t fwd_pass_state_scratch_bytes(const Problem& p) {
+    if (p.dtype != SSD_BF16 || p.b == 0 || p.L == 0) return 0;
+    return ring_bytes(p) + ctrl_bytes(p);
+}
+size_t fwd_pass_state_ctrl_offset(const Problem& p) { return ring_bytes(p); }
+size_t fwd_pass_state_ctrl_bytes(const Problem& p) { return ctrl_bytes(p); }
+
+cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void* B,
+                                     const float* Gcs, const float* dtT, const float* init,
+                                     void* hiddens, float* final_state, void* scratch,
+                                     cudaStream_t stream) {
+    float* ring = (float*)scratch;
+    unsigned int* ctrl = (unsigned int*)((char*)scratch + ring_bytes(p));
     CUtensorMap tx, tb;
     const uint64_t xd[4] = {(uint64_t)p.P, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
     const uint64_t xs[3] = {(uint64_t)p.P * 2, (uint64_t)p.H * p.P * 2,
@@ -308,23 +528,26 @@ cudaError_t launch_pp(const Problem& p, const void* x, const void* B, const floa
         !encode_tmap_4d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, bd, bs, box,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    auto kern = fwd_pass_state_tc<PP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(fwd_pass_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmem);
+    if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
+        e = cudaFuncSetAttribute(fwd_pass_state_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((p.N + 127) / 128), (unsigned)(p.b * p.H));
-    kern<<<grid, kThreads, Cfg::kSmem, stream>>>(tx, tb, Gcs, dtT, init, (__nv_bfloat16*)hid, fin,
-                                                 (int)p.H, (int)p.P, (int)p.N, (int)p.Q,
-                                                 (int)p.nc, (int)p.Lp, (int)p.hpg);
+    int resident = 0;
+    if ((e = resident_ctas(&resident)) != cudaSuccess) return e;
+    FpsParams q;
+    q.H = (int)p.H; q.P = (int)p.P; q.N = (int)p.N; q.Q = (int)p.Q; q.nc = (int)p.nc;
+    q.Lp = (int)p.Lp; q.hpg = (int)p.hpg;
+    q.nmb = (int)((p.N + 127) / 128);
+    q.npb = (int)((p.P + 63) / 64);
+    q.nchains = (int)chains(p);
+    if ((int64_t)q.nchains * p.nc >= (int64_t)1 << 31) return cudaErrorInvalidValue;
+    q.W = q.nchains * q.nc;
+    q.G = std::min(q.W, resident);
+    fwd_pass_state_tc<<<(unsigned)q.G, kThreads, kSmem, stream>>>(
+        tx, tb, Gcs, dtT, init, (__nv_bfloat16*)hiddens, final_state, ring, ctrl, q);
     return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void* B,
-                                     const float* Gcs, const float* dtT, const float* init,
-                                     void* hiddens, float* final_state, cudaStream_t stream) {
-    if (p.P <= 64) return launch_pp<64>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
-    return launch_pp<128>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
 }
 
 unsigned int take_fwd_pass_state_error() {

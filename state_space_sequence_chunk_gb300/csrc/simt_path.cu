@@ -248,9 +248,17 @@ cudaError_t launch_co(const Problem& p, const void* x, const void* B, const void
 
 cudaError_t launch_fwd_pass_state(const Problem& p, const void* x, const void* B,
                                   const float* Gcs, const float* dtT, const float* init,
-                                  void* hiddens, float* final_state, cudaStream_t stream) {
-    if (p.dtype == SSD_BF16)
-        return launch_fwd_pass_state_tc(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
+                                  void* hiddens, float* final_state, void* scratch,
+                                  bool ctrl_zeroed, cudaStream_t stream) {
+    if (p.dtype == SSD_BF16) {
+        if (!ctrl_zeroed) {
+            const cudaError_t e = cudaMemsetAsync((char*)scratch + fwd_pass_state_ctrl_offset(p), 0,
+                                                  fwd_pass_state_ctrl_bytes(p), stream);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_fwd_pass_state_tc(p, x, B, Gcs, dtT, init, hiddens, final_state, scratch,
+                                        stream);
+    }
     return launch_fps<float>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
 }
 

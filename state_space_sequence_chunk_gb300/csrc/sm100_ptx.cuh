@@ -81,6 +81,58 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
 }
 
 // ---------------------------------------------------------------------------
+// Flags in global memory, for hand-offs between CTAs of one launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait until *flag >= target (an acquire read), with the same bound and error
+// protocol as mbar_wait.  The flag is written by another CTA of the same
+// launch that already holds an earlier work ticket, so the wait ends.
+__device__ __forceinline__ bool flag_wait_geq(const unsigned int* flag, unsigned int target,
+                                              unsigned int* err, unsigned int code) {
+    if (ld_acquire_gpu(flag) >= target) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(flag) >= target) return true;
+        const long long dt = clock64() - t0;
+        if (dt > kWaitSlowCycles) {
+            if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
+            if (dt > kWaitLimitCycles) {
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait until a shared-memory counter written by other warps of the CTA reaches
+// `target` (same bound and error protocol as mbar_wait).
+__device__ __forceinline__ bool smem_wait_geq(volatile int* ctr, int target, unsigned int* err,
+                                              unsigned int code) {
+    if (*ctr >= target) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(20);
+        if (*ctr >= target) return true;
+        const long long dt = clock64() - t0;
+        if (dt > kWaitSlowCycles) {
+            if (*reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
+            if (dt > kWaitLimitCycles) {
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // TMA (tensor maps are __grid_constant__ kernel parameters)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
@@ -127,6 +179,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // async-proxy (TMA / tensor-core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Register reallocation between warpgroups (every thread of the warpgroup
+// executes it; the shares must add up to the CTA's launch allocation)
+// ---------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------------------

@@ -120,7 +120,14 @@ size_t ssd_fwd_workspace_bytes(const ssd_dims* d) {
     Problem p;
     if (make_problem(d, &p) != SSD_OK) return 0;
     if (p.b == 0 || p.L == 0) return 0;
-    return 2 * round_up(gcs_bytes(p), kAlign) + round_up(hid_bytes(p), kAlign);
+    return 2 * round_up(gcs_bytes(p), kAlign) + round_up(hid_bytes(p), kAlign) +
+           fwd_pass_state_scratch_bytes(p);
+}
+
+size_t ssd_fwd_pass_state_scratch_bytes(const ssd_dims* d) {
+    Problem p;
+    if (make_problem(d, &p) != SSD_OK) return 0;
+    return fwd_pass_state_scratch_bytes(p);
 }
 
 ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A, float* Gcs,
@@ -137,12 +144,13 @@ ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A, 
         if (overlap(r, rng(Gcs, gb)) || overlap(r, rng(dtT, gb))) return SSD_ERR_ALIAS;
     if (overlap(rng(Gcs, gb), rng(dtT, gb))) return SSD_ERR_ALIAS;
     if ((s = check_arch()) != SSD_OK) return s;
-    return from_cuda(launch_chunk_cumsum(p, dt, A, Gcs, dtT, (cudaStream_t)stream));
+    return from_cuda(launch_chunk_cumsum(p, dt, A, Gcs, dtT, nullptr, 0, (cudaStream_t)stream));
 }
 
 ssd_status ssd_fwd_pass_state(const ssd_dims* d, const void* x, const void* B, const float* Gcs,
                               const float* dtT, const float* init_state, void* hiddens,
-                              float* final_state, void* stream) {
+                              float* final_state, void* scratch, size_t scratch_bytes,
+                              void* stream) {
     Problem p;
     ssd_status s = make_problem(d, &p);
     if (s != SSD_OK) return s;
@@ -161,8 +169,12 @@ ssd_status ssd_fwd_pass_state(const ssd_dims* d, const void* x, const void* B, c
         return from_cuda(e);
     }
     if (!x || !B || !Gcs || !dtT || !hiddens) return SSD_ERR_NULL;
+    const size_t need = fwd_pass_state_scratch_bytes(p);
+    if (need > 0 && !scratch) return SSD_ERR_NULL;
+    if (scratch_bytes < need) return SSD_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(B) || !aligned16(Gcs) || !aligned16(dtT) ||
-        !aligned16(init_state) || !aligned16(hiddens) || !aligned16(final_state))
+        !aligned16(init_state) || !aligned16(hiddens) || !aligned16(final_state) ||
+        !aligned16(scratch))
         return SSD_ERR_ALIGN;
     const size_t es = (size_t)p.esize, gb = gcs_bytes(p);
     const Range in[] = {rng(x, (size_t)(p.b * p.L * p.H * p.P) * es),
@@ -176,9 +188,13 @@ ssd_status ssd_fwd_pass_state(const ssd_dims* d, const void* x, const void* B, c
     if (init_state && final_state && init_state != final_state && overlap(in[4], fin))
         return SSD_ERR_ALIAS;
     if (overlap(hid, fin)) return SSD_ERR_ALIAS;
+    const Range scr = rng(need > 0 ? scratch : nullptr, need);
+    for (const Range& r : in)
+        if (overlap(r, scr)) return SSD_ERR_ALIAS;
+    if (overlap(scr, hid) || overlap(scr, fin)) return SSD_ERR_ALIAS;
     if ((s = check_arch()) != SSD_OK) return s;
     return from_cuda(launch_fwd_pass_state(p, x, B, Gcs, dtT, init_state, hiddens, final_state,
-                                           (cudaStream_t)stream));
+                                           scratch, false, (cudaStream_t)stream));
 }
 
 ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, const void* C,
@@ -212,7 +228,7 @@ ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const floa
     if (p.b == 0) return SSD_OK;
     if (p.L == 0)  // nothing to compute; the state passes through
         return ssd_fwd_pass_state(d, nullptr, nullptr, nullptr, nullptr, init_state, nullptr,
-                                  final_state, stream);
+                                  final_state, nullptr, 0, stream);
     if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_NULL;
     if (!workspace) return SSD_ERR_NULL;
     if (workspace_bytes < ssd_fwd_workspace_bytes(d)) return SSD_ERR_WORKSPACE;
@@ -241,9 +257,16 @@ ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const floa
     float* Gcs = (float*)w;
     float* dtT = (float*)(w + round_up(gcs_bytes(p), kAlign));
     void* hid = (void*)(w + 2 * round_up(gcs_bytes(p), kAlign));
+    void* scratch = (void*)(w + 2 * round_up(gcs_bytes(p), kAlign) + round_up(hid_bytes(p), kAlign));
+    const bool has_scratch = fwd_pass_state_scratch_bytes(p) > 0;
+    unsigned int* ctrl =
+        has_scratch ? (unsigned int*)((char*)scratch + fwd_pass_state_ctrl_offset(p)) : nullptr;
+    const int ctrl_words = has_scratch ? (int)(fwd_pass_state_ctrl_bytes(p) / 4) : 0;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = launch_chunk_cumsum(p, dt, A, Gcs, dtT, st);
-    if (e == cudaSuccess) e = launch_fwd_pass_state(p, x, B, Gcs, dtT, init_state, hid, final_state, st);
+    // chunk_cumsum clears fwd_pass_state's control block on the way
+    cudaError_t e = launch_chunk_cumsum(p, dt, A, Gcs, dtT, ctrl, ctrl_words, st);
+    if (e == cudaSuccess)
+        e = launch_fwd_pass_state(p, x, B, Gcs, dtT, init_state, hid, final_state, scratch, true, st);
     if (e == cudaSuccess) e = launch_compute_out(p, x, B, C, Gcs, dtT, hid, D, y, st);
     return from_cuda(e);
 }

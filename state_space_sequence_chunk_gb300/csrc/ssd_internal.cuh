@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "ssd.h"
@@ -23,13 +24,30 @@ struct Problem {
     int esize;    // bytes per element of x, B, C, y, hiddens
 };
 
+inline size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Scratch of the tensor-core fwd_pass_state (bf16 only; 0 bytes otherwise): a
+// two-slot fp32 state ring per chain, then a control block of 32-bit words --
+// word 0 the work-ticket counter, words kCtrlFlagOffset + chain the chains'
+// hand-off flags.  The control block must be zero when the kernel starts.
+constexpr int kCtrlFlagOffset = 32;
+size_t fwd_pass_state_scratch_bytes(const Problem& p);
+size_t fwd_pass_state_ctrl_offset(const Problem& p);
+size_t fwd_pass_state_ctrl_bytes(const Problem& p);
+
 // Launchers (defined next to their kernels).  All enqueue on `stream` and
-// return cudaGetLastError().
+// return cudaGetLastError().  chunk_cumsum also zeroes `zero_words` 32-bit
+// words at `zero_ptr` (may be NULL), so that a following fwd_pass_state finds
+// its control block cleared without a separate launch.
 cudaError_t launch_chunk_cumsum(const Problem& p, const float* dt, const float* A, float* Gcs,
-                                float* dtT, cudaStream_t stream);
+                                float* dtT, unsigned int* zero_ptr, int zero_words,
+                                cudaStream_t stream);
+// `scratch` holds fwd_pass_state_scratch_bytes(p) bytes; unless `ctrl_zeroed`,
+// its control block is cleared with a memset first.
 cudaError_t launch_fwd_pass_state(const Problem& p, const void* x, const void* B,
                                   const float* Gcs, const float* dtT, const float* init,
-                                  void* hiddens, float* final_state, cudaStream_t stream);
+                                  void* hiddens, float* final_state, void* scratch,
+                                  bool ctrl_zeroed, cudaStream_t stream);
 cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, const void* C,
                                const float* Gcs, const float* dtT, const void* hiddens,
                                const float* D, void* y, cudaStream_t stream);
@@ -37,7 +55,8 @@ cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, c
 // Tensor-core (tcgen05) variants for bf16 inputs.
 cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void* B,
                                      const float* Gcs, const float* dtT, const float* init,
-                                     void* hiddens, float* final_state, cudaStream_t stream);
+                                     void* hiddens, float* final_state, void* scratch,
+                                     cudaStream_t stream);
 bool compute_out_tc_supports(const Problem& p);
 cudaError_t launch_compute_out_tc(const Problem& p, const void* x, const void* B, const void* C,
                                   const float* Gcs, const float* dtT, const void* hiddens,

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.ssd_abi_version() == 1
+    assert lib.ssd_abi_version() == 2
     for code in range(0, 9):
         s = lib.ssd_status_string(code)
         assert s and s != b"unknown status"
@@ -58,8 +58,20 @@ def test_workspace_bytes(lib):
     gcs = 2 * 4 * nc * 128 * 4
     hid = 2 * 4 * nc * 64 * 128 * 2
     ru = lambda v: (v + 255) // 256 * 256
-    assert ssd.ssd_fwd_workspace_bytes(d) == 2 * ru(gcs) + ru(hid)
+    # fwd_pass_state scratch (bf16): a two-slot fp32 state ring of 128 rows x 64
+    # (P padded) per (batch, head, 128-row block of N), then 32 + chains words
+    chains = 2 * 4 * 1
+    scratch = ru(chains * 2 * 128 * 64 * 4) + ru((32 + chains) * 4)
+    assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(d)) == scratch
+    assert ssd.ssd_fwd_workspace_bytes(d) == 2 * ru(gcs) + ru(hid) + scratch
     assert ssd.ssd_intermediate_bytes(d) == (gcs, hid)
+    d32 = dims(dtype=ssd.SSD_F32)
+    assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(d32)) == 0
+    assert ssd.ssd_fwd_workspace_bytes(d32) == 2 * ru(gcs) + ru(2 * hid)
+    d2 = dims(dstate=256, headdim=96)   # two row blocks per head, P padded to 128
+    chains2 = 2 * 4 * 2
+    assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(d2)) == (
+        ru(chains2 * 2 * 128 * 128 * 4) + ru((32 + chains2) * 4))
     assert ssd.ssd_fwd_workspace_bytes(dims(seqlen=0)) == 0
     assert ssd.ssd_fwd_workspace_bytes(dims(chunk_size=100)) == 0
 
@@ -110,11 +122,18 @@ def test_per_step_validation(lib):
     a = _fwd_args()
     assert lib.ssd_chunk_cumsum(ctypes.byref(d), a[0], None, a[2], a[3], None) == 1
     assert lib.ssd_chunk_cumsum(ctypes.byref(d), a[0], a[1], a[2], a[2], None) == 8
-    assert lib.ssd_fwd_pass_state(ctypes.byref(d), a[0], a[1], a[2], a[3], a[4], None, a[6],
-                                  None) == 1
+    big = ctypes.c_size_t(1 << 40)
+    fps = lambda *args: lib.ssd_fwd_pass_state(ctypes.byref(d), *args)
+    assert fps(a[0], a[1], a[2], a[3], a[4], None, a[6], a[7], big, None) == 1
     hid_in_x = ctypes.c_void_p(a[0].value + 1024)
-    assert lib.ssd_fwd_pass_state(ctypes.byref(d), a[0], a[1], a[2], a[3], a[4], hid_in_x, a[6],
-                                  None) == 8
+    assert fps(a[0], a[1], a[2], a[3], a[4], hid_in_x, a[6], a[7], big, None) == 8
+    # the bf16 path needs its scratch: NULL, too small, misaligned, overlapping
+    assert fps(a[0], a[1], a[2], a[3], a[4], a[5], a[6], None, big, None) == 1
+    assert fps(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], ctypes.c_size_t(64), None) == 5
+    assert fps(a[0], a[1], a[2], a[3], a[4], a[5], a[6], ctypes.c_void_p(a[7].value + 4), big,
+               None) == 4
+    assert fps(a[0], a[1], a[2], a[3], a[4], a[5], a[6], ctypes.c_void_p(a[1].value + 512), big,
+               None) == 8
     assert lib.ssd_compute_out(ctypes.byref(d), a[0], a[1], a[2], a[3], a[4], a[5], None,
                                ctypes.c_void_p(a[0].value), None) == 8
 

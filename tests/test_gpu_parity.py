@@ -5,6 +5,8 @@ bound max|out - ref| / max|ref| <= 1e-3 (fp32 inputs) or 1e-2 (bf16 inputs).
 Small problems are compared in full; the full-size workloads on sampled
 (batch, head) slices, each of which is an exact, independent recurrence.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -216,6 +218,41 @@ def test_deterministic_and_stream_ordered():
     s.synchronize()
     assert np.array_equal(y1, y2.float().cpu().numpy())
     assert np.array_equal(f1, f2.cpu().numpy())
+
+
+def test_workspace_contents_do_not_matter():
+    """The workspace (and its fwd_pass_state control block) may hold anything
+    on entry: fill it with 0xFF bytes, run twice through the same buffer, and
+    compare with a fresh run and with the oracle.  Also the step entry point
+    with a garbage scratch buffer."""
+    w = small(seqlen=700, nheads=6, dtype="bf16", chunk=128, headdim=64, dstate=128,
+              init_std=0.1, batch=2)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, "bf16")
+    y_ref, f_ref = oracle_fwd(inp)
+    dims = ssd.dims_for(dev["x"], dev["B"], 128)
+    ws = torch.full((ssd.ssd_fwd_workspace_bytes(dims),), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        y, f = ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                           dev["init_state"], chunk_size=128, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((y.float().cpu().numpy(), f.cpu().numpy()))
+    assert ssd.ssd_take_device_errors() == 0
+    for y, f in outs:
+        assert rel_err(y, y_ref) < TOL["bf16"] and rel_err(f, f_ref) < TOL["bf16"]
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    Gcs, dtT = ssd.ssd_chunk_cumsum(dev["dt"], dev["A"], chunk_size=128)
+    scr = torch.full((int(ssd.load_library().ssd_fwd_pass_state_scratch_bytes(
+        ctypes.byref(dims))),), 0xA5, dtype=torch.uint8, device="cuda")
+    hid1, fin1 = ssd.ssd_fwd_pass_state(dev["x"], dev["B"], Gcs, dtT, dev["init_state"],
+                                        chunk_size=128, scratch=scr)
+    hid2, fin2 = ssd.ssd_fwd_pass_state(dev["x"], dev["B"], Gcs, dtT, dev["init_state"],
+                                        chunk_size=128, scratch=scr)
+    torch.cuda.synchronize()
+    assert ssd.ssd_take_device_errors() == 0
+    assert torch.equal(hid1, hid2) and torch.equal(fin1, fin2)
+    assert np.array_equal(fin1.cpu().numpy(), outs[0][1])
 
 
 def test_errors_are_raised():
