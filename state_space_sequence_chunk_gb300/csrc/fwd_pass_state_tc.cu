@@ -45,6 +45,8 @@
 // padded rows/columns are computed and never stored.
 #include <cuda.h>
 
+#include <string.h>
+
 #include <algorithm>
 
 #include "sm100_ptx.cuh"
@@ -62,8 +64,14 @@ constexpr int kCols = 64;           // state columns (of P) per chain
 constexpr int kScalerWarps = 6;
 constexpr int kFoldWarps = 4;
 constexpr int kThreads = 32 * (2 + kScalerWarps + kFoldWarps);
-constexpr int kAccSlots = 3;        // TMEM accumulators (chunk products in flight)
-constexpr int kStages = 4;
+// TMEM (256 columns): chunk-product accumulators and running-state slots of
+// 64 columns each -- three accumulators and one state, or, with an init
+// state, two and two (the next chain's initial state waits in the spare slot).
+constexpr int kMaxAccSlots = 3;
+template <bool kHasInit> __host__ __device__ constexpr int acc_slots() { return kHasInit ? 2 : 3; }
+// TMA ring depth: four stages, or three when a 32 KB init-state tile shares
+// the shared memory.
+template <bool kHasInit> __host__ __device__ constexpr int stages() { return kHasInit ? 3 : 4; }
 constexpr int kVecSlots = 2;        // per-chunk g / dt buffers
 constexpr int kMinBlocks = 2;       // CTAs per SM
 // Register cap: two 384-thread CTAs per SM stay below the register file's
@@ -74,13 +82,17 @@ constexpr int kBBytes = kSub * 128 * 2;            // B sub-tile (128 state rows
 constexpr int kStageBytes = kXBytes + kBBytes;     // multiple of 1024
 constexpr int kMaxQ = 256;
 constexpr int kVecSlotBytes = 2 * kMaxQ * 4;       // g[Q], dt[Q] of one chunk
-constexpr int kStateCol = kAccSlots * kCols;       // TMEM column of the running state
-constexpr int kTmemCols = 256;                     // 3 accumulators + the state, power of two
+constexpr int kTmemCols = 256;
 constexpr int kBarBytes = 512;
-constexpr int kSmem = kStages * kStageBytes + kVecSlots * kVecSlotBytes + kBarBytes + 1024;
+// state tile in shared memory (init in, final out): fp32 [64 p][128 n]
+constexpr int kInitBytes = kCols * 128 * 4;
+template <bool kHasInit>
+__host__ __device__ constexpr int smem_bytes() {
+    return stages<kHasInit>() * kStageBytes + (kHasInit ? kInitBytes : 0) +
+           kVecSlots * kVecSlotBytes + kBarBytes + 1024;
+}
 constexpr uint32_t kIdesc = make_idesc(1, 128, kCols, 1, 1);
 constexpr int kSlotFloats = 128 * kCols;           // one state slot of the hand-off buffer
-static_assert(kStateCol + kCols <= kTmemCols, "TMEM layout");
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 
 struct FpsParams {
@@ -144,27 +156,33 @@ __device__ __forceinline__ Piece piece_of(const Range& r, int i, const FpsParams
     return u;
 }
 
+template <bool kHasInit>
 __global__ void __maxnreg__(kMaxRegs)
 fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                  const float* __restrict__ Gcs, const float* __restrict__ dtT, const float* init,
-                  __nv_bfloat16* __restrict__ hiddens, float* final_state, float* ring,
-                  unsigned int* ctrl, const FpsParams q) {
-    constexpr int S = kStages;
+                  const float* init, const float* __restrict__ Gcs,
+                  const float* __restrict__ dtT, __nv_bfloat16* __restrict__ hiddens,
+                  float* final_state, float* ring, unsigned int* ctrl, const FpsParams q) {
+    constexpr int S = stages<kHasInit>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* vecs = smem + S * kStageBytes;   // kVecSlots x (g[Q], dt[Q])
+    float* init_tile = reinterpret_cast<float*>(smem + S * kStageBytes);   // [64 p][128 n]
+    uint8_t* vecs = smem + S * kStageBytes + (kHasInit ? kInitBytes : 0);   // kVecSlots x (g[Q], dt[Q])
     uint64_t* bars = reinterpret_cast<uint64_t*>(vecs + kVecSlots * kVecSlotBytes);
     // barrier indices
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto scaled = [&](int s) { return smem_u32(bars + S + s); };
     auto empty = [&](int s) { return smem_u32(bars + 2 * S + s); };
     auto acc_full = [&](int k) { return smem_u32(bars + 3 * S + k); };
-    auto acc_empty = [&](int k) { return smem_u32(bars + 3 * S + kAccSlots + k); };
-    auto vec_full = [&](int v) { return smem_u32(bars + 3 * S + 2 * kAccSlots + v); };
-    auto vec_empty = [&](int v) { return smem_u32(bars + 3 * S + 2 * kAccSlots + kVecSlots + v); };
-    const uint32_t fold_done = smem_u32(bars + 3 * S + 2 * kAccSlots + 2 * kVecSlots);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 2 * kAccSlots + 2 * kVecSlots + 1);
+    constexpr int A = acc_slots<kHasInit>();
+    constexpr int kB = 3 * S + 2 * kMaxAccSlots;   // first barrier after the ring / accumulator ones
+    auto acc_empty = [&](int k) { return smem_u32(bars + 3 * S + kMaxAccSlots + k); };
+    auto vec_full = [&](int v) { return smem_u32(bars + kB + v); };
+    auto vec_empty = [&](int v) { return smem_u32(bars + kB + kVecSlots + v); };
+    const uint32_t fold_done = smem_u32(bars + kB + 2 * kVecSlots);
+    const uint32_t init_full = smem_u32(bars + kB + 2 * kVecSlots + 1);
+    const uint32_t tile_free = smem_u32(bars + kB + 2 * kVecSlots + 2);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kB + 2 * kVecSlots + 3);
     int* range_id = reinterpret_cast<int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,7 +195,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             mbar_init(scaled(s), 32 * kScalerWarps);
             mbar_init(empty(s), 1);
         }
-        for (int k = 0; k < kAccSlots; ++k) {
+        for (int k = 0; k < A; ++k) {
             mbar_init(acc_full(k), 1);
             mbar_init(acc_empty(k), 32 * kFoldWarps);
         }
@@ -186,6 +204,8 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             mbar_init(vec_empty(v), 32 * kScalerWarps);
         }
         mbar_init(fold_done, kFoldWarps);
+        mbar_init(init_full, 32 * kFoldWarps);
+        mbar_init(tile_free, 32 * kFoldWarps);
         fence_mbar_init();
         // ranges in dispatch order: the range before this one belongs to a CTA
         // that is already running
@@ -245,14 +265,14 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         if (lane == 0) {
             int i = 0;
             for (int qc = 0; qc < nchunks; ++qc) {
-                const int slot = qc % kAccSlots;
+                const int slot = qc % A;
                 bool ok = true;
                 for (int sub = 0; sub < nsub; ++sub, ++i) {
                     const int s = i % S, k = i / S;
                     if (!mbar_wait(scaled(s), k & 1, &g_fps_error, 1u)) { ok = false; break; }
                     // the fold warps have read this slot's previous product
                     if (sub == 0 &&
-                        !mbar_wait(acc_empty(slot), ((qc / kAccSlots) & 1) ^ 1, &g_fps_error, 1u)) {
+                        !mbar_wait(acc_empty(slot), ((qc / A) & 1) ^ 1, &g_fps_error, 1u)) {
                         ok = false;
                         break;
                     }
@@ -316,36 +336,108 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     } else {
         // ---------------- fold warps: hiddens[c] = S, S <- 2^{g_last} S + D_c ----------------
         // Thread = TMEM lane = state row n of the chain's 128-row block.  The
-        // running state S^T lives in TMEM columns [kStateCol, kStateCol + 64).  A
-        // hand-off slot holds S^T as [16][128 rows][4] fp32, so that a warp's
-        // float4 accesses cover 512 contiguous bytes.  Every exit from this loop
-        // is warp-uniform: the warp-collective TMEM accesses and __syncwarp calls
-        // never wait for a lane that has left.
+        // running state S^T of a piece lives in a TMEM state slot (piece parity
+        // picks the slot when there are two).  A hand-off slot in global memory
+        // holds S^T as [16][128 rows][4] fp32, so that a warp's float4 accesses
+        // cover 512 contiguous bytes.  Every exit from this loop is warp-uniform:
+        // the warp-collective TMEM accesses and __syncwarp calls never wait for a
+        // lane that has left.
+        constexpr int kStates = kHasInit ? 2 : 1;
         const int quarter = warp & 3;
         const int rl = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t st_addr = lane_base + kStateCol;
-        int qc = 0;  // chunk counter (accumulator ring position)
+        const uint32_t st_base = lane_base + A * kCols;
+        // The state tile in shared memory: fp32 [64 p][128 n]; thread n only
+        // reads / writes column n in the fold (conflict-free), and the copies to
+        // and from global memory move whole 512-byte rows.  These copies use the
+        // LSU path (cp.async in, vector stores out), not the TMA, so that they
+        // never queue behind the x / B stream.
+        float* tcol = init_tile + rl;
+        auto tile_at = [&](int pp) -> float& { return tcol[pp * 128]; };
+        int qc = 0;       // chunk counter (accumulator ring position)
+        int ntile = 0;    // init tiles consumed (init_full phases)
+        int nfree = 0;    // tile_free phases
+        int ld_next = 0;  // next piece to consider for an init-tile load
+        // Init tiles (rows p of [b, H, P, N], 128 columns of N, zero-filled past P
+        // and N) are fetched by all fold threads, one piece ahead of their use.
+        auto issue_next_init = [&]() {
+            while (ld_next < rg.pieces() && piece_of(rg, ld_next, q).c0 != 0) ++ld_next;
+            if (ld_next < rg.pieces()) {
+                const Piece un = piece_of(rg, ld_next, q);
+                const int rows = min(q.P - un.pb * kCols, kCols), ncols = min(q.N - un.mb * 128, 128);
+                const float* g0 = init + ((int64_t)un.bh * q.P + un.pb * kCols) * q.N + un.mb * 128;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int idx = i * 128 + rl, pp = idx >> 5, c4 = idx & 31;
+                    const bool v = pp < rows && 4 * c4 < ncols;
+                    cp_async_16(smem_u32(init_tile + pp * 128 + 4 * c4),
+                                v ? g0 + (int64_t)pp * q.N + 4 * c4 : g0, v ? 16u : 0u);
+                }
+                cp_async_mbar_arrive_noinc(init_full);
+                ++ld_next;
+            }
+        };
+        // the next init tile -> a TMEM state slot
+        auto take_tile = [&](uint32_t slot_addr) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(init_full, ntile & 1, &g_fps_error, 1u))) return false;
+            ++ntile;
+#pragma unroll
+            for (int jj = 0; jj < kCols / 16; ++jj) {
+                uint32_t v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(tile_at(16 * jj + k));
+                __syncwarp();
+                tmem_st_x16(slot_addr + 16 * jj, v);
+            }
+            tmem_wait_st();
+            return true;
+        };
+        // barrier of the fold threads over the tile buffer: every thread waits
+        // until all of them have finished their accesses (warp-uniform result)
+        auto tile_sync = [&]() -> bool {
+            __syncwarp();
+            mbar_arrive(tile_free);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(tile_free, nfree & 1, &g_fps_error, 1u));
+            ++nfree;
+            return ok;
+        };
+        if (kHasInit) issue_next_init();
+        const float* gfirst = Gcs + q.Q - 1;   // g_last of chunk c of head bh: gfirst[bh*Lp + c*Q]
+        float gl_first = 0.f;                  // g_last of the next piece's first chunk
+        {
+            const Piece u0 = piece_of(rg, 0, q);
+            gl_first = gfirst[(int64_t)u0.bh * q.Lp + (int64_t)u0.c0 * q.Q];
+        }
         for (int pi = 0; pi < rg.pieces(); ++pi) {
             const Piece u = piece_of(rg, pi, q);
             const int n = u.mb * 128 + rl;
             const bool nok = n < q.N;
             const int p0 = u.pb * kCols;
             const int64_t sbase = (int64_t)u.bh * q.P * q.N;
-            const float* grow = Gcs + (int64_t)u.bh * q.Lp + q.Q - 1;   // g_last of chunk c: grow[c*Q]
-            float gl_next = grow[(int64_t)u.c0 * q.Q];
-            // the piece's initial state -> TMEM
+            const uint32_t sa = st_base + (pi % kStates) * kCols;
+            const float* grow = gfirst + (int64_t)u.bh * q.Lp;
+            float gl_next = gl_first;
+            if (pi + 1 < rg.pieces()) {  // prefetch for the next piece
+                const Piece un = piece_of(rg, pi + 1, q);
+                gl_first = gfirst[(int64_t)un.bh * q.Lp + (int64_t)un.c0 * q.Q];
+            }
+            // the piece's initial state -> TMEM slot sa
             if (u.c0 == 0) {
-                const float* ip = init + sbase + (int64_t)p0 * q.N + n;
-                const int pl = (init != nullptr && nok) ? q.P - p0 : 0;   // valid columns
+                if (kHasInit) {
+                    if (pi == 0) {  // later pieces found theirs in sa already
+                        if (!take_tile(sa)) break;
+                        if (!tile_sync()) break;
+                        issue_next_init();
+                    }
+                } else {
 #pragma unroll
-                for (int jj = 0; jj < kCols / 16; ++jj) {
-                    uint32_t v[16];
+                    for (int jj = 0; jj < kCols / 16; ++jj) {
+                        uint32_t v[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        v[k] = __float_as_uint(16 * jj + k < pl ? ip[(int64_t)(16 * jj + k) * q.N] : 0.f);
-                    __syncwarp();
-                    tmem_st_x16(st_addr + 16 * jj, v);
+                        for (int k = 0; k < 16; ++k) v[k] = 0u;
+                        __syncwarp();
+                        tmem_st_x16(sa + 16 * jj, v);
+                    }
                 }
             } else {
                 // the state published by the CTA of the previous range
@@ -364,7 +456,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                         v[4 * q4 + 2] = __float_as_uint(f.z); v[4 * q4 + 3] = __float_as_uint(f.w);
                     }
                     __syncwarp();
-                    tmem_st_x16(st_addr + 16 * jj, v);
+                    tmem_st_x16(sa + 16 * jj, v);
                 }
             }
             tmem_wait_st();
@@ -372,9 +464,8 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             for (int c = u.c0; c < u.c1; ++c, ++qc) {
                 const float e = exp2f(gl_next);
                 if (c + 1 < u.c1) gl_next = grow[(int64_t)(c + 1) * q.Q];
-                const int slot = qc % kAccSlots;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(acc_full(slot), (qc / kAccSlots) & 1, &g_fps_error, 1u))) {
+                const int slot = qc % A;
+                if (!__all_sync(0xffffffffu, mbar_wait(acc_full(slot), (qc / A) & 1, &g_fps_error, 1u))) {
                     ok = false;
                     break;
                 }
@@ -385,13 +476,13 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 for (int jj = 0; jj < kCols / 16; ++jj) {
                     __syncwarp();
                     uint32_t sv[16], d[16];
-                    tmem_ld_x16(st_addr + 16 * jj, sv);
+                    tmem_ld_x16(sa + 16 * jj, sv);
                     tmem_ld_x16(acc + 16 * jj, d);
                     tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         d[k] = __float_as_uint(fmaf(e, __uint_as_float(sv[k]), __uint_as_float(d[k])));
-                    tmem_st_x16(st_addr + 16 * jj, d);
+                    tmem_st_x16(sa + 16 * jj, d);
                     // chunk-start state S -> hiddens[c] (row n holds S[:, n]): 16
                     // contiguous bf16 per slice (P is a multiple of 16)
                     if (nok && p0 + 16 * jj < q.P) {
@@ -415,45 +506,90 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 mbar_arrive(acc_empty(slot));
             }
             if (!__all_sync(0xffffffffu, ok)) break;
+            // the next piece's initial state into the spare slot, so that it can
+            // start at once, before the tile buffer is reused below
+            const bool next_tile = kHasInit && pi + 1 < rg.pieces() && piece_of(rg, pi + 1, q).c0 == 0;
+            if (next_tile && !take_tile(st_base + ((pi + 1) % kStates) * kCols)) break;
             // the piece's final state: to final_state, or published for the next range
             const bool last = u.c1 == q.nc;
-            float* dst = ring + ((int64_t)u.ch * 2 + (rk & 1)) * kSlotFloats;
-            const int pl = nok ? q.P - p0 : 0;
+            if (last && final_state != nullptr && kHasInit) {
+                // through the tile buffer: columns in, rows out as 16-byte stores
+                if (next_tile && !tile_sync()) break;   // everyone has read the tile
 #pragma unroll
-            for (int jj = 0; jj < kCols / 16; ++jj) {
-                __syncwarp();
-                uint32_t sv[16];
-                tmem_ld_x16(st_addr + 16 * jj, sv);
-                tmem_wait_ld();
-                if (!last) {
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    __syncwarp();
+                    uint32_t sv[16];
+                    tmem_ld_x16(sa + 16 * jj, sv);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        __stcg(reinterpret_cast<float4*>(dst + ((4 * jj + q4) * 128 + rl) * 4),
-                               make_float4(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1]),
-                                           __uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])));
-                } else if (final_state != nullptr) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (16 * jj + k < pl)
-                            final_state[sbase + (int64_t)(p0 + 16 * jj + k) * q.N + n] = __uint_as_float(sv[k]);
+                    for (int k = 0; k < 16; ++k) tile_at(16 * jj + k) = __uint_as_float(sv[k]);
                 }
-            }
-            if (!last) {
-                // publish: every fold warp's stores, then one release of the chain's
-                // flag (a range publishes at most once)
-                __syncwarp();
-                if (lane == 0) mbar_arrive(fold_done);
-                bool okp = true;
-                if (rl == 0) {
-                    okp = mbar_wait(fold_done, 0, &g_fps_error, 1u);
-                    if (okp) {
-                        __threadfence();
-                        st_release_gpu(flags + u.ch, (unsigned)u.c1);
+                if (!tile_sync()) break;
+                {
+                    const int rows = min(q.P - p0, kCols), ncols = min(q.N - u.mb * 128, 128);
+                    float* g0 = final_state + ((int64_t)u.bh * q.P + p0) * q.N + u.mb * 128;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int idx = i * 128 + rl, pp = idx >> 5, c4 = idx & 31;
+                        if (pp < rows && 4 * c4 < ncols)
+                            *reinterpret_cast<float4*>(g0 + (int64_t)pp * q.N + 4 * c4) =
+                                *reinterpret_cast<const float4*>(init_tile + pp * 128 + 4 * c4);
                     }
                 }
-                if (!__shfl_sync(0xffffffffu, okp, 0)) break;
+                if (!tile_sync()) break;   // the tile has been read before it is refilled
+                issue_next_init();
+            } else {
+                if (next_tile) {
+                    if (!tile_sync()) break;
+                    issue_next_init();
+                }
+                if (last) {
+                    if (final_state != nullptr) {
+                        const int pl = nok ? q.P - p0 : 0;
+#pragma unroll
+                        for (int jj = 0; jj < kCols / 16; ++jj) {
+                            __syncwarp();
+                            uint32_t sv[16];
+                            tmem_ld_x16(sa + 16 * jj, sv);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                if (16 * jj + k < pl)
+                                    final_state[sbase + (int64_t)(p0 + 16 * jj + k) * q.N + n] =
+                                        __uint_as_float(sv[k]);
+                        }
+                    }
+                } else {
+                    float* dst = ring + ((int64_t)u.ch * 2 + (rk & 1)) * kSlotFloats;
+#pragma unroll
+                    for (int jj = 0; jj < kCols / 16; ++jj) {
+                        __syncwarp();
+                        uint32_t sv[16];
+                        tmem_ld_x16(sa + 16 * jj, sv);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            __stcg(reinterpret_cast<float4*>(dst + ((4 * jj + q4) * 128 + rl) * 4),
+                                   make_float4(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1]),
+                                               __uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])));
+                    }
+                    // publish: every fold warp's stores, then one release of the
+                    // chain's flag (a range publishes at most once)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(fold_done);
+                    bool okp = true;
+                    if (rl == 0) {
+                        okp = mbar_wait(fold_done, 0, &g_fps_error, 1u);
+                        if (okp) {
+                            __threadfence();
+                            st_release_gpu(flags + u.ch, (unsigned)u.c1);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, okp, 0)) break;
+                }
             }
         }
+        if (kHasInit) cp_async_wait_all();  // no copy into shared memory outlives the CTA
     }
     tc_fence_before();
     __syncthreads();
@@ -492,7 +628,7 @@ cudaError_t resident_ctas(int* out) {
         (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) !=
             cudaSuccess)
         return e;
-    int per_sm = std::min(smem_sm / (kSmem + 1024), 512 / kTmemCols);
+    int per_sm = std::min(smem_sm / (smem_bytes<true>() + 1024), 512 / kTmemCols);
     per_sm = std::min(per_sm, regs_sm / (kThreads * kMaxRegs));
     per_sm = std::max(1, std::min(per_sm, kMinBlocks));
     *out = sms * per_sm;
@@ -528,10 +664,11 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
         !encode_tmap_4d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, bd, bs, box,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(fwd_pass_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmem);
+    auto kern = init != nullptr ? fwd_pass_state_tc<true> : fwd_pass_state_tc<false>;
+    const int smem = init != nullptr ? smem_bytes<true>() : smem_bytes<false>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
-        e = cudaFuncSetAttribute(fwd_pass_state_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int resident = 0;
@@ -545,8 +682,8 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     if ((int64_t)q.nchains * p.nc >= (int64_t)1 << 31) return cudaErrorInvalidValue;
     q.W = q.nchains * q.nc;
     q.G = std::min(q.W, resident);
-    fwd_pass_state_tc<<<(unsigned)q.G, kThreads, kSmem, stream>>>(
-        tx, tb, Gcs, dtT, init, (__nv_bfloat16*)hiddens, final_state, ring, ctrl, q);
+    kern<<<(unsigned)q.G, kThreads, smem, stream>>>(tx, tb, init, Gcs, dtT, (__nv_bfloat16*)hiddens,
+                                                    final_state, ring, ctrl, q);
     return cudaGetLastError();
 }
 

@@ -81,6 +81,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
 }
 
 // ---------------------------------------------------------------------------
+// cp.async (LSU path global -> shared copies, completion on an mbarrier)
+// ---------------------------------------------------------------------------
+// 16-byte copy; src_bytes < 16 zero-fills the rest (0: all zeros, src unread).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// Arrive on `bar` once all of this thread's earlier cp.async copies have landed
+// (the arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Flags in global memory, for hand-offs between CTAs of one launch
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
@@ -90,6 +107,9 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
 }
 __device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 // Wait until *flag >= target (an acquire read), with the same bound and error
 // protocol as mbar_wait.  The flag is written by another CTA of the same
@@ -149,6 +169,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 __device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1,

@@ -29,19 +29,29 @@ EncodeTiledFn encoder() {
 
 }  // namespace
 
-bool encode_tmap_4d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
-                    const uint64_t dims[4], const uint64_t strides_bytes[3],
-                    const uint32_t box[4], CUtensorMapSwizzle swizzle) {
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encoder();
-    if (!fn) return false;
-    cuuint64_t gdim[4] = {dims[0], dims[1], dims[2], dims[3]};
-    cuuint64_t gstr[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
-    cuuint32_t bdim[4] = {box[0], box[1], box[2], box[3]};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, dtype, 4, const_cast<void*>(base), gdim, gstr, bdim, estr,
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t gdim[5], gstr[4];
+    cuuint32_t bdim[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) gstr[i] = strides_bytes[i];
+    }
+    CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstr, bdim, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_4d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    const uint64_t dims[4], const uint64_t strides_bytes[3],
+                    const uint32_t box[4], CUtensorMapSwizzle swizzle) {
+    return encode_tmap(map, dtype, 4, base, dims, strides_bytes, box, swizzle);
 }
 
 }  // namespace ssd

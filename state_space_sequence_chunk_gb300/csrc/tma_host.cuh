@@ -9,6 +9,13 @@
 
 namespace ssd {
 
+// Encode a tiled map of rank 1..5 (dims[0] contiguous; strides_bytes holds the
+// byte strides of dims 1..rank-1).  Returns false if the encoder is unavailable
+// or rejects the arguments.
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle);
+
 // Encode a 4-D tiled map.  dims[0] is the contiguous dimension; strides_bytes
 // are the byte strides of dims 1..3.  Returns false if the encoder is
 // unavailable or rejects the arguments.
