@@ -542,42 +542,31 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(smem_u32(b_accfree + es));
-                    // y rows go to shared memory in the 128-byte-swizzled layout of the
-                    // tensor map, then one thread stores the 128-row block with TMA
-                    // (rows past seqlen and columns past headdim are clipped by it).
-                    // Block 0 of a 256-token chunk stages in the stage's h tile (free
-                    // once both C h^T products are done); otherwise each row
-                    // overwrites its own x row (free once the last A X product is
-                    // done, which the d_done wait above covers).
-                    uint8_t* stage_rw = stage_ptr + s * Cfg::kStageBytes;
-                    uint8_t* ybuf = (Q > 128 && I == 0) ? stage_rw + Cfg::kXBytes : stage_rw + I * 128 * kRowBytes;
-                    if (i < Q) {
+                    // y = acc + D x, stored straight from registers: each thread
+                    // writes its own row (128 contiguous bytes, 16 at a time).  The
+                    // x row is read from the stage's swizzled tile, after which the
+                    // stage no longer holds anything this head needs.
+                    const int t = ui.c * Q + i;   // token
+                    if (i < Q && t < L) {
                         const uint8_t* xr = st + i * kRowBytes;
-                        uint8_t* yr = ybuf + row * kRowBytes;
+                        __nv_bfloat16* yr = y + (((int64_t)ui.b * L + t) * H + ui.h) * P;
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
-                            const int off = (ch ^ (i & 7)) << 4;   // (row & 7) == (i & 7)
-                            const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
-                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                            uint32_t ow[4];
+                            if (ch * 8 < P) {
+                                const int off = (ch ^ (i & 7)) << 4;
+                                const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
+                                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                                uint32_t ow[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int p0 = ch * 8 + 2 * e;
-                                const uint32_t* vv = p0 < 32 ? v0 : v1;
-                                ow[e] = pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
-                                                  __uint_as_float(vv[(p0 & 31) + 1]) + dh * bf16hi(xw[e]));
+                                for (int e = 0; e < 4; ++e) {
+                                    const int p0 = ch * 8 + 2 * e;
+                                    const uint32_t* vv = p0 < 32 ? v0 : v1;
+                                    ow[e] = pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
+                                                      __uint_as_float(vv[(p0 & 31) + 1]) + dh * bf16hi(xw[e]));
+                                }
+                                *reinterpret_cast<uint4*>(yr + ch * 8) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                             }
-                            uint4 ov;
-                            ov.x = ow[0]; ov.y = ow[1]; ov.z = ow[2]; ov.w = ow[3];
-                            *reinterpret_cast<uint4*>(yr + off) = ov;
                         }
-                    }
-                    fence_proxy_async_smem();
-                    named_bar_sync(2 + es, 128);
-                    if (row == 0) {
-                        tma_store_4d(&tm_y, smem_u32(ybuf), 0, ui.h, ui.c * Q + I * 128, ui.b);
-                        bulk_commit_group();
-                        bulk_wait_group_read0();   // the stage is released only after this read
                     }
                 }
             }
