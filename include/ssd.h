@@ -170,6 +170,19 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
  */
 unsigned int ssd_take_device_errors(void);
 
+/*
+ * ssd_debug_withhold_handoffs -- test hook for failure detection.  With `on`
+ * nonzero, later bf16 fwd_pass_state launches on the current device skip
+ * publishing the state at the end of each CTA's work range, so that the CTA
+ * that continues the chain waits in vain.  That wait is bounded (about 1 s of
+ * SM clock): it gives up, sets bit 0 of the error word and the launch ends
+ * early with undefined hiddens / final_state (and y).  The device context stays
+ * usable; ssd_take_device_errors() reports and clears the bit.  Pass 0 to
+ * restore normal operation.  Not for production use.  Returns SSD_ERR_CUDA if
+ * the flag cannot be written.
+ */
+ssd_status ssd_debug_withhold_handoffs(int on);
+
 /* Size of the fixed device scratch buffer used by ssd_fwd_noalloc: 32 MiB. */
 #define SSD_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
 

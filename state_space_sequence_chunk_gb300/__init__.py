@@ -33,7 +33,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE"
 EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
            "ssd_fwd_pass_state_scratch_bytes", "ssd_compute_out", "ssd_fwd_noalloc",
-           "ssd_take_device_errors"]
+           "ssd_take_device_errors", "ssd_debug_withhold_handoffs"]
 
 
 class SSDError(RuntimeError):
@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_fwd_pass_state.restype = ctypes.c_int
         lib.ssd_compute_out.argtypes = [dp] + [vp] * 9
         lib.ssd_compute_out.restype = ctypes.c_int
+        lib.ssd_debug_withhold_handoffs.argtypes = [ctypes.c_int]
+        lib.ssd_debug_withhold_handoffs.restype = ctypes.c_int
         lib.ssd_take_device_errors.argtypes = []
         lib.ssd_take_device_errors.restype = ctypes.c_uint
         lib.ssd_fwd_noalloc.argtypes = [dp] + [vp] * 10
@@ -129,6 +131,13 @@ def ssd_take_device_errors() -> int:
     """Read and clear the kernels' device-side error bits (0 = no bounded wait
     ever gave up).  Synchronises the device."""
     return int(load_library().ssd_take_device_errors())
+
+
+def ssd_debug_withhold_handoffs(on: bool) -> None:
+    """Test hook for failure detection: with ``on``, fwd_pass_state launches skip
+    their range hand-offs, so the receiving CTAs' bounded waits give up and the
+    launch ends early with error bit 0 set (see ``ssd_take_device_errors``)."""
+    _check(load_library().ssd_debug_withhold_handoffs(1 if on else 0))
 
 
 def ssd_fwd_workspace_bytes(dims: Dims) -> int:

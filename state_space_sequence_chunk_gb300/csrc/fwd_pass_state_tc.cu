@@ -57,6 +57,9 @@ namespace ssd {
 namespace {
 
 __device__ unsigned int g_fps_error;  // bit 0: a bounded wait gave up
+// Test hook (ssd_debug_withhold_handoffs): nonzero makes every range skip
+// publishing its end state, so that the receiving ranges' bounded waits run out.
+__device__ unsigned int g_fps_withhold;
 
 constexpr int kSub = 64;            // tokens per pipeline stage
 constexpr int kRowBytes = 128;      // one swizzle row (64 bf16)
@@ -182,7 +185,8 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     const uint32_t fold_done = smem_u32(bars + kB + 2 * kVecSlots);
     const uint32_t init_full = smem_u32(bars + kB + 2 * kVecSlots + 1);
     const uint32_t tile_free = smem_u32(bars + kB + 2 * kVecSlots + 2);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kB + 2 * kVecSlots + 3);
+    const uint32_t mma_drain = smem_u32(bars + kB + 2 * kVecSlots + 3);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kB + 2 * kVecSlots + 4);
     int* range_id = reinterpret_cast<int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -206,6 +210,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         mbar_init(fold_done, kFoldWarps);
         mbar_init(init_full, 32 * kFoldWarps);
         mbar_init(tile_free, 32 * kFoldWarps);
+        mbar_init(mma_drain, 1);
         fence_mbar_init();
         // ranges in dispatch order: the range before this one belongs to a CTA
         // that is already running
@@ -259,6 +264,13 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     }
                 }
             }
+            // No copy may land in shared memory after the CTA has left: wait for the
+            // last stages and g/dt slots issued (already complete unless a bounded
+            // wait elsewhere gave up and the consumers stopped early).
+            for (int j = i - min(i, S); j < i; ++j)
+                (void)mbar_wait(full(j % S), (j / S) & 1, &g_fps_error, 1u);
+            for (int j = cv - min(cv, kVecSlots); j < cv; ++j)
+                (void)mbar_wait(vec_full(j % kVecSlots), (j / kVecSlots) & 1, &g_fps_error, 1u);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer: one chunk product per accumulator slot ----------------
@@ -294,6 +306,9 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 }
                 if (!ok) break;
             }
+            // every MMA issued has finished before TMEM is released
+            mma_commit(mma_drain);
+            (void)mbar_wait(mma_drain, 0, &g_fps_error, 1u);
         }
     } else if (warp < 2 + kScalerWarps) {
         // ---------------- scaler warps: x_q <- x_q * dt_q 2^{g_last - g_q} ----------------
@@ -580,7 +595,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     bool okp = true;
                     if (rl == 0) {
                         okp = mbar_wait(fold_done, 0, &g_fps_error, 1u);
-                        if (okp) {
+                        if (okp && *reinterpret_cast<volatile unsigned int*>(&g_fps_withhold) == 0u) {
                             __threadfence();
                             st_release_gpu(flags + u.ch, (unsigned)u.c1);
                         }
@@ -685,6 +700,10 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     kern<<<(unsigned)q.G, kThreads, smem, stream>>>(tx, tb, init, Gcs, dtT, (__nv_bfloat16*)hiddens,
                                                     final_state, ring, ctrl, q);
     return cudaGetLastError();
+}
+
+cudaError_t set_fwd_pass_state_withhold(unsigned int on) {
+    return cudaMemcpyToSymbol(g_fps_withhold, &on, sizeof(on));
 }
 
 unsigned int take_fwd_pass_state_error() {

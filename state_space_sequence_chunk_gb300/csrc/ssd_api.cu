@@ -92,6 +92,10 @@ unsigned int ssd_take_device_errors(void) {
     return (a ? 1u : 0u) | (b ? 2u : 0u);
 }
 
+ssd_status ssd_debug_withhold_handoffs(int on) {
+    return from_cuda(set_fwd_pass_state_withhold(on ? 1u : 0u));
+}
+
 const char* ssd_status_string(ssd_status s) {
     switch (s) {
         case SSD_OK: return "ok";

@@ -64,6 +64,8 @@ cudaError_t launch_compute_out_tc(const Problem& p, const void* x, const void* B
 // Read and clear the device-side error word of a kernel module (bit 0: a
 // bounded wait gave up).  Synchronous.
 unsigned int take_fwd_pass_state_error();
+// Test hook: nonzero makes fwd_pass_state withhold its range hand-offs.
+cudaError_t set_fwd_pass_state_withhold(unsigned int on);
 unsigned int take_compute_out_error();
 
 // Element loads/stores shared by the kernels.

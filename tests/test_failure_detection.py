@@ -1,0 +1,43 @@
+"""Failure detection without a GPU fault.
+
+fwd_pass_state hands the running state from one CTA's work range to the next
+through a flag in global memory; the receiving CTA's wait is bounded (about
+1 s of SM clock).  Here a test hook makes every range withhold its hand-off: the
+waits must give up, the launch must end with the error bit set (no hang, no
+fault), and the same context must then produce correct results again.
+"""
+import time
+
+import numpy as np
+import pytest
+
+import state_space_sequence_chunk_gb300 as ssd
+from state_space_sequence_chunk_gb300 import synth
+from harness import TOL, gpu_fwd, oracle_fwd, rel_err, small, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def test_withheld_handoff_times_out_and_is_reported():
+    # 2 chains x 16 chunks: far fewer units than resident CTAs, so every CTA takes
+    # one chunk and each chain crosses 15 range boundaries
+    w = small(seqlen=4096, nheads=2, ngroups=1, headdim=64, dstate=128, chunk=256,
+              dtype="bf16", init_std=0.1, batch=1)
+    inp = synth.make_inputs(w)
+    dev = to_device(inp, "bf16")
+    assert ssd.ssd_take_device_errors() == 0
+    t0 = time.time()
+    try:
+        ssd.ssd_debug_withhold_handoffs(True)
+        ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                    dev["init_state"], chunk_size=256)
+        errs = ssd.ssd_take_device_errors()   # synchronises
+    finally:
+        ssd.ssd_debug_withhold_handoffs(False)
+    elapsed = time.time() - t0
+    assert errs & 1, "the bounded hand-off wait should have given up"
+    assert elapsed < 60
+    # the context is still usable, and the next call is exact again
+    y, fin = gpu_fwd(dev, 256)
+    y_ref, fin_ref = oracle_fwd(inp)
+    assert rel_err(y, y_ref) < TOL["bf16"] and rel_err(fin, fin_ref) < TOL["bf16"]
