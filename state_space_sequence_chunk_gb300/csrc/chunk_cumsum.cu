@@ -15,6 +15,7 @@
 // carrying the running total between blocks.  Tokens past
 // seqlen read as dt = 0, and the padded tail of the last chunk takes exactly
 // the value at the last real token.
+#include "sm100_ptx.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -28,6 +29,7 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
                     float* __restrict__ Gcs, float* __restrict__ dtT,
                     int L, int H, int Q, int Lp, unsigned int* zero_ptr, int zero_words) {
     __shared__ float tile[256][kHeadsPerCta + 1];
+    grid_launch_dependents();   // fwd_pass_state may start its set-up meanwhile
     // the first CTA also clears the next kernel's control block
     if (zero_ptr != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
         for (int i = threadIdx.x; i < zero_words; i += kThreads) zero_ptr[i] = 0u;

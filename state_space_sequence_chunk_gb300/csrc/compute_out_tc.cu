@@ -217,7 +217,10 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     for (int j = 0; j < Cfg::kBSlots; ++j) mbar_arrive(smem_u32(b_full + bslot[j]));
                     sc += Cfg::kBSlots;
                 }
-                // head stage: x, h, g, dt
+                // head stage: x, h, g, dt.  h, g and dt come from the earlier
+                // steps: the first head stage waits for them (the group's C and B,
+                // inputs, were requested before)
+                if (u == u0) grid_dependency_wait();
                 const int s = sc % NST, k = sc / NST;
                 mbar_wait(smem_u32(b_empty + s), (k & 1) ^ 1, err, 1u);
                 const uint32_t fb = smem_u32(b_full + s);
@@ -619,10 +622,19 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     if (e != cudaSuccess) return e;
     const int64_t units = p.b * p.nc * p.H;
     const int grid = (int)(units < sms ? units : sms);
-    kern<<<grid, kThreads, Cfg::kSmem, stream>>>(tx, tc, tb, th, ty, Gcs, dtT, D, (__nv_bfloat16*)y,
-                                                 (int)p.L, (int)p.H, (int)p.P, (int)p.nc,
-                                                 (int)p.Lp, (int)p.hpg, (int)units);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)Cfg::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.chained ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, tx, tc, tb, th, ty, Gcs, dtT, D, (__nv_bfloat16*)y, (int)p.L,
+                           (int)p.H, (int)p.P, (int)p.nc, (int)p.Lp, (int)p.hpg, (int)units);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

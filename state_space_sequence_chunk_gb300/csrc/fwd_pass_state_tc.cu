@@ -212,6 +212,8 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         mbar_init(tile_free, 32 * kFoldWarps);
         mbar_init(mma_drain, 1);
         fence_mbar_init();
+        // chunk_cumsum (G, dt, the cleared control block) must be complete
+        grid_dependency_wait();
         // ranges in dispatch order: the range before this one belongs to a CTA
         // that is already running
         *range_id = (int)atomicAdd(ctrl, 1u);
@@ -225,6 +227,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     const int rk = *range_id;
     const Range rg = range_of(rk, q);
     const int nchunks = rg.hi - rg.lo;
+    grid_launch_dependents();   // compute_out may take each SM as this kernel leaves it
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -697,9 +700,19 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     if ((int64_t)q.nchains * p.nc >= (int64_t)1 << 31) return cudaErrorInvalidValue;
     q.W = q.nchains * q.nc;
     q.G = std::min(q.W, resident);
-    kern<<<(unsigned)q.G, kThreads, smem, stream>>>(tx, tb, init, Gcs, dtT, (__nv_bfloat16*)hiddens,
-                                                    final_state, ring, ctrl, q);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)q.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.chained ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, tx, tb, init, Gcs, dtT, (__nv_bfloat16*)hiddens,
+                           final_state, ring, ctrl, q);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t set_fwd_pass_state_withhold(unsigned int on) {

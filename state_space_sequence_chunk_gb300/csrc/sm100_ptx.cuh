@@ -98,6 +98,20 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Wait until the grids this launch depends on have completed and their memory
+// is visible (returns at once for a launch without such a dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next launch on the stream to be scheduled (it still waits with
+// grid_dependency_wait before reading this grid's output).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Flags in global memory, for hand-offs between CTAs of one launch
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {

@@ -267,6 +267,7 @@ ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const floa
         has_scratch ? (unsigned int*)((char*)scratch + fwd_pass_state_ctrl_offset(p)) : nullptr;
     const int ctrl_words = has_scratch ? (int)(fwd_pass_state_ctrl_bytes(p) / 4) : 0;
     cudaStream_t st = (cudaStream_t)stream;
+    p.chained = true;
     // chunk_cumsum clears fwd_pass_state's control block on the way
     cudaError_t e = launch_chunk_cumsum(p, dt, A, Gcs, dtT, ctrl, ctrl_words, st);
     if (e == cudaSuccess)

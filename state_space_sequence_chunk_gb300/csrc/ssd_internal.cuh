@@ -22,6 +22,11 @@ struct Problem {
     int64_t hpg;  // heads per group, H / G
     int dtype;    // ssd_dtype
     int esize;    // bytes per element of x, B, C, y, hiddens
+    // Set by ssd_fwd: the three launches form one chain on one stream, so the
+    // tensor-core kernels are launched with programmatic dependent launch (each
+    // may start its set-up while its predecessor drains; its first read of the
+    // predecessor's output waits for that grid with griddepcontrol.wait).
+    bool chained = false;
 };
 
 inline size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
