@@ -618,6 +618,423 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     }
 }
 
+// ===========================================================================
+// Paired variant (no initial state, N <= 128, P <= 64, an even number of heads
+// per group): one CTA per SM walks two adjacent heads of the same group in
+// lockstep.  Both heads' chunk products take the same B tile as the MMA's A
+// operand, so every B tile is loaded once for two heads, and the 512 TMEM
+// columns of a whole SM hold both running states and six chunk products (three
+// per head in flight).  A work unit is one chunk of a pair-chain (batch, head
+// pair); ranges, pieces and hand-offs are those of the kernel above, with a
+// hand-off flag and a two-slot buffer per head.
+//
+// The two x tiles of a stage sit side by side, so one N = 128 MMA per K step
+// computes both heads' products (columns [0, 64) head 0, [64, 128) head 1 of a
+// product-slot pair).  With P = 64 (kTmaH) the chunk-start states leave through
+// a 128-byte-swizzled shared-memory tile per head and one TMA tensor store per
+// chunk (full 128-byte lines), instead of 16-byte stores from every thread,
+// one row per lane, that touch 32 lines per warp instruction.
+// ===========================================================================
+constexpr int kPProdSlots = 6;                    // chunk products in flight (3 per head)
+constexpr int kPScalerWarps = 8;
+constexpr int kPThreads = 32 * (2 + kPScalerWarps + 8);   // 576: + two fold warpgroups
+constexpr int kPStageBytes = 2 * kXBytes + kBBytes;       // x0 | x1 | B, 32 KB
+constexpr int kPVecSlots = 3;
+constexpr int kPVecSlotBytes = 4 * kMaxQ * 4;     // g, dt of both heads
+constexpr int kPBarBytes = 1024;
+constexpr int kPHBytes = 128 * kRowBytes;         // hiddens tile of one head: <= 128 rows of 64 p
+// TMA ring depth: five stages when two hiddens tiles share the shared memory
+template <bool kTmaH> __host__ __device__ constexpr int pair_stages() { return kTmaH ? 5 : 6; }
+template <bool kTmaH>
+__host__ __device__ constexpr int pair_smem() {
+    return pair_stages<kTmaH>() * kPStageBytes + (kTmaH ? 2 * kPHBytes : 0) +
+           kPVecSlots * kPVecSlotBytes + kPBarBytes + 1024;
+}
+constexpr uint32_t kIdescPair = make_idesc(1, 128, 2 * kCols, 1, 1);
+static_assert(kPStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+
+template <bool kTmaH>
+__global__ void __launch_bounds__(kPThreads, 1)
+fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                       const __grid_constant__ CUtensorMap tm_h,
+                       const float* __restrict__ Gcs, const float* __restrict__ dtT,
+                       __nv_bfloat16* __restrict__ hiddens, float* final_state, float* ring,
+                       unsigned int* ctrl, const FpsParams q) {
+    constexpr int S = pair_stages<kTmaH>();
+    constexpr int PS = kPProdSlots;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* htile = smem + S * kPStageBytes;  // kTmaH: hiddens tiles of head 0 / 1
+    uint8_t* vecs = htile + (kTmaH ? 2 * kPHBytes : 0);   // kPVecSlots x (g0, dt0, g1, dt1)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(vecs + kPVecSlots * kPVecSlotBytes);
+    auto full = [&](int s) { return smem_u32(bars + s); };
+    auto scaled = [&](int s) { return smem_u32(bars + S + s); };
+    auto empty = [&](int s) { return smem_u32(bars + 2 * S + s); };
+    auto prod_full = [&](int k) { return smem_u32(bars + 3 * S + k); };
+    auto prod_empty = [&](int k) { return smem_u32(bars + 3 * S + PS + k); };
+    auto vec_full = [&](int v) { return smem_u32(bars + 3 * S + 2 * PS + v); };
+    auto vec_empty = [&](int v) { return smem_u32(bars + 3 * S + 2 * PS + kPVecSlots + v); };
+    auto fold_done = [&](int hd) { return smem_u32(bars + 3 * S + 2 * PS + 2 * kPVecSlots + hd); };
+    const uint32_t mma_drain = smem_u32(bars + 3 * S + 2 * PS + 2 * kPVecSlots + 2);
+    // kTmaH: hiddens tile written (one arrival per fold warp) / read by its store
+    auto h_full = [&](int hd) { return smem_u32(bars + 3 * S + 2 * PS + 2 * kPVecSlots + 3 + hd); };
+    auto h_free = [&](int hd) { return smem_u32(bars + 3 * S + 2 * PS + 2 * kPVecSlots + 5 + hd); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 2 * PS + 2 * kPVecSlots + 7);
+    int* range_id = reinterpret_cast<int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nsub = q.Q / kSub;
+    unsigned int* flags = ctrl + kCtrlFlagOffset;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(scaled(s), 32 * kPScalerWarps);
+            mbar_init(empty(s), 1);
+        }
+        for (int k = 0; k < PS; ++k) {
+            mbar_init(prod_full(k), 1);
+            mbar_init(prod_empty(k), 128);
+        }
+        for (int v = 0; v < kPVecSlots; ++v) {
+            mbar_init(vec_full(v), 1);
+            mbar_init(vec_empty(v), 32 * kPScalerWarps);
+        }
+        mbar_init(fold_done(0), 4);
+        mbar_init(fold_done(1), 4);
+        mbar_init(mma_drain, 1);
+        for (int hd = 0; hd < 2; ++hd) {
+            mbar_init(h_full(hd), 4);
+            mbar_init(h_free(hd), 1);
+        }
+        fence_mbar_init();
+        grid_dependency_wait();   // chunk_cumsum (G, dt, the cleared control block)
+        *range_id = (int)atomicAdd(ctrl, 1u);
+    }
+    __syncwarp();
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t stage0 = smem_u32(smem);
+    const int rk = *range_id;
+    const Range rg = range_of(rk, q);
+    const int nchunks = rg.hi - rg.lo;
+    grid_launch_dependents();
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int i = 0, cv = 0;
+            bool ok = true;
+            for (int pi = 0; pi < rg.pieces() && ok; ++pi) {
+                const Piece u = piece_of(rg, pi, q);
+                const int bh0 = 2 * u.bh;                  // the pair's first head
+                const int b = bh0 / q.H, h0 = bh0 - b * q.H, grp = h0 / q.hpg;
+                const int64_t ro = (int64_t)bh0 * q.Lp;
+                for (int c = u.c0; c < u.c1 && ok; ++c, ++cv) {
+                    const int vslot = cv % kPVecSlots;
+                    if (!mbar_wait(vec_empty(vslot), ((cv / kPVecSlots) & 1) ^ 1, &g_fps_error, 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vs = smem_u32(vecs + vslot * kPVecSlotBytes);
+                    const int64_t co = (int64_t)c * q.Q;
+                    mbar_arrive_expect_tx(vec_full(vslot), 4 * q.Q * 4);
+                    bulk_load(vs, Gcs + ro + co, q.Q * 4, vec_full(vslot));
+                    bulk_load(vs + kMaxQ * 4, dtT + ro + co, q.Q * 4, vec_full(vslot));
+                    bulk_load(vs + 2 * kMaxQ * 4, Gcs + ro + q.Lp + co, q.Q * 4, vec_full(vslot));
+                    bulk_load(vs + 3 * kMaxQ * 4, dtT + ro + q.Lp + co, q.Q * 4, vec_full(vslot));
+                    for (int sub = 0; sub < nsub; ++sub, ++i) {
+                        const int s = i % S, k = i / S;
+                        if (!mbar_wait(empty(s), (k & 1) ^ 1, &g_fps_error, 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t xs = stage0 + s * kPStageBytes, bs = xs + 2 * kXBytes;
+                        const int tok = c * q.Q + sub * kSub;
+                        mbar_arrive_expect_tx(full(s), kPStageBytes);
+                        tma_load_4d(xs, &tm_x, full(s), 0, h0, tok, b);
+                        tma_load_4d(xs + kXBytes, &tm_x, full(s), 0, h0 + 1, tok, b);
+#pragma unroll
+                        for (int jb = 0; jb < 2; ++jb)
+                            tma_load_4d(bs + jb * kSub * kRowBytes, &tm_b, full(s), jb * 64, grp, tok, b);
+                    }
+                }
+            }
+            for (int j = i - min(i, S); j < i; ++j)
+                (void)mbar_wait(full(j % S), (j / S) & 1, &g_fps_error, 1u);
+            for (int j = cv - min(cv, kPVecSlots); j < cv; ++j)
+                (void)mbar_wait(vec_full(j % kPVecSlots), (j / kPVecSlots) & 1, &g_fps_error, 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: both heads' products share the B operand ----------------
+        if (lane == 0) {
+            int i = 0;
+            for (int qc = 0; qc < nchunks; ++qc) {
+                const int p0 = 2 * qc, p1 = 2 * qc + 1;   // product numbers of head 0 / 1
+                const int sl0 = p0 % PS, sl1 = p1 % PS;
+                bool ok = true;
+                for (int sub = 0; sub < nsub; ++sub, ++i) {
+                    const int s = i % S, k = i / S;
+                    if (!mbar_wait(scaled(s), k & 1, &g_fps_error, 1u)) { ok = false; break; }
+                    if (sub == 0 &&
+                        (!mbar_wait(prod_empty(sl0), ((p0 / PS) & 1) ^ 1, &g_fps_error, 1u) ||
+                         !mbar_wait(prod_empty(sl1), ((p1 / PS) & 1) ^ 1, &g_fps_error, 1u))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = stage0 + s * kPStageBytes, bs = xs + 2 * kXBytes;
+                    const uint64_t ad0 = smem_desc_sw128(bs, kSub * kRowBytes, 8 * kRowBytes);
+                    // B operand: x0 | x1, two 64-column swizzle atoms kXBytes apart;
+                    // the products of slot pair (sl0, sl1 = sl0 + 1) are adjacent in TMEM
+                    const uint64_t bd0 = smem_desc_sw128(xs, kXBytes, 8 * kRowBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kSub / 16; ++kk) {
+                        const uint64_t ko = (uint64_t)((kk * 16 * kRowBytes) >> 4);
+                        const uint32_t acc = (sub > 0 || kk > 0) ? 1u : 0u;
+                        mma_f16_ss(tmem + 128 + sl0 * kCols, ad0 + ko, bd0 + ko, kIdescPair, acc);
+                    }
+                    mma_commit(empty(s));
+                    if (sub == nsub - 1) {
+                        mma_commit(prod_full(sl0));
+                        mma_commit(prod_full(sl1));
+                    }
+                }
+                if (!ok) break;
+            }
+            mma_commit(mma_drain);
+            (void)mbar_wait(mma_drain, 0, &g_fps_error, 1u);
+        }
+    } else if (warp < 2 + kPScalerWarps) {
+        // ---------------- scaler warps: both heads' x rows ----------------
+        const int tid = threadIdx.x - 64;
+        constexpr int kVecs = 2 * kSub * 8;   // 16-byte vectors of the two x tiles
+        constexpr int kPer = kVecs / (32 * kPScalerWarps);
+        const int nstages = nchunks * nsub;
+        for (int i = 0; i < nstages; ++i) {
+            const int s = i % S, k = i / S;
+            const int cv = i / nsub, sub = i - cv * nsub, vslot = cv % kPVecSlots;
+            if (!mbar_wait(full(s), k & 1, &g_fps_error, 1u)) break;
+            if (sub == 0 && !mbar_wait(vec_full(vslot), (cv / kPVecSlots) & 1, &g_fps_error, 1u)) break;
+            const float* vbase = reinterpret_cast<const float*>(vecs + vslot * kPVecSlotBytes);
+            uint8_t* xs = smem + s * kPStageBytes;
+#pragma unroll
+            for (int kq = 0; kq < kPer; ++kq) {
+                const int v = tid + kq * 32 * kPScalerWarps;
+                const int hd = v >> 9, r = (v >> 3) & (kSub - 1);
+                const float* gch = vbase + hd * 2 * kMaxQ;    // g of this head's chunk
+                const float* gv = gch + sub * kSub;
+                const float* dv = gv + kMaxQ;
+                const float sc = dv[r] * exp2f(gch[q.Q - 1] - gv[r]);
+                uint4* ptr = reinterpret_cast<uint4*>(xs + hd * kXBytes + r * kRowBytes) + (v & 7);
+                uint4 w = *ptr;
+                w.x = pack_bf16(bf16lo(w.x) * sc, bf16hi(w.x) * sc);
+                w.y = pack_bf16(bf16lo(w.y) * sc, bf16hi(w.y) * sc);
+                w.z = pack_bf16(bf16lo(w.z) * sc, bf16hi(w.z) * sc);
+                w.w = pack_bf16(bf16lo(w.w) * sc, bf16hi(w.w) * sc);
+                *ptr = w;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(scaled(s));
+            if (sub == nsub - 1) mbar_arrive(vec_empty(vslot));
+        }
+    } else {
+        // ---------------- fold warpgroups: one per head of the pair ----------------
+        // Warps 10..13 fold head 0's products, 14..17 head 1's; thread = TMEM lane
+        // = state row n; the running state of head hd sits in TMEM columns
+        // [64 hd, 64 hd + 64).  Exits from this loop are warp-uniform.
+        const int hd = (warp - 2 - kPScalerWarps) >> 2;
+        const int quarter = warp & 3;
+        const int rl = quarter * 32 + lane;
+        const bool nok = rl < q.N;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t sa = lane_base + hd * kCols;
+        int qc = 0;
+        for (int pi = 0; pi < rg.pieces(); ++pi) {
+            const Piece u = piece_of(rg, pi, q);
+            const int bh = 2 * u.bh + hd;                  // this head
+            const int ch = 2 * u.ch + hd;                  // its hand-off chain
+            const int64_t sbase = (int64_t)bh * q.P * q.N;
+            const float* grow = Gcs + (int64_t)bh * q.Lp + q.Q - 1;
+            float gl_next = grow[(int64_t)u.c0 * q.Q];
+            if (u.c0 == 0) {
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = 0u;
+                    __syncwarp();
+                    tmem_st_x16(sa + 16 * jj, v);
+                }
+            } else {
+                bool ok = true;
+                if (lane == 0) ok = flag_wait_geq(flags + ch, (unsigned)u.c0, &g_fps_error, 1u);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                (void)ld_acquire_gpu(flags + ch);
+                const float* src = ring + ((int64_t)ch * 2 + ((rk - 1) & 1)) * kSlotFloats;
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float4 f = __ldcg(reinterpret_cast<const float4*>(src + ((4 * jj + q4) * 128 + rl) * 4));
+                        v[4 * q4] = __float_as_uint(f.x); v[4 * q4 + 1] = __float_as_uint(f.y);
+                        v[4 * q4 + 2] = __float_as_uint(f.z); v[4 * q4 + 3] = __float_as_uint(f.w);
+                    }
+                    __syncwarp();
+                    tmem_st_x16(sa + 16 * jj, v);
+                }
+            }
+            tmem_wait_st();
+            bool ok = true;
+            for (int c = u.c0; c < u.c1; ++c, ++qc) {
+                const float e = exp2f(gl_next);
+                if (c + 1 < u.c1) gl_next = grow[(int64_t)(c + 1) * q.Q];
+                const int pn = 2 * qc + hd, slot = pn % PS;
+                if (!__all_sync(0xffffffffu, mbar_wait(prod_full(slot), (pn / PS) & 1, &g_fps_error, 1u))) {
+                    ok = false;
+                    break;
+                }
+                if (kTmaH && qc > 0) {
+                    // the previous chunk's store has read this head's tile
+                    if (rl == 0) {
+                        bulk_wait_group_read0();
+                        mbar_arrive(h_free(hd));
+                    }
+                    if (!__all_sync(0xffffffffu, mbar_wait(h_free(hd), (qc - 1) & 1, &g_fps_error, 1u))) {
+                        ok = false;
+                        break;
+                    }
+                }
+                tc_fence_after();
+                const uint32_t acc = lane_base + 128 + slot * kCols;
+                __nv_bfloat16* hp = hiddens + (((int64_t)bh * q.nc + c) * q.N + rl) * q.P;
+                // row rl of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rl % 8)) * 16
+                uint8_t* trow = htile + hd * kPHBytes + rl * kRowBytes;
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    __syncwarp();
+                    uint32_t sv[16], d[16];
+                    tmem_ld_x16(sa + 16 * jj, sv);
+                    tmem_ld_x16(acc + 16 * jj, d);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        d[k] = __float_as_uint(fmaf(e, __uint_as_float(sv[k]), __uint_as_float(d[k])));
+                    tmem_st_x16(sa + 16 * jj, d);
+                    if (kTmaH) {
+                        if (nok) {
+                            uint4 w0, w1;
+                            w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
+                            w0.y = pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3]));
+                            w0.z = pack_bf16(__uint_as_float(sv[4]), __uint_as_float(sv[5]));
+                            w0.w = pack_bf16(__uint_as_float(sv[6]), __uint_as_float(sv[7]));
+                            w1.x = pack_bf16(__uint_as_float(sv[8]), __uint_as_float(sv[9]));
+                            w1.y = pack_bf16(__uint_as_float(sv[10]), __uint_as_float(sv[11]));
+                            w1.z = pack_bf16(__uint_as_float(sv[12]), __uint_as_float(sv[13]));
+                            w1.w = pack_bf16(__uint_as_float(sv[14]), __uint_as_float(sv[15]));
+                            *reinterpret_cast<uint4*>(trow + (((2 * jj) ^ (rl & 7)) << 4)) = w0;
+                            *reinterpret_cast<uint4*>(trow + (((2 * jj + 1) ^ (rl & 7)) << 4)) = w1;
+                        }
+                    } else if (nok && 16 * jj < q.P) {
+                        uint4 w0, w1;
+                        w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
+                        w0.y = pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3]));
+                        w0.z = pack_bf16(__uint_as_float(sv[4]), __uint_as_float(sv[5]));
+                        w0.w = pack_bf16(__uint_as_float(sv[6]), __uint_as_float(sv[7]));
+                        w1.x = pack_bf16(__uint_as_float(sv[8]), __uint_as_float(sv[9]));
+                        w1.y = pack_bf16(__uint_as_float(sv[10]), __uint_as_float(sv[11]));
+                        w1.z = pack_bf16(__uint_as_float(sv[12]), __uint_as_float(sv[13]));
+                        w1.w = pack_bf16(__uint_as_float(sv[14]), __uint_as_float(sv[15]));
+                        uint4* hdst = reinterpret_cast<uint4*>(hp + 16 * jj);
+                        hdst[0] = w0;
+                        hdst[1] = w1;
+                    }
+                }
+                if (kTmaH) {
+                    fence_proxy_async_smem();   // tile writes -> the TMA store
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(h_full(hd));
+                }
+                __syncwarp();
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(prod_empty(slot));
+                if (kTmaH) {
+                    bool okh = true;
+                    if (rl == 0) {
+                        okh = mbar_wait(h_full(hd), qc & 1, &g_fps_error, 1u);
+                        if (okh) {
+                            tma_store_3d(&tm_h, smem_u32(htile + hd * kPHBytes), 0, 0, bh * q.nc + c);
+                            bulk_commit_group();
+                        }
+                    }
+                    if (!__all_sync(0xffffffffu, okh)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const bool last = u.c1 == q.nc;
+            if (last) {
+                if (final_state != nullptr) {
+                    const int pl = nok ? q.P : 0;
+#pragma unroll
+                    for (int jj = 0; jj < kCols / 16; ++jj) {
+                        __syncwarp();
+                        uint32_t sv[16];
+                        tmem_ld_x16(sa + 16 * jj, sv);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (16 * jj + k < pl)
+                                final_state[sbase + (int64_t)(16 * jj + k) * q.N + rl] = __uint_as_float(sv[k]);
+                    }
+                }
+            } else {
+                float* dst = ring + ((int64_t)ch * 2 + (rk & 1)) * kSlotFloats;
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    __syncwarp();
+                    uint32_t sv[16];
+                    tmem_ld_x16(sa + 16 * jj, sv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        __stcg(reinterpret_cast<float4*>(dst + ((4 * jj + q4) * 128 + rl) * 4),
+                               make_float4(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1]),
+                                           __uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(fold_done(hd));
+                bool okp = true;
+                if (rl == 0) {
+                    okp = mbar_wait(fold_done(hd), 0, &g_fps_error, 1u);
+                    if (okp && *reinterpret_cast<volatile unsigned int*>(&g_fps_withhold) == 0u) {
+                        __threadfence();
+                        st_release_gpu(flags + ch, (unsigned)u.c1);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, okp, 0)) break;
+            }
+        }
+        if (kTmaH && rl == 0) bulk_wait_group0();   // the hiddens stores have completed
+    }
+    __syncwarp();   // lanes that skipped a role loop wait for its lane 0
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 int64_t chains(const Problem& p) { return p.b * p.H * ((p.N + 127) / 128) * ((p.P + 63) / 64); }
 size_t ring_bytes(const Problem& p) {
     return round_up256((size_t)chains(p) * 2 * kSlotFloats * sizeof(float));
@@ -654,6 +1071,13 @@ cudaError_t resident_ctas(int* out) {
     return cudaSuccess;
 }
 
+// The paired kernel serves inputs without an initial state whose state block
+// fits one chain (N <= 128, P <= 64) and whose groups hold an even number of
+// heads, so that heads 2k and 2k+1 read the same B.
+bool paired(const Problem& p, const float* init) {
+    return init == nullptr && p.N <= 128 && p.P <= 64 && p.H % 2 == 0 && p.hpg % 2 == 0;
+}
+
 }  // namespace
 
 size_t fwd_pass_state_scratch_bytes(const Problem& p) {
@@ -682,15 +1106,6 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
         !encode_tmap_4d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, bd, bs, box,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    auto kern = init != nullptr ? fwd_pass_state_tc<true> : fwd_pass_state_tc<false>;
-    const int smem = init != nullptr ? smem_bytes<true>() : smem_bytes<false>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    int resident = 0;
-    if ((e = resident_ctas(&resident)) != cudaSuccess) return e;
     FpsParams q;
     q.H = (int)p.H; q.P = (int)p.P; q.N = (int)p.N; q.Q = (int)p.Q; q.nc = (int)p.nc;
     q.Lp = (int)p.Lp; q.hpg = (int)p.hpg;
@@ -698,18 +1113,63 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     q.npb = (int)((p.P + 63) / 64);
     q.nchains = (int)chains(p);
     if ((int64_t)q.nchains * p.nc >= (int64_t)1 << 31) return cudaErrorInvalidValue;
-    q.W = q.nchains * q.nc;
-    q.G = std::min(q.W, resident);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)q.G);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.chained ? 1 : 0;
+    cudaError_t e;
+    if (paired(p, init)) {
+        // one CTA per SM; a chain is a pair of heads (its flags and hand-off
+        // slots stay per head: chains() counts heads)
+        // P = 64: hiddens leave through TMA stores of [N rows][64 p] tiles
+        const bool tma_h = p.P == 64;
+        CUtensorMap th;
+        memset(&th, 0, sizeof(th));
+        if (tma_h) {
+            const uint64_t hd[3] = {(uint64_t)p.P, (uint64_t)p.N, (uint64_t)(p.b * p.H * p.nc)};
+            const uint64_t hs[2] = {(uint64_t)p.P * 2, (uint64_t)p.N * p.P * 2};
+            const uint32_t hbox[3] = {64, (uint32_t)p.N, 1};
+            if (!encode_tmap(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, hiddens, hd, hs, hbox,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+        }
+        auto pk = tma_h ? fwd_pass_state_pair_tc<true> : fwd_pass_state_pair_tc<false>;
+        const int psmem = tma_h ? pair_smem<true>() : pair_smem<false>();
+        if ((e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(pk, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return e;
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        q.nchains /= 2;
+        q.W = q.nchains * q.nc;
+        q.G = std::min(q.W, sms);
+        cfg.gridDim = dim3((unsigned)q.G);
+        cfg.blockDim = dim3(kPThreads);
+        cfg.dynamicSmemBytes = (size_t)psmem;
+        e = cudaLaunchKernelEx(&cfg, pk, tx, tb, th, Gcs, dtT, (__nv_bfloat16*)hiddens, final_state,
+                               ring, ctrl, q);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
+    auto kern = init != nullptr ? fwd_pass_state_tc<true> : fwd_pass_state_tc<false>;
+    const int smem = init != nullptr ? smem_bytes<true>() : smem_bytes<false>();
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int resident = 0;
+    if ((e = resident_ctas(&resident)) != cudaSuccess) return e;
+    q.W = q.nchains * q.nc;
+    q.G = std::min(q.W, resident);
+    cfg.gridDim = dim3((unsigned)q.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
     e = cudaLaunchKernelEx(&cfg, kern, tx, tb, init, Gcs, dtT, (__nv_bfloat16*)hiddens,
                            final_state, ring, ctrl, q);
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -18,11 +18,13 @@ from harness import TOL, gpu_fwd, oracle_fwd, rel_err, small, to_device
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_handoff_times_out_and_is_reported():
-    # 2 chains x 16 chunks: far fewer units than resident CTAs, so every CTA takes
-    # one chunk and each chain crosses 15 range boundaries
+@pytest.mark.parametrize("init_std", [0.1, 0.0], ids=["per-head", "paired-heads"])
+def test_withheld_handoff_times_out_and_is_reported(init_std):
+    # 2 heads x 16 chunks: far fewer units than CTAs, so every CTA takes one
+    # chunk and each chain crosses 15 range boundaries.  Without an initial
+    # state the two heads walk as one pair-chain.
     w = small(seqlen=4096, nheads=2, ngroups=1, headdim=64, dstate=128, chunk=256,
-              dtype="bf16", init_std=0.1, batch=1)
+              dtype="bf16", init_std=init_std, batch=1)
     inp = synth.make_inputs(w)
     dev = to_device(inp, "bf16")
     assert ssd.ssd_take_device_errors() == 0

@@ -83,6 +83,11 @@ CASES = [
     ("bf16", 64, 200, 2, 2, 128, 256, True, True),    # largest P and N
     ("bf16", 128, 333, 2, 1, 16, 16, True, True),     # smallest P and N
     ("bf16", 64, 150, 2, 1, 48, 48, True, True),      # N splits a warp's state rows
+    # no initial state: heads 2k, 2k+1 of one group walk together, sharing B
+    ("bf16", 128, 1000, 6, 3, 32, 64, False, True),   # paired heads, ragged tail
+    ("bf16", 256, 4096, 4, 1, 64, 128, False, False), # paired, one chunk per CTA
+    ("bf16", 64, 700, 6, 2, 64, 128, False, True),    # odd heads per group: unpaired
+    ("bf16", 64, 300, 4, 2, 64, 48, False, True),     # paired, TMA-stored 48-row states
 ]
 
 
