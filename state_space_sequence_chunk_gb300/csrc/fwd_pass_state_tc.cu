@@ -651,15 +651,34 @@ __host__ __device__ constexpr int pair_smem() {
            kPVecSlots * kPVecSlotBytes + kPBarBytes + 1024;
 }
 constexpr uint32_t kIdescPair = make_idesc(1, 128, 2 * kCols, 1, 1);
+
+// Long chains (many ranges per chain) run in two passes instead of handing
+// the state from range to range in order (a serial walk over every chunk of
+// the chain):
+//   kModeLocal  every piece starts from a zero state and keeps no hiddens; it
+//               writes its end state A and its log2 decay sum to the aggregate
+//               buffer (one slot per head of piece 2 k + [second chain of
+//               range k]);
+//   scan        a CUDA-core kernel walks each head's pieces in chunk order:
+//               start = S, S <- 2^{sum} S + A, replacing A by the piece's
+//               start state, and writes final_state;
+//   kModeApply  every piece starts from its start state and writes hiddens.
+// Ranges are then independent, and a chain's serial part is one fma per
+// element and piece.  A range spans at most two chains here (range length <=
+// nc), so slot indices 2 k and 2 k + 1 cover every piece.
+constexpr int kModeHandoff = 0;
+constexpr int kModeLocal = 1;
+constexpr int kModeApply = 2;
 static_assert(kPStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 
-template <bool kTmaH>
+template <bool kTmaH, int kMode>
 __global__ void __launch_bounds__(kPThreads, 1)
 fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                        const __grid_constant__ CUtensorMap tm_h,
                        const float* __restrict__ Gcs, const float* __restrict__ dtT,
                        __nv_bfloat16* __restrict__ hiddens, float* final_state, float* ring,
-                       unsigned int* ctrl, const FpsParams q) {
+                       unsigned int* ctrl, float* agg, float* agg_lsum, const FpsParams q) {
+    static_assert(kMode != kModeLocal || !kTmaH, "the local pass stores no hiddens");
     constexpr int S = pair_stages<kTmaH>();
     constexpr int PS = kPProdSlots;
     extern __shared__ uint8_t smem_raw[];
@@ -710,7 +729,8 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         }
         fence_mbar_init();
         grid_dependency_wait();   // chunk_cumsum (G, dt, the cleared control block)
-        *range_id = (int)atomicAdd(ctrl, 1u);
+        // hand-offs need ranges in dispatch order; the two passes have none
+        *range_id = kMode == kModeHandoff ? (int)atomicAdd(ctrl, 1u) : (int)blockIdx.x;
     }
     __syncwarp();
     if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
@@ -861,7 +881,24 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             const int64_t sbase = (int64_t)bh * q.P * q.N;
             const float* grow = Gcs + (int64_t)bh * q.Lp + q.Q - 1;
             float gl_next = grow[(int64_t)u.c0 * q.Q];
-            if (u.c0 == 0) {
+            float lsum = 0.f;   // kModeLocal: log2 of the piece's decay product
+            // kModeLocal / kModeApply: the piece's aggregate slot
+            const int64_t aslot = (int64_t)(2 * rk + (u.ch == rg.ch_first ? 0 : 1)) * 2 + hd;
+            if (kMode == kModeApply) {
+                const float* src = agg + aslot * kSlotFloats;
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float4 f = __ldcg(reinterpret_cast<const float4*>(src + ((4 * jj + q4) * 128 + rl) * 4));
+                        v[4 * q4] = __float_as_uint(f.x); v[4 * q4 + 1] = __float_as_uint(f.y);
+                        v[4 * q4 + 2] = __float_as_uint(f.z); v[4 * q4 + 3] = __float_as_uint(f.w);
+                    }
+                    __syncwarp();
+                    tmem_st_x16(sa + 16 * jj, v);
+                }
+            } else if (kMode == kModeLocal || u.c0 == 0) {
 #pragma unroll
                 for (int jj = 0; jj < kCols / 16; ++jj) {
                     uint32_t v[16];
@@ -893,6 +930,7 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             bool ok = true;
             for (int c = u.c0; c < u.c1; ++c, ++qc) {
                 const float e = exp2f(gl_next);
+                lsum += gl_next;
                 if (c + 1 < u.c1) gl_next = grow[(int64_t)(c + 1) * q.Q];
                 const int pn = 2 * qc + hd, slot = pn % PS;
                 if (!__all_sync(0xffffffffu, mbar_wait(prod_full(slot), (pn / PS) & 1, &g_fps_error, 1u))) {
@@ -926,7 +964,9 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                     for (int k = 0; k < 16; ++k)
                         d[k] = __float_as_uint(fmaf(e, __uint_as_float(sv[k]), __uint_as_float(d[k])));
                     tmem_st_x16(sa + 16 * jj, d);
-                    if (kTmaH) {
+                    if (kMode == kModeLocal) {
+                        // no hiddens in the local pass
+                    } else if (kTmaH) {
                         if (nok) {
                             uint4 w0, w1;
                             w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
@@ -981,7 +1021,25 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             }
             if (!__all_sync(0xffffffffu, ok)) break;
             const bool last = u.c1 == q.nc;
-            if (last) {
+            if (kMode == kModeLocal) {
+                // the piece's end state and log2 decay, for the scan
+                float* dst = agg + aslot * kSlotFloats;
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    __syncwarp();
+                    uint32_t sv[16];
+                    tmem_ld_x16(sa + 16 * jj, sv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        __stcg(reinterpret_cast<float4*>(dst + ((4 * jj + q4) * 128 + rl) * 4),
+                               make_float4(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1]),
+                                           __uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])));
+                }
+                if (rl == 0) agg_lsum[aslot] = lsum;
+            } else if (kMode == kModeApply) {
+                // final_state comes from the scan
+            } else if (last) {
                 if (final_state != nullptr) {
                     const int pl = nok ? q.P : 0;
 #pragma unroll
@@ -1035,6 +1093,39 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     }
 }
 
+// The scan between the two passes (CUDA cores).  Thread = one element of a
+// head's state in the aggregate-slot layout (float4 column group, TMEM lane,
+// component), blockIdx.y = batch * H + head.  It walks the head's pieces in
+// chunk order (ranges k = the one holding the chain's first unit, k + 1, ...):
+// start = S, S <- 2^{sum} S + A, with the piece's start state written over A.
+// S begins at init_state (or zero) and ends as final_state.
+__global__ void __launch_bounds__(256)
+fwd_pass_state_scan(const float* init, float* agg, const float* __restrict__ agg_lsum,
+                    float* final_state, const FpsParams q) {
+    const int f = blockIdx.x * blockDim.x + threadIdx.x;
+    if (f >= kSlotFloats) return;
+    const int bh = blockIdx.y, pc = bh >> 1, hd = bh & 1;
+    const int n = (f >> 2) & 127, p = (f >> 9) * 4 + (f & 3);
+    const bool valid = p < q.P && n < q.N;
+    const int64_t sidx = ((int64_t)bh * q.P + p) * q.N + n;
+    float S = (init != nullptr && valid) ? init[sidx] : 0.f;
+    const int u0 = pc * q.nc, u1 = u0 + q.nc;   // the pair-chain's units
+    int k = (int)((long long)u0 * q.G / q.W);
+    while (k + 1 < q.G && (int)((long long)(k + 1) * q.W / q.G) <= u0) ++k;
+    while (k > 0 && (int)((long long)k * q.W / q.G) > u0) --k;
+    for (; k < q.G; ++k) {
+        const int lo = (int)((long long)k * q.W / q.G);
+        if (lo >= u1) break;
+        const int64_t aslot = (int64_t)(2 * k + (lo / q.nc == pc ? 0 : 1)) * 2 + hd;
+        float* a = agg + aslot * kSlotFloats + f;
+        const float A = __ldcg(a);
+        const float decay = exp2f(__ldcg(agg_lsum + aslot));
+        __stcg(a, S);
+        S = fmaf(decay, S, A);
+    }
+    if (final_state != nullptr && valid) final_state[sidx] = S;
+}
+
 int64_t chains(const Problem& p) { return p.b * p.H * ((p.N + 127) / 128) * ((p.P + 63) / 64); }
 size_t ring_bytes(const Problem& p) {
     return round_up256((size_t)chains(p) * 2 * kSlotFloats * sizeof(float));
@@ -1074,15 +1165,32 @@ cudaError_t resident_ctas(int* out) {
 // The paired kernel serves inputs without an initial state whose state block
 // fits one chain (N <= 128, P <= 64) and whose groups hold an even number of
 // heads, so that heads 2k and 2k+1 read the same B.
-bool paired(const Problem& p, const float* init) {
-    return init == nullptr && p.N <= 128 && p.P <= 64 && p.H % 2 == 0 && p.hpg % 2 == 0;
+bool pair_geometry(const Problem& p) {
+    return p.N <= 128 && p.P <= 64 && p.H % 2 == 0 && p.hpg % 2 == 0;
+}
+bool paired(const Problem& p, const float* init) { return init == nullptr && pair_geometry(p); }
+
+// Two passes for long chains (the paired kernel's local and apply modes with
+// the scan between them), with an initial state or without.  The workspace
+// holds the aggregate slots for up to kTwoPassMaxCtas ranges whenever a
+// problem could take this path; whether it does depends on the device's SM
+// count (a range must not span more than two chains).
+constexpr int kTwoPassMinChunks = 64;
+constexpr int kTwoPassMaxCtas = 256;
+bool two_pass_candidate(const Problem& p) {
+    return p.dtype == SSD_BF16 && pair_geometry(p) && p.nc >= kTwoPassMinChunks;
+}
+size_t agg_state_bytes() { return round_up256((size_t)2 * kTwoPassMaxCtas * 2 * kSlotFloats * 4); }
+size_t agg_bytes(const Problem& p) {
+    return two_pass_candidate(p) ? agg_state_bytes() + round_up256((size_t)2 * kTwoPassMaxCtas * 2 * 4)
+                                 : 0;
 }
 
 }  // namespace
 
 size_t fwd_pass_state_scratch_bytes(const Problem& p) {
     if (p.dtype != SSD_BF16 || p.b == 0 || p.L == 0) return 0;
-    return ring_bytes(p) + ctrl_bytes(p);
+    return ring_bytes(p) + ctrl_bytes(p) + agg_bytes(p);
 }
 size_t fwd_pass_state_ctrl_offset(const Problem& p) { return ring_bytes(p); }
 size_t fwd_pass_state_ctrl_bytes(const Problem& p) { return ctrl_bytes(p); }
@@ -1121,7 +1229,17 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     cfg.attrs = attr;
     cfg.numAttrs = p.chained ? 1 : 0;
     cudaError_t e;
-    if (paired(p, init)) {
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    bool two_pass = false;
+    if (two_pass_candidate(p)) {
+        const int64_t W2 = (int64_t)(q.nchains / 2) * p.nc;
+        const int64_t G2 = std::min<int64_t>(std::min<int64_t>(W2, sms), kTwoPassMaxCtas);
+        two_pass = (W2 + G2 - 1) / G2 <= p.nc / 2;   // two or more ranges per chain
+    }
+    if (two_pass || paired(p, init)) {
         // one CTA per SM; a chain is a pair of heads (its flags and hand-off
         // slots stay per head: chains() counts heads)
         // P = 64: hiddens leave through TMA stores of [N rows][64 p] tiles
@@ -1136,25 +1254,44 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
                              CU_TENSOR_MAP_SWIZZLE_128B))
                 return cudaErrorInvalidValue;
         }
-        auto pk = tma_h ? fwd_pass_state_pair_tc<true> : fwd_pass_state_pair_tc<false>;
-        const int psmem = tma_h ? pair_smem<true>() : pair_smem<false>();
-        if ((e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(pk, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
-            return e;
-        int dev = 0, sms = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return e;
         q.nchains /= 2;
         q.W = q.nchains * q.nc;
         q.G = std::min(q.W, sms);
+        if (two_pass) q.G = std::min(q.G, kTwoPassMaxCtas);
         cfg.gridDim = dim3((unsigned)q.G);
         cfg.blockDim = dim3(kPThreads);
-        cfg.dynamicSmemBytes = (size_t)psmem;
-        e = cudaLaunchKernelEx(&cfg, pk, tx, tb, th, Gcs, dtT, (__nv_bfloat16*)hiddens, final_state,
-                               ring, ctrl, q);
-        return e != cudaSuccess ? e : cudaGetLastError();
+        using PairKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, const float*,
+                                    __nv_bfloat16*, float*, float*, unsigned int*, float*, float*,
+                                    FpsParams);
+        auto launch_pair = [&](PairKernel pk, int psmem, float* agg, float* lsum) -> cudaError_t {
+            cudaError_t le;
+            if ((le = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) !=
+                    cudaSuccess ||
+                (le = cudaFuncSetAttribute(pk, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+                return le;
+            cfg.dynamicSmemBytes = (size_t)psmem;
+            le = cudaLaunchKernelEx(&cfg, pk, tx, tb, th, Gcs, dtT, (__nv_bfloat16*)hiddens,
+                                    final_state, ring, ctrl, agg, lsum, q);
+            return le != cudaSuccess ? le : cudaGetLastError();
+        };
+        if (!two_pass)
+            return tma_h ? launch_pair(fwd_pass_state_pair_tc<true, kModeHandoff>, pair_smem<true>(),
+                                       nullptr, nullptr)
+                         : launch_pair(fwd_pass_state_pair_tc<false, kModeHandoff>, pair_smem<false>(),
+                                       nullptr, nullptr);
+        float* agg = (float*)((char*)scratch + ring_bytes(p) + ctrl_bytes(p));
+        float* lsum = (float*)((char*)agg + agg_state_bytes());
+        if ((e = launch_pair(fwd_pass_state_pair_tc<false, kModeLocal>, pair_smem<false>(), agg,
+                             lsum)) != cudaSuccess)
+            return e;
+        fwd_pass_state_scan<<<dim3((kSlotFloats + 255) / 256, (unsigned)(p.b * p.H)), 256, 0, stream>>>(
+            init, agg, lsum, final_state, q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        cfg.numAttrs = p.chained ? 1 : 0;   // the apply pass may set up while the scan runs
+        return tma_h ? launch_pair(fwd_pass_state_pair_tc<true, kModeApply>, pair_smem<true>(), agg, lsum)
+                     : launch_pair(fwd_pass_state_pair_tc<false, kModeApply>, pair_smem<false>(), agg,
+                                   lsum);
     }
     auto kern = init != nullptr ? fwd_pass_state_tc<true> : fwd_pass_state_tc<false>;
     const int smem = init != nullptr ? smem_bytes<true>() : smem_bytes<false>();

@@ -72,6 +72,17 @@ def test_workspace_bytes(lib):
     chains2 = 2 * 4 * 2
     assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(d2)) == (
         ru(chains2 * 2 * 128 * 128 * 4) + ru((32 + chains2) * 4))
+    # long chains (nc >= 64, paired-head geometry): + aggregate slots for up to
+    # 256 ranges (two fp32 state slots of 128 x 64 per range and head pair) and
+    # their log2 decay sums
+    dl = dims(seqlen=64 * 128)
+    chains_l = 2 * 4
+    agg = ru(2 * 256 * 2 * 128 * 64 * 4) + ru(2 * 256 * 2 * 4)
+    assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(dl)) == (
+        ru(chains_l * 2 * 128 * 64 * 4) + ru((32 + chains_l) * 4) + agg)
+    dodd = dims(seqlen=64 * 128, ngroups=4)   # one head per group: no pairs
+    assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(dodd)) == (
+        ru(chains_l * 2 * 128 * 64 * 4) + ru((32 + chains_l) * 4))
     assert ssd.ssd_fwd_workspace_bytes(dims(seqlen=0)) == 0
     assert ssd.ssd_fwd_workspace_bytes(dims(chunk_size=100)) == 0
 
