@@ -619,14 +619,16 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
 }
 
 // ===========================================================================
-// Paired variant (no initial state, N <= 128, P <= 64, an even number of heads
-// per group): one CTA per SM walks two adjacent heads of the same group in
+// Paired variant (N <= 128, P <= 64, an even number of heads per group): one
+// CTA per SM walks two adjacent heads of the same group in
 // lockstep.  Both heads' chunk products take the same B tile as the MMA's A
 // operand, so every B tile is loaded once for two heads, and the 512 TMEM
 // columns of a whole SM hold both running states and six chunk products (three
 // per head in flight).  A work unit is one chunk of a pair-chain (batch, head
 // pair); ranges, pieces and hand-offs are those of the kernel above, with a
-// hand-off flag and a two-slot buffer per head.
+// hand-off flag and a two-slot buffer per head.  A chain's initial state is
+// read from init_state at its first chunk (lane n of each warp takes column n,
+// so every row of the read is one coalesced 128-byte line).
 //
 // The two x tiles of a stage sit side by side, so one N = 128 MMA per K step
 // computes both heads' products (columns [0, 64) head 0, [64, 128) head 1 of a
@@ -674,7 +676,7 @@ static_assert(kPStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle 
 template <bool kTmaH, int kMode>
 __global__ void __launch_bounds__(kPThreads, 1)
 fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                       const __grid_constant__ CUtensorMap tm_h,
+                       const __grid_constant__ CUtensorMap tm_h, const float* init,
                        const float* __restrict__ Gcs, const float* __restrict__ dtT,
                        __nv_bfloat16* __restrict__ hiddens, float* final_state, float* ring,
                        unsigned int* ctrl, float* agg, float* agg_lsum, const FpsParams q) {
@@ -899,11 +901,15 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                     tmem_st_x16(sa + 16 * jj, v);
                 }
             } else if (kMode == kModeLocal || u.c0 == 0) {
+                // zero, or (hand-off mode) the chain's initial state [P][N]:
+                // lane rl takes column n = rl, coalesced across the warp
+                const float* ib = (kMode == kModeHandoff && init != nullptr && nok) ? init + sbase + rl : nullptr;
 #pragma unroll
                 for (int jj = 0; jj < kCols / 16; ++jj) {
                     uint32_t v[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = 0u;
+                    for (int k = 0; k < 16; ++k)
+                        v[k] = (ib != nullptr && 16 * jj + k < q.P) ? __float_as_uint(__ldg(ib + (int64_t)(16 * jj + k) * q.N)) : 0u;
                     __syncwarp();
                     tmem_st_x16(sa + 16 * jj, v);
                 }
@@ -1162,13 +1168,13 @@ cudaError_t resident_ctas(int* out) {
     return cudaSuccess;
 }
 
-// The paired kernel serves inputs without an initial state whose state block
-// fits one chain (N <= 128, P <= 64) and whose groups hold an even number of
-// heads, so that heads 2k and 2k+1 read the same B.
+// The paired kernel serves inputs whose state block fits one chain (N <= 128,
+// P <= 64) and whose groups hold an even number of heads, so that heads 2k
+// and 2k+1 read the same B.
 bool pair_geometry(const Problem& p) {
     return p.N <= 128 && p.P <= 64 && p.H % 2 == 0 && p.hpg % 2 == 0;
 }
-bool paired(const Problem& p, const float* init) { return init == nullptr && pair_geometry(p); }
+bool paired(const Problem& p) { return pair_geometry(p); }
 
 // Two passes for long chains (the paired kernel's local and apply modes with
 // the scan between them), with an initial state or without.  The workspace
@@ -1239,7 +1245,7 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
         const int64_t G2 = std::min<int64_t>(std::min<int64_t>(W2, sms), kTwoPassMaxCtas);
         two_pass = (W2 + G2 - 1) / G2 <= p.nc / 2;   // two or more ranges per chain
     }
-    if (two_pass || paired(p, init)) {
+    if (two_pass || paired(p)) {
         // one CTA per SM; a chain is a pair of heads (its flags and hand-off
         // slots stay per head: chains() counts heads)
         // P = 64: hiddens leave through TMA stores of [N rows][64 p] tiles
@@ -1261,8 +1267,8 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
         cfg.gridDim = dim3((unsigned)q.G);
         cfg.blockDim = dim3(kPThreads);
         using PairKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, const float*,
-                                    __nv_bfloat16*, float*, float*, unsigned int*, float*, float*,
-                                    FpsParams);
+                                    const float*, __nv_bfloat16*, float*, float*, unsigned int*, float*,
+                                    float*, FpsParams);
         auto launch_pair = [&](PairKernel pk, int psmem, float* agg, float* lsum) -> cudaError_t {
             cudaError_t le;
             if ((le = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) !=
@@ -1271,8 +1277,8 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
                                            (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
                 return le;
             cfg.dynamicSmemBytes = (size_t)psmem;
-            le = cudaLaunchKernelEx(&cfg, pk, tx, tb, th, Gcs, dtT, (__nv_bfloat16*)hiddens,
-                                    final_state, ring, ctrl, agg, lsum, q);
+            le = cudaLaunchKernelEx(&cfg, pk, tx, tb, th, two_pass ? nullptr : init, Gcs, dtT,
+                                    (__nv_bfloat16*)hiddens, final_state, ring, ctrl, agg, lsum, q);
             return le != cudaSuccess ? le : cudaGetLastError();
         };
         if (!two_pass)

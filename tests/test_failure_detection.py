@@ -18,12 +18,14 @@ from harness import TOL, gpu_fwd, oracle_fwd, rel_err, small, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("init_std", [0.1, 0.0], ids=["per-head", "paired-heads"])
-def test_withheld_handoff_times_out_and_is_reported(init_std):
+@pytest.mark.parametrize("init_std,ngroups", [(0.1, 2), (0.0, 1), (0.1, 1)],
+                         ids=["per-head", "paired-heads", "paired-heads-init"])
+def test_withheld_handoff_times_out_and_is_reported(init_std, ngroups):
     # 2 heads x 16 chunks: far fewer units than CTAs, so every CTA takes one
-    # chunk and each chain crosses 15 range boundaries.  Without an initial
-    # state the two heads walk as one pair-chain.
-    w = small(seqlen=4096, nheads=2, ngroups=1, headdim=64, dstate=128, chunk=256,
+    # chunk and each chain crosses 15 range boundaries.  With both heads in one
+    # group they walk as one pair-chain; one head per group takes the one-head
+    # kernel.
+    w = small(seqlen=4096, nheads=2, ngroups=ngroups, headdim=64, dstate=128, chunk=256,
               dtype="bf16", init_std=init_std, batch=1)
     inp = synth.make_inputs(w)
     dev = to_device(inp, "bf16")

@@ -87,6 +87,7 @@ CASES = [
     ("bf16", 128, 1000, 6, 3, 32, 64, False, True),   # paired heads, ragged tail
     ("bf16", 256, 4096, 4, 1, 64, 128, False, False), # paired, one chunk per CTA
     ("bf16", 64, 700, 6, 2, 64, 128, False, True),    # odd heads per group: unpaired
+    ("bf16", 128, 1000, 3, 3, 64, 128, True, True),   # unpaired, with an initial state
     ("bf16", 64, 300, 4, 2, 64, 48, False, True),     # paired, TMA-stored 48-row states
     # long chains: local pass, scan over each chain's ranges, apply pass
     ("bf16", 128, 15999, 4, 2, 64, 128, True, True),  # with an initial state, ragged
