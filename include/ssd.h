@@ -129,7 +129,10 @@ ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A,
 /* Bytes of device scratch that ssd_fwd_pass_state needs for `d`: for bf16, a
  * two-slot fp32 state buffer per (batch, head, 128-row block of N), through
  * which the units of one head's chunk sequence hand the state on, and a small
- * control block; 0 for fp32, or if `d` is invalid or empty. */
+ * control block; for long chunk sequences (>= 64 chunks, N <= 128, P <= 64,
+ * an even number of heads per group) also 32 MiB of per-range aggregate
+ * states, with which the ranges of a sequence run independently and a short
+ * scan joins them; 0 for fp32, or if `d` is invalid or empty. */
 size_t ssd_fwd_pass_state_scratch_bytes(const ssd_dims* d);
 
 /*
