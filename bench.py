@@ -54,7 +54,16 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--decode", action="store_true",
+                    help="time ssd_step (one token per stream) on the decode configuration "
+                         "instead of the forward pass")
     return ap.parse_args()
+
+
+# Decode configuration for --decode: the Mamba-2-layer head shape with 64 streams,
+# one token per stream and step (state 168 MB: larger than L2).
+DECODE = dict(batch=64, nheads=80, headdim=64, dstate=128, ngroups=1, dtype="bf16")
+DECODE_METRIC = "SSD decode tokens/s on 1 GB300 (ssd_step, one token per stream) and % of HBM roofline"
 
 
 # --- algorithmic byte model (per launch; the method's minimum traffic) -----------
@@ -79,6 +88,20 @@ def byte_model(w: synth.Workload) -> dict:
         "fwd_pass_state": x + bc + 2 * gcs + init + hid + st,    # x, B, Gcs, dtT, init -> hiddens, final
         "compute_out": x + 2 * bc + 2 * gcs + hid + D + x,       # x, B, C, Gcs, dtT, hiddens, D -> y
     }
+
+
+def launches_per_step(w: synth.Workload, sms: int) -> int:
+    """Kernels one ssd_fwd enqueues: three, or five when fwd_pass_state takes
+    its two-pass form for long chains (same rule as the library's launcher)."""
+    hpg = w.nheads // w.ngroups
+    nc = -(-w.seqlen // w.chunk)
+    if (w.dtype == "bf16" and w.dstate <= 128 and w.headdim <= 64 and w.nheads % 2 == 0
+            and hpg % 2 == 0 and nc >= 64):
+        W = w.batch * w.nheads // 2 * nc
+        G = min(W, sms, 256)
+        if -(-W // G) <= nc // 2:
+            return 5
+    return 3
 
 
 def measured_peaks():
@@ -267,8 +290,103 @@ def config_of(w: synth.Workload) -> dict:
 
 # --- GPU arm ---------------------------------------------------------------------
 
+def decode_main(args):
+    """ssd_step timed like the forward pass: W untimed steps, K timed steps with an
+    L2 flush before each, CUDA events on the launching stream.  The state stays in
+    HBM between steps (as in a decode loop); x, dt, B, C of one token per stream
+    are the step's inputs."""
+    import torch
+    import state_space_sequence_chunk_gb300 as ssd
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = synth.Workload("decode_step_bf16", DECODE["batch"], 1, DECODE["nheads"], DECODE["headdim"],
+                       DECODE["dstate"], DECODE["ngroups"], 64, DECODE["dtype"], init_std=0.1,
+                       seed=20261202 + 9)
+    inp = synth.make_inputs(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    up = lambda a, dt=None: None if a is None else (torch.from_numpy(a).to(dev) if dt is None
+                                                    else torch.from_numpy(a).to(dev).to(dt))
+    x, B, C = (up(inp[k], torch.bfloat16) for k in ("x", "B", "C"))
+    dt, A, D = up(inp["dt"]), up(inp["A"]), up(inp["D"])
+    state = up(inp["init_state"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    step = lambda: ssd.ssd_step(x, dt, A, B, C, D, state)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for s0, s1 in evs:
+        flush.fill_(1)
+        s0.record(stream)
+        step()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # end to end: the token's inputs from pinned host memory, y back to the host
+    host = {k: torch.from_numpy(inp[k]).to(torch.bfloat16 if k in ("x", "B", "C") else torch.float32)
+            .pin_memory() for k in ("x", "dt", "B", "C")}
+    y_h = torch.empty(tuple(x.shape), dtype=torch.bfloat16).pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+
+    def e2e():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        y = ssd.ssd_step(dev_in["x"], dev_in["dt"], A, dev_in["B"], dev_in["C"], D, state)
+        y_h.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        e2e()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(20)]
+    for s0, s1 in eev:
+        flush.fill_(1)
+        s0.record(stream)
+        e2e()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    clocks = sampler.stop()
+    b, H, P, N, G = w.batch, w.nheads, w.headdim, w.dstate, w.ngroups
+    algo = 2 * b * H * P * N * 4 + 2 * b * H * P * 2 + b * H * 4 + 2 * b * G * N * 2 + 2 * H * 4
+    peak, peak_kind = measured_peaks()
+    achieved = algo / (ms * 1e-3) / 1e9
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    line = {
+        "metric": DECODE_METRIC, "value": b / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "streams": b, "tokens_per_step": 1, "nheads": H,
+                   "headdim": P, "dstate": N, "ngroups": G, "l2": "flushed before every step"},
+        "roofline": {"bound": "hbm", "kernel": "ssd_step", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes": algo},
+        "e2e": {"value": b / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": y_h.numel() * y_h.element_size()},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                          inp["init_state"], lib=oracle.load())
+        t_cpu = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": b / t_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"the whole step ({b} streams x {H} heads, one token), "
+                                          f"fp64, single thread; {t_cpu:.3f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.decode:
+        return decode_main(args)
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, w)
@@ -437,7 +555,7 @@ def main():
             "method_roofline_frac": sum(model.values()) / (ms_per_step * 1e-3) / 1e9 / peak,
             "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": launches_per_step(w, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
             "clocks": clocks,
         }
         if world == 1 and not args.no_cpu_baseline:

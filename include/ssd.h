@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 2
+#define SSD_ABI_VERSION 3
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
@@ -185,6 +185,27 @@ unsigned int ssd_take_device_errors(void);
  * the flag cannot be written.
  */
 ssd_status ssd_debug_withhold_handoffs(int on);
+
+/*
+ * ssd_step -- the token-by-token recurrence, for decoding and other short
+ * inputs ("The Mamba-2 Recurrence"; the linear-time streaming mode in which
+ * one call's final state is the next call's initial state).  For each
+ * (b, h), starting from S = state[b, h] and for t = 0 .. seqlen-1 in order:
+ *   S <- exp(A[h] dt[b,t,h]) S + dt[b,t,h] x[b,t,h,:] B[b,t,g,:]^T
+ *   y[b,t,h,:] = S C[b,t,g,:] + D[h] x[b,t,h,:]        (g = h / (H/G))
+ * and finally state[b, h] = S.  This is ssd_fwd's result computed without
+ * chunking: one pass over the state (read once, written once), so it suits
+ * a few tokens per call; long inputs belong to ssd_fwd.
+ *   d          shapes and dtype as for ssd_fwd; chunk_size is not used.
+ *   x, dt, A, B, C, D   as for ssd_fwd (D may be NULL).
+ *   state      [b, H, P, N] fp32, read and updated in place (required).
+ *   y          output [b, L, H, P] in the x dtype (required).
+ * Pointers are device pointers, 16-byte aligned; state and y must not
+ * overlap each other or an input (SSD_ERR_ALIAS).  Asynchronous on `stream`.
+ */
+ssd_status ssd_step(const ssd_dims* d, const void* x, const float* dt, const float* A,
+                    const void* B, const void* C, const float* D, float* state, void* y,
+                    void* stream);
 
 /* Size of the fixed device scratch buffer used by ssd_fwd_noalloc: 32 MiB. */
 #define SSD_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)

@@ -33,7 +33,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE"
 EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
            "ssd_fwd_pass_state_scratch_bytes", "ssd_compute_out", "ssd_fwd_noalloc",
-           "ssd_take_device_errors", "ssd_debug_withhold_handoffs"]
+           "ssd_take_device_errors", "ssd_debug_withhold_handoffs", "ssd_step"]
 
 
 class SSDError(RuntimeError):
@@ -90,6 +90,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_take_device_errors.restype = ctypes.c_uint
         lib.ssd_fwd_noalloc.argtypes = [dp] + [vp] * 10
         lib.ssd_fwd_noalloc.restype = ctypes.c_int
+        lib.ssd_step.argtypes = [dp] + [vp] * 9
+        lib.ssd_step.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -220,6 +222,17 @@ def ssd_compute_out(x, B, C, Gcs, dtT, hiddens, D=None, chunk_size: int = 256):
     y = torch.empty_like(x)
     _check(lib.ssd_compute_out(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(C), _ptr(Gcs), _ptr(dtT),
                                _ptr(hiddens), _ptr(D), _ptr(y), _stream()))
+    return y
+
+
+def ssd_step(x, dt, A, B, C, D, state):
+    """Token-by-token recurrence over x's L tokens (decode): updates ``state``
+    [b, H, P, N] fp32 in place and returns y [b, L, H, P] in x.dtype."""
+    lib = load_library()
+    dims = dims_for(x, B, 64)
+    y = torch.empty_like(x)
+    _check(lib.ssd_step(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                        _ptr(state), _ptr(y), _stream()))
     return y
 
 

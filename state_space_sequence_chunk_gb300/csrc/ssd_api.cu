@@ -223,6 +223,33 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
     return from_cuda(launch_compute_out(p, x, B, C, Gcs, dtT, hiddens, D, y, (cudaStream_t)stream));
 }
 
+ssd_status ssd_step(const ssd_dims* d, const void* x, const float* dt, const float* A,
+                    const void* B, const void* C, const float* D, float* state, void* y,
+                    void* stream) {
+    if (!d) return SSD_ERR_NULL;
+    ssd_dims dd = *d;
+    dd.chunk_size = 64;   // not used by the step; any value passes
+    Problem p;
+    ssd_status s = make_problem(&dd, &p);
+    if (s != SSD_OK) return s;
+    if (p.b == 0 || p.L == 0) return SSD_OK;
+    if (!x || !dt || !A || !B || !C || !state || !y) return SSD_ERR_NULL;
+    if (!aligned16(x) || !aligned16(dt) || !aligned16(A) || !aligned16(B) || !aligned16(C) ||
+        !aligned16(D) || !aligned16(state) || !aligned16(y))
+        return SSD_ERR_ALIGN;
+    const size_t es = (size_t)p.esize;
+    const size_t xb = (size_t)(p.b * p.L * p.H * p.P) * es;
+    const size_t bcb = (size_t)(p.b * p.L * p.G * p.N) * es;
+    const Range in[] = {rng(x, xb), rng(dt, (size_t)(p.b * p.L * p.H) * 4), rng(A, (size_t)p.H * 4),
+                        rng(B, bcb), rng(C, bcb), rng(D, (size_t)p.H * 4)};
+    const Range sr = rng(state, (size_t)(p.b * p.H * p.P * p.N) * 4), yr = rng(y, xb);
+    for (const Range& r : in)
+        if (overlap(r, sr) || overlap(r, yr)) return SSD_ERR_ALIAS;
+    if (overlap(sr, yr)) return SSD_ERR_ALIAS;
+    if ((s = check_arch()) != SSD_OK) return s;
+    return from_cuda(launch_ssd_step(p, x, dt, A, B, C, D, state, y, (cudaStream_t)stream));
+}
+
 ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const float* A,
                    const void* B, const void* C, const float* D, const float* init_state, void* y,
                    float* final_state, void* workspace, size_t workspace_bytes, void* stream) {

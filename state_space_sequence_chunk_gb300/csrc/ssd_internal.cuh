@@ -57,6 +57,11 @@ cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, c
                                const float* Gcs, const float* dtT, const void* hiddens,
                                const float* D, void* y, cudaStream_t stream);
 
+// The token-by-token recurrence over p.L tokens from `state` (in place).
+cudaError_t launch_ssd_step(const Problem& p, const void* x, const float* dt, const float* A,
+                            const void* B, const void* C, const float* D, float* state, void* y,
+                            cudaStream_t stream);
+
 // Tensor-core (tcgen05) variants for bf16 inputs.
 cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void* B,
                                      const float* Gcs, const float* dtT, const float* init,

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.ssd_abi_version() == 2
+    assert lib.ssd_abi_version() == 3
     for code in range(0, 9):
         s = lib.ssd_status_string(code)
         assert s and s != b"unknown status"
@@ -147,6 +147,26 @@ def test_per_step_validation(lib):
                None) == 8
     assert lib.ssd_compute_out(ctypes.byref(d), a[0], a[1], a[2], a[3], a[4], a[5], None,
                                ctypes.c_void_p(a[0].value), None) == 8
+
+
+def test_step_validation(lib):
+    # ssd_step(d, x, dt, A, B, C, D, state, y, stream); chunk_size is not used
+    a = _fwd_args()
+    step = lambda d, *args: lib.ssd_step(ctypes.byref(d), *args, None)
+    d = dims(seqlen=2, chunk_size=100)
+    assert step(d, None, a[1], a[2], a[3], a[4], a[5], a[6], a[7]) == 1
+    assert step(d, a[0], a[1], a[2], a[3], a[4], a[5], None, a[7]) == 1   # state required
+    assert step(d, a[0], a[1], a[2], a[3], a[4], a[5], a[6], None) == 1   # y required
+    assert step(d, a[0], a[1], a[2], ctypes.c_void_p(a[3].value + 8), a[4], a[5], a[6],
+                a[7]) == 4
+    assert step(d, a[0], a[1], a[2], a[3], a[4], a[5], a[6],
+                ctypes.c_void_p(a[0].value + 64)) == 8                      # y inside x
+    assert step(d, a[0], a[1], a[2], a[3], a[4], a[5], ctypes.c_void_p(a[4].value + 256),
+                a[7]) == 8                                                  # state inside C
+    assert step(dims(seqlen=2, headdim=40), *a[:8]) == 2
+    assert step(dims(seqlen=0), *a[:8]) == 0                                # nothing to do
+    # D is optional: NULL passes validation and fails only at the device check
+    assert step(d, a[0], a[1], a[2], a[3], a[4], None, a[6], a[7]) in (0, 6, 7)
 
 
 def test_binding_raises_without_library(tmp_path):
