@@ -1104,30 +1104,54 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 // component), blockIdx.y = batch * H + head.  It walks the head's pieces in
 // chunk order (ranges k = the one holding the chain's first unit, k + 1, ...):
 // start = S, S <- 2^{sum} S + A, with the piece's start state written over A.
-// S begins at init_state (or zero) and ends as final_state.
+// S begins at init_state (or zero) and ends as final_state.  The pieces'
+// slots and decays are staged in shared memory, kScanBatch at a time, and
+// each thread loads the batch's A values before its serial fma chain, so that
+// the loads overlap instead of queueing behind one another.
+constexpr int kScanBatch = 32;
 __global__ void __launch_bounds__(256)
 fwd_pass_state_scan(const float* init, float* agg, const float* __restrict__ agg_lsum,
                     float* final_state, const FpsParams q) {
+    __shared__ int s_slot[kScanBatch];
+    __shared__ float s_decay[kScanBatch];
     const int f = blockIdx.x * blockDim.x + threadIdx.x;
-    if (f >= kSlotFloats) return;
     const int bh = blockIdx.y, pc = bh >> 1, hd = bh & 1;
     const int n = (f >> 2) & 127, p = (f >> 9) * 4 + (f & 3);
-    const bool valid = p < q.P && n < q.N;
+    const bool live = f < kSlotFloats;
+    const bool valid = live && p < q.P && n < q.N;
     const int64_t sidx = ((int64_t)bh * q.P + p) * q.N + n;
     float S = (init != nullptr && valid) ? init[sidx] : 0.f;
     const int u0 = pc * q.nc, u1 = u0 + q.nc;   // the pair-chain's units
-    int k = (int)((long long)u0 * q.G / q.W);
-    while (k + 1 < q.G && (int)((long long)(k + 1) * q.W / q.G) <= u0) ++k;
-    while (k > 0 && (int)((long long)k * q.W / q.G) > u0) --k;
-    for (; k < q.G; ++k) {
-        const int lo = (int)((long long)k * q.W / q.G);
-        if (lo >= u1) break;
-        const int64_t aslot = (int64_t)(2 * k + (lo / q.nc == pc ? 0 : 1)) * 2 + hd;
-        float* a = agg + aslot * kSlotFloats + f;
-        const float A = __ldcg(a);
-        const float decay = exp2f(__ldcg(agg_lsum + aslot));
-        __stcg(a, S);
-        S = fmaf(decay, S, A);
+    auto range_lo = [&](int k) { return (int)((long long)k * q.W / q.G); };
+    int k0 = (int)((long long)u0 * q.G / q.W);
+    while (k0 + 1 < q.G && range_lo(k0 + 1) <= u0) ++k0;
+    while (k0 > 0 && range_lo(k0) > u0) --k0;
+    int k1 = k0;                                 // one past the chain's last range
+    while (k1 < q.G && range_lo(k1) < u1) ++k1;
+    for (int kb = k0; kb < k1; kb += kScanBatch) {
+        const int nb = min(kScanBatch, k1 - kb);
+        __syncthreads();   // the previous batch's table has been read
+        if ((int)threadIdx.x < nb) {
+            const int k = kb + (int)threadIdx.x;
+            const int slot = (2 * k + (range_lo(k) / q.nc == pc ? 0 : 1)) * 2 + hd;
+            s_slot[threadIdx.x] = slot;
+            s_decay[threadIdx.x] = exp2f(__ldcg(agg_lsum + slot));
+        }
+        __syncthreads();
+        if (!live) continue;
+        for (int i0 = 0; i0 < nb; i0 += 8) {
+            float Av[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                Av[i] = i0 + i < nb ? __ldcg(agg + (int64_t)s_slot[i0 + i] * kSlotFloats + f) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i0 + i < nb) {
+                    __stcg(agg + (int64_t)s_slot[i0 + i] * kSlotFloats + f, S);
+                    S = fmaf(s_decay[i0 + i], S, Av[i]);
+                }
+            }
+        }
     }
     if (final_state != nullptr && valid) final_state[sidx] = S;
 }
