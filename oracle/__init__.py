@@ -19,6 +19,8 @@ Functions (all fp64, all pinned by ``tests/test_oracle_pins.py``):
   "Kernel 1: chunk_cumsum", base-2 scaled.
 * :func:`chunked` -- the chunked closed form of section "Step 3: Add Back the
   Decay, Safely, in Log-Space"; used only to pin :func:`recurrence`.
+* :func:`causal_conv1d` -- the depthwise causal convolution of the Helion
+  hackathon gallery's "Causal Conv1d" entries (the Mamba-2 block's neighbour).
 """
 from __future__ import annotations
 
@@ -57,6 +59,8 @@ def _declare(lib):
     lib.ssd_oracle_chunk_cumsum.restype = ctypes.c_int
     lib.ssd_oracle_chunked.argtypes = [i64] * 7 + [dp] * 9
     lib.ssd_oracle_chunked.restype = ctypes.c_int
+    lib.ssd_oracle_causal_conv1d.argtypes = [i64] * 4 + [dp] * 4
+    lib.ssd_oracle_causal_conv1d.restype = ctypes.c_int
     return lib
 
 
@@ -136,3 +140,18 @@ def chunked(x, dt, A, B, C, D=None, init_state=None, chunk: int = 64, lib=None):
     if rc != 0:
         raise ValueError(f"ssd_oracle_chunked failed with code {rc}")
     return y, fin
+
+
+def causal_conv1d(x, weight, bias=None, lib=None):
+    """Depthwise causal conv1d (fp64): x [b, d, L], weight [d, W], bias [d] or None;
+    returns out [b, d, L] (Helion hackathon gallery, "Causal Conv1d")."""
+    lib = lib or load()
+    x, weight, bias = _f64(x), _f64(weight), _f64(bias)
+    b, d, L = x.shape
+    W = weight.shape[1]
+    assert weight.shape == (d, W) and (bias is None or bias.shape == (d,))
+    out = np.zeros((b, d, L), np.float64)
+    rc = lib.ssd_oracle_causal_conv1d(b, d, L, W, _ptr(x), _ptr(weight), _ptr(bias), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"ssd_oracle_causal_conv1d failed with code {rc}")
+    return out

@@ -1,5 +1,6 @@
 /*
- * ssd_oracle.c -- the CPU oracle for the Mamba-2 SSD forward pass.
+ * ssd_oracle.c -- the CPU oracle for the Mamba-2 SSD forward pass (and the
+ * causal depthwise conv1d that precedes it in a Mamba-2 block).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
  * this file: only the tests, the smoke check and the CPU-baseline leg of the
@@ -19,6 +20,8 @@
  *   [P2] The zhiding.cn Chinese rendering of the NVIDIA / Jane Street cuTile
  *        Mamba-2 article, section "Mamba-2架构" (the recurrence and the chunked
  *        closed forms, given there as LaTeX).
+ *   [P3] The Helion hackathon gallery (cerebralvalley.ai), its "Causal Conv1d
+ *        (causal_conv1d)" entries (the convolution's definition).
  *
  * Layouts (row-major, contiguous; b = batch, t = token, h = head, g = group):
  *   x    [batch, seqlen, nheads, headdim]      dt   [batch, seqlen, nheads]
@@ -233,5 +236,39 @@ int ssd_oracle_chunked(int64_t batch, int64_t seqlen, int64_t nheads, int64_t he
         }
     }
     free(S); free(Snew); free(g);
+    return ORACLE_OK;
+}
+
+/*
+ * ssd_oracle_causal_conv1d -- depthwise causal 1-D convolution, the Mamba /
+ * Mamba-2 block's neighbour of the SSD (parity pinned: tests/oracle_pins.py).
+ *
+ * [P3] Helion hackathon gallery, the "Causal Conv1d (causal_conv1d)" entry:
+ * each channel is convolved independently with a short filter of W taps,
+ * with causal (left) zero padding:
+ *   out[b, d, t] = bias[d] + sum_{k=0}^{W-1} weight[d, k] * x[b, d, t - W + 1 + k],
+ * where x at a negative time index reads as 0.
+ * Layouts: x, out [batch, dim, seqlen]; weight [dim, width]; bias [dim] or
+ * NULL (treated as 0).  Returns 0 on success.
+ */
+int ssd_oracle_causal_conv1d(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                             const double* x, const double* weight, const double* bias,
+                             double* out) {
+    if (batch < 0 || dim < 1 || seqlen < 0 || width < 1 || !x || !weight || !out)
+        return ORACLE_BAD_ARGS;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const double* xr = x + (b * dim + d) * seqlen;
+            double* orow = out + (b * dim + d) * seqlen;
+            for (int64_t t = 0; t < seqlen; ++t) {
+                double acc = bias ? bias[d] : 0.0;
+                for (int64_t k = 0; k < width; ++k) {
+                    const int64_t ts = t - width + 1 + k;
+                    if (ts >= 0) acc += weight[d * width + k] * xr[ts];
+                }
+                orow[t] = acc;
+            }
+        }
+    }
     return ORACLE_OK;
 }

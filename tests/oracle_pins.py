@@ -200,6 +200,48 @@ def pin_chunk_cumsum(lib):
     assert np.all(np.diff(G.reshape(b, H, L), axis=2)[:, :, np.arange(L - 1) % Q != Q - 1] < 0)
 
 
+# --- causal conv1d (Helion hackathon gallery, "Causal Conv1d (causal_conv1d)":
+# out[b, d, t] = bias[d] + sum_k weight[d, k] x[b, d, t - W + 1 + k], left zero padding)
+
+def pin_conv1d_hand_example(lib):
+    """x = [1, 2, 3, 4], taps [1, 0, -1], bias 0.25, worked by hand:
+    out[t] = x[t-2] - x[t]  ->  [-1, -2, -2, -2] + 0.25."""
+    out = oracle.causal_conv1d(np.array([[[1.0, 2.0, 3.0, 4.0]]]), np.array([[1.0, 0.0, -1.0]]),
+                               np.array([0.25]), lib=lib)
+    np.testing.assert_allclose(out[0, 0], [-0.75, -1.75, -1.75, -1.75], rtol=0, atol=1e-15)
+
+
+def pin_conv1d_library(lib):
+    """Each row is numpy's full convolution with the reversed taps, cut to the
+    first L samples (the causal part), plus the bias."""
+    rng = np.random.default_rng(11)
+    b, d, L, W = 2, 5, 23, 4
+    x = rng.standard_normal((b, d, L))
+    w = rng.standard_normal((d, W))
+    bias = rng.standard_normal(d)
+    out = oracle.causal_conv1d(x, w, bias, lib=lib)
+    for i in range(b):
+        for c in range(d):
+            ref = np.convolve(x[i, c], w[c, ::-1])[:L] + bias[c]
+            np.testing.assert_allclose(out[i, c], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_conv1d_impulse_and_causality(lib):
+    """A unit impulse at t0 returns the taps in reverse from t0 on (nothing
+    before t0: no output reads the future), and width 1 is a per-channel scale."""
+    W, L, t0 = 4, 12, 5
+    w = np.array([[0.5, -1.0, 2.0, 3.0]])
+    x = np.zeros((1, 1, L)); x[0, 0, t0] = 1.0
+    out = oracle.causal_conv1d(x, w, None, lib=lib)[0, 0]
+    expect = np.zeros(L); expect[t0:t0 + W] = w[0, ::-1]
+    np.testing.assert_array_equal(out, expect)
+    rng = np.random.default_rng(12)
+    x2 = rng.standard_normal((2, 3, 9)); w1 = rng.standard_normal((3, 1)); b1 = rng.standard_normal(3)
+    out1 = oracle.causal_conv1d(x2, w1, b1, lib=lib)
+    np.testing.assert_allclose(out1, x2 * w1[None, :, :] + b1[None, :, None], rtol=1e-15, atol=1e-15)
+
+
 ALL_PINS = [pin_hand_example, pin_chunked_closed_form, pin_linear_attention, pin_dt_zero,
             pin_geometric, pin_D_isolation, pin_split_composition, pin_linearity,
-            pin_checkpoints, pin_chunk_cumsum]
+            pin_checkpoints, pin_chunk_cumsum, pin_conv1d_hand_example, pin_conv1d_library,
+            pin_conv1d_impulse_and_causality]

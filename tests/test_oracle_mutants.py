@@ -32,6 +32,12 @@ MUTANTS = [
      "                run += A[h] * dt[(b * seqlen + t) * nheads + h];"),
     ("cumsum_natural_log", "= log2e * run;", "= run;"),
     ("cumsum_no_chunk_reset", "if (t % chunk == 0) run = 0.0;", "if (t == 0) run = 0.0;"),
+    ("conv_shifted_window", "const int64_t ts = t - width + 1 + k;", "const int64_t ts = t - width + k;"),
+    ("conv_reads_future", "const int64_t ts = t - width + 1 + k;", "const int64_t ts = t + k;"),
+    ("conv_taps_reversed", "acc += weight[d * width + k] * xr[ts];",
+     "acc += weight[d * width + (width - 1 - k)] * xr[ts];"),
+    ("conv_dropped_bias", "double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
+    ("conv_padding_drops_first", "if (ts >= 0) acc", "if (ts > 0) acc"),
 ]
 
 
