@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="time ssd_step (one token per stream) on the decode configuration "
                          "instead of the forward pass")
+    ap.add_argument("--conv1d", action="store_true",
+                    help="time the depthwise causal conv1d on the Mamba-2 block's xBC shape "
+                         "instead of the forward pass")
     return ap.parse_args()
 
 
@@ -290,6 +293,101 @@ def config_of(w: synth.Workload) -> dict:
 
 # --- GPU arm ---------------------------------------------------------------------
 
+# conv1d configuration for --conv1d: the Mamba-2 layer's xBC channels
+# (H*P + 2*G*N = 5120 + 256), batch 4, 4096 tokens, width 4, bf16 (x 176 MB).
+CONV = dict(batch=4, dim=80 * 64 + 2 * 128, seqlen=4096, width=4)
+CONV_METRIC = "causal conv1d tokens/s on 1 GB300 (Mamba-2 xBC channels) and % of HBM roofline"
+
+
+def conv1d_main(args):
+    """ssd_causal_conv1d timed like the forward pass (W untimed runs, K timed runs,
+    L2 flushed before each, CUDA events)."""
+    import torch
+    import state_space_sequence_chunk_gb300 as ssd
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    b, d, L, W = CONV["batch"], CONV["dim"], CONV["seqlen"], CONV["width"]
+    rng = np.random.default_rng(20261202 + 11)
+    x_np = rng.standard_normal((b, d, L)).astype(np.float32)
+    w_np = (rng.standard_normal((d, W)) / 2).astype(np.float32)
+    b_np = rng.standard_normal(d).astype(np.float32)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = torch.from_numpy(x_np).to(dev).to(torch.bfloat16)
+    w = torch.from_numpy(w_np).to(dev)
+    bias = torch.from_numpy(b_np).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    run = lambda: ssd.causal_conv1d(x, w, bias)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for s0, s1 in evs:
+        flush.fill_(1)
+        s0.record(stream)
+        run()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b2) for a, b2 in evs)
+    x_h = x.cpu().pin_memory()
+    out_h = torch.empty_like(x_h).pin_memory()
+    x_d = torch.empty_like(x)
+
+    def e2e():
+        x_d.copy_(x_h, non_blocking=True)
+        out_h.copy_(ssd.causal_conv1d(x_d, w, bias), non_blocking=True)
+
+    for _ in range(3):
+        e2e()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(20)]
+    for s0, s1 in eev:
+        flush.fill_(1)
+        s0.record(stream)
+        e2e()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in eev)
+    clocks = sampler.stop()
+    algo = 2 * b * d * L * 2 + d * W * 4 + d * 4
+    peak, peak_kind = measured_peaks()
+    achieved = algo / (ms * 1e-3) / 1e9
+    line = {
+        "metric": CONV_METRIC, "value": b * L / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "causal_conv1d_xbc_bf16", "batch": b, "dim": d, "seqlen": L,
+                   "width": W, "l2": "flushed before every step"},
+        "roofline": {"bound": "hbm", "kernel": "causal_conv1d", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes": algo},
+        "e2e": {"value": b * L / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.numel() * 2, "d2h_bytes_per_step": out_h.numel() * 2},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        nrows = 0
+        t_cpu = 0.0
+        xb = x.float().cpu().numpy()
+        while t_cpu < min(args.cpu_seconds, 5.0) and nrows < d:
+            t0 = time.perf_counter()
+            oracle.causal_conv1d(xb[:1, nrows:nrows + 64], w_np[nrows:nrows + 64], b_np[nrows:nrows + 64])
+            t_cpu += time.perf_counter() - t0
+            nrows += 64
+        full = t_cpu / min(nrows, d) * d * b
+        line["cpu_baseline"] = {"value": b * L / full, "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{min(nrows, d)} of {b * d} channel rows, fp64, single "
+                                          f"thread; {t_cpu:.2f} s measured, projected {full:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def decode_main(args):
     """ssd_step timed like the forward pass: W untimed steps, K timed steps with an
     L2 flush before each, CUDA events on the launching stream.  The state stays in
@@ -387,6 +485,8 @@ def main():
     args = parse()
     if args.decode:
         return decode_main(args)
+    if args.conv1d:
+        return conv1d_main(args)
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, w)

@@ -207,6 +207,31 @@ ssd_status ssd_step(const ssd_dims* d, const void* x, const float* dt, const flo
                     const void* B, const void* C, const float* D, float* state, void* y,
                     void* stream);
 
+/* Sizes of a depthwise causal conv1d: x and out are [batch, dim, seqlen] in
+ * `dtype`; the filter has `width` taps per channel. */
+typedef struct {
+    int64_t batch, dim, seqlen, width;
+    int32_t dtype;      /* ssd_dtype of x and out */
+    int32_t reserved;   /* must be 0 */
+} ssd_conv_dims;
+
+/*
+ * ssd_causal_conv1d -- the depthwise causal 1-D convolution that precedes the
+ * SSD in a Mamba-2 block (Helion hackathon gallery, "Causal Conv1d"):
+ *   out[b, d, t] = bias[d] + sum_{k=0}^{W-1} weight[d, k] x[b, d, t - W + 1 + k]
+ * with x read as 0 at negative t (causal left padding, done in the kernel).
+ *   d        batch >= 0, 1 <= dim <= 65535, seqlen >= 0, 1 <= width <= 8,
+ *            batch <= 65535; else SSD_ERR_SHAPE (SSD_ERR_DTYPE for dtype).
+ *   x        [batch, dim, seqlen] in d->dtype (required).
+ *   weight   [dim, width] fp32 (required); bias [dim] fp32 or NULL (0).
+ *   out      [batch, dim, seqlen] in d->dtype (required); it must not
+ *            overlap x, weight or bias (SSD_ERR_ALIAS).
+ * Device pointers, 16-byte aligned (SSD_ERR_ALIGN).  fp32 arithmetic.
+ * Asynchronous on `stream`.
+ */
+ssd_status ssd_causal_conv1d(const ssd_conv_dims* d, const void* x, const float* weight,
+                             const float* bias, void* out, void* stream);
+
 /* Size of the fixed device scratch buffer used by ssd_fwd_noalloc: 32 MiB. */
 #define SSD_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
 

@@ -33,7 +33,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE"
 EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
            "ssd_fwd_pass_state_scratch_bytes", "ssd_compute_out", "ssd_fwd_noalloc",
-           "ssd_take_device_errors", "ssd_debug_withhold_handoffs", "ssd_step"]
+           "ssd_take_device_errors", "ssd_debug_withhold_handoffs", "ssd_step",
+           "ssd_causal_conv1d"]
 
 
 class SSDError(RuntimeError):
@@ -42,6 +43,11 @@ class SSDError(RuntimeError):
     def __init__(self, code: int, message: str):
         super().__init__(f"{STATUS.get(code, code)}: {message}")
         self.code = code
+
+
+class ConvDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("width", ctypes.c_int64), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Dims(ctypes.Structure):
@@ -92,6 +98,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_fwd_noalloc.restype = ctypes.c_int
         lib.ssd_step.argtypes = [dp] + [vp] * 9
         lib.ssd_step.restype = ctypes.c_int
+        lib.ssd_causal_conv1d.argtypes = [ctypes.POINTER(ConvDims)] + [vp] * 5
+        lib.ssd_causal_conv1d.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -223,6 +231,23 @@ def ssd_compute_out(x, B, C, Gcs, dtT, hiddens, D=None, chunk_size: int = 256):
     _check(lib.ssd_compute_out(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(C), _ptr(Gcs), _ptr(dtT),
                                _ptr(hiddens), _ptr(D), _ptr(y), _stream()))
     return y
+
+
+def causal_conv1d(x, weight, bias=None):
+    """Depthwise causal conv1d: x [b, dim, L] (bf16 or fp32), weight [dim, W] fp32,
+    bias [dim] fp32 or None; returns out [b, dim, L] in x.dtype."""
+    lib = load_library()
+    if x.dim() != 3 or weight.dim() != 2:
+        raise ValueError("x must be [b, dim, L] and weight [dim, W]")
+    code = SSD_BF16 if x.dtype == torch.bfloat16 else SSD_F32
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    b, dim, L = x.shape
+    d = ConvDims(b, dim, L, weight.shape[1], code, 0)
+    out = torch.empty_like(x)
+    _check(lib.ssd_causal_conv1d(ctypes.byref(d), _ptr(x), _ptr(weight), _ptr(bias), _ptr(out),
+                                 _stream()))
+    return out
 
 
 def ssd_step(x, dt, A, B, C, D, state):

@@ -223,6 +223,32 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
     return from_cuda(launch_compute_out(p, x, B, C, Gcs, dtT, hiddens, D, y, (cudaStream_t)stream));
 }
 
+ssd_status ssd_causal_conv1d(const ssd_conv_dims* d, const void* x, const float* weight,
+                             const float* bias, void* out, void* stream) {
+    if (!d) return SSD_ERR_NULL;
+    if (d->dtype != SSD_F32 && d->dtype != SSD_BF16) return SSD_ERR_DTYPE;
+    if (d->reserved != 0 || d->batch < 0 || d->batch > 65535 || d->dim < 1 || d->dim > 65535 ||
+        d->seqlen < 0 || d->seqlen > (1LL << 30) || d->width < 1 || d->width > 8)
+        return SSD_ERR_SHAPE;
+    if (d->batch * d->dim > (1LL << 31) / (d->seqlen > 0 ? d->seqlen : 1)) return SSD_ERR_SHAPE;
+    ConvProblem p;
+    p.b = d->batch; p.dim = d->dim; p.L = d->seqlen; p.W = d->width;
+    p.dtype = d->dtype;
+    p.esize = d->dtype == SSD_BF16 ? 2 : 4;
+    if (p.b == 0 || p.L == 0) return SSD_OK;
+    if (!x || !weight || !out) return SSD_ERR_NULL;
+    if (!aligned16(x) || !aligned16(weight) || !aligned16(bias) || !aligned16(out))
+        return SSD_ERR_ALIGN;
+    const size_t xb = (size_t)(p.b * p.dim * p.L) * p.esize;
+    const Range orr = rng(out, xb);
+    if (overlap(orr, rng(x, xb)) || overlap(orr, rng(weight, (size_t)(p.dim * p.W) * 4)) ||
+        overlap(orr, rng(bias, (size_t)p.dim * 4)))
+        return SSD_ERR_ALIAS;
+    ssd_status s = check_arch();
+    if (s != SSD_OK) return s;
+    return from_cuda(launch_causal_conv1d(p, x, weight, bias, out, (cudaStream_t)stream));
+}
+
 ssd_status ssd_step(const ssd_dims* d, const void* x, const float* dt, const float* A,
                     const void* B, const void* C, const float* D, float* state, void* y,
                     void* stream) {

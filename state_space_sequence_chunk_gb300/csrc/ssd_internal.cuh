@@ -57,6 +57,15 @@ cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, c
                                const float* Gcs, const float* dtT, const void* hiddens,
                                const float* D, void* y, cudaStream_t stream);
 
+// Depthwise causal conv1d sizes after validation (ssd_causal_conv1d).
+struct ConvProblem {
+    int64_t b, dim, L, W;
+    int dtype;   // ssd_dtype of x and out
+    int esize;
+};
+cudaError_t launch_causal_conv1d(const ConvProblem& p, const void* x, const float* weight,
+                                 const float* bias, void* out, cudaStream_t stream);
+
 // The token-by-token recurrence over p.L tokens from `state` (in place).
 cudaError_t launch_ssd_step(const Problem& p, const void* x, const float* dt, const float* A,
                             const void* B, const void* C, const float* D, float* state, void* y,

@@ -169,6 +169,26 @@ def test_step_validation(lib):
     assert step(d, a[0], a[1], a[2], a[3], a[4], None, a[6], a[7]) in (0, 6, 7)
 
 
+def test_conv1d_validation(lib):
+    a = _fwd_args(4)
+    conv = lambda d, *args: lib.ssd_causal_conv1d(ctypes.byref(d), *args, None)
+    cd = lambda **kw: ssd.ConvDims(*[dict(batch=2, dim=8, seqlen=64, width=4, dtype=ssd.SSD_BF16,
+                                            reserved=0, **{})[k] if k not in kw else kw[k]
+                                       for k, _ in ssd.ConvDims._fields_])
+    assert conv(cd(width=0), *a) == 2
+    assert conv(cd(width=9), *a) == 2
+    assert conv(cd(dim=0), *a) == 2
+    assert conv(cd(dtype=7), *a) == 3
+    assert conv(cd(reserved=1), *a) == 2
+    assert conv(cd(), None, a[1], a[2], a[3]) == 1
+    assert conv(cd(), a[0], None, a[2], a[3]) == 1
+    assert conv(cd(), a[0], a[1], a[2], ctypes.c_void_p(a[3].value + 4)) == 4
+    assert conv(cd(), a[0], a[1], a[2], ctypes.c_void_p(a[0].value + 256)) == 8   # out inside x
+    assert conv(cd(seqlen=0), *a) == 0
+    # bias is optional: NULL passes validation and fails only at the device check
+    assert conv(cd(), a[0], a[1], None, a[3]) in (0, 6, 7)
+
+
 def test_binding_raises_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="CUDA library not found"):
         saved = ssd._lib
