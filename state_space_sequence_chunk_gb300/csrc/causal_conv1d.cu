@@ -9,11 +9,11 @@
 // bound by memory bandwidth; the padding is done in the kernel (no padded
 // copy of x), as several of the gallery's entries recommend.
 //
-// GB300 design: plain CUDA-core code shaped for coalescing.  A thread owns 16
-// consecutive bytes of one row (8 bf16 or 4 fp32 outputs), loads them with one
-// vector load, takes the W - 1 samples before them from the neighbouring lane
+// GB300 design: plain CUDA-core code shaped for coalescing.  A thread owns two
+// 16-byte vectors of one row (8 bf16 or 4 fp32 outputs each), loads both with
+// vector loads, takes the W - 1 samples before each from the neighbouring lane
 // by shuffles (lane 0 reads its own from global memory; they are in L1), and
-// writes one vector store.  Rows whose length is not a multiple of the vector
+// writes vector stores.  Rows whose length is not a multiple of the vector
 // width take a one-output-per-thread kernel.  fp32 arithmetic; x and out are
 // bf16 or fp32, weight and bias fp32.
 #include "ssd_internal.cuh"
@@ -56,7 +56,11 @@ template <> struct Vec<float> {
     }
 };
 
-// Vector path: L % Vec<T>::kN == 0.  grid (ceil(L / (threads * V)), dim, batch).
+// Vector path: L % Vec<T>::kN == 0.  A CTA covers kSpan = kVecPerThread *
+// threads * V consecutive samples of one row; thread i owns vectors i and
+// i + threads, so both loads are in flight together and every warp access
+// stays 512 contiguous bytes.  grid (ceil(L / kSpan), dim, batch).
+constexpr int kVecPerThread = 2;
 template <typename T, int W>
 __global__ void __launch_bounds__(kConvThreads)
 conv1d_vec_kernel(const T* __restrict__ x, const float* __restrict__ weight,
@@ -65,41 +69,48 @@ conv1d_vec_kernel(const T* __restrict__ x, const float* __restrict__ weight,
     static_assert(W >= 1 && W - 1 <= V, "the halo must come from one neighbouring lane");
     const int d = blockIdx.y, b = blockIdx.z, lane = threadIdx.x & 31;
     const int64_t row = ((int64_t)b * dim + d) * L;
-    const int t0 = (blockIdx.x * kConvThreads + threadIdx.x) * V;
     float wk[W];
 #pragma unroll
     for (int k = 0; k < W; ++k) wk[k] = __ldg(weight + (int64_t)d * W + k);
     const float bs = bias != nullptr ? __ldg(bias + d) : 0.f;
-    const bool live = t0 < L;
-    float v[V];
-    if (live) Vec<T>::load(x + row + t0, v);
-    else
+    float v[kVecPerThread][V];
+    int t0[kVecPerThread];
 #pragma unroll
-        for (int i = 0; i < V; ++i) v[i] = 0.f;
-    // xx = the W - 1 samples before t0, then this thread's V samples
-    float xx[W - 1 + V];
+    for (int r = 0; r < kVecPerThread; ++r) {
+        t0[r] = ((blockIdx.x * kVecPerThread + r) * kConvThreads + threadIdx.x) * V;
+        if (t0[r] < L) Vec<T>::load(x + row + t0[r], v[r]);
+        else
 #pragma unroll
-    for (int i = 0; i < V; ++i) xx[W - 1 + i] = v[i];
+            for (int i = 0; i < V; ++i) v[r][i] = 0.f;
+    }
 #pragma unroll
-    for (int k = 0; k < W - 1; ++k) {
-        const float from_left = __shfl_up_sync(0xffffffffu, v[V - (W - 1) + k], 1);
-        float h = from_left;
-        if (lane == 0) {
-            const int ts = t0 - (W - 1) + k;
-            h = (live && ts >= 0) ? to_f32(x[row + ts]) : 0.f;
+    for (int r = 0; r < kVecPerThread; ++r) {
+        const bool live = t0[r] < L;
+        // xx = the W - 1 samples before t0, then this vector's V samples
+        float xx[W - 1 + V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) xx[W - 1 + i] = v[r][i];
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) {
+            float h = __shfl_up_sync(0xffffffffu, v[r][V - (W - 1) + k], 1);
+            if (lane == 0) {
+                const int ts = t0[r] - (W - 1) + k;
+                h = (live && ts >= 0) ? to_f32(x[row + ts]) : 0.f;
+            }
+            xx[k] = h;
         }
-        xx[k] = h;
-    }
-    if (!live) return;
-    float o[V];
+        if (live) {
+            float o[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-        float acc = bs;
+            for (int i = 0; i < V; ++i) {
+                float acc = bs;
 #pragma unroll
-        for (int k = 0; k < W; ++k) acc = fmaf(wk[k], xx[i + k], acc);
-        o[i] = acc;
+                for (int k = 0; k < W; ++k) acc = fmaf(wk[k], xx[i + k], acc);
+                o[i] = acc;
+            }
+            Vec<T>::store(out + row + t0[r], o);
+        }
     }
-    Vec<T>::store(out + row + t0, o);
 }
 
 // Any L: one output per thread.  grid (ceil(L / threads), dim, batch).
@@ -128,8 +139,8 @@ cudaError_t launch_t(const ConvProblem& p, const void* x, const float* weight, c
     const int dim = (int)p.dim, L = (int)p.L;
     // the vector path takes its W - 1 earlier samples from the left lane alone
     if (L % V == 0 && p.W - 1 <= V) {
-        const dim3 grid((unsigned)((L / V + kConvThreads - 1) / kConvThreads), (unsigned)dim,
-                        (unsigned)p.b);
+        const int span = kVecPerThread * kConvThreads * V;
+        const dim3 grid((unsigned)((L + span - 1) / span), (unsigned)dim, (unsigned)p.b);
         switch (p.W) {
             case 1: conv1d_vec_kernel<T, 1><<<grid, kConvThreads, 0, stream>>>(xt, weight, bias, ot, dim, L); break;
             case 2: conv1d_vec_kernel<T, 2><<<grid, kConvThreads, 0, stream>>>(xt, weight, bias, ot, dim, L); break;
