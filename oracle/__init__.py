@@ -21,6 +21,8 @@ Functions (all fp64, all pinned by ``tests/test_oracle_pins.py``):
   Decay, Safely, in Log-Space"; used only to pin :func:`recurrence`.
 * :func:`causal_conv1d` -- the depthwise causal convolution of the Helion
   hackathon gallery's "Causal Conv1d" entries (the Mamba-2 block's neighbour).
+* :func:`gdn_fwd_h`, :func:`gdn_fwd_o` -- the Gated DeltaNet chunk kernels of
+  the same gallery's "GDN chunk_fwd_h" / "GDN chunk_fwd_o" entries, step by step.
 """
 from __future__ import annotations
 
@@ -61,6 +63,10 @@ def _declare(lib):
     lib.ssd_oracle_chunked.restype = ctypes.c_int
     lib.ssd_oracle_causal_conv1d.argtypes = [i64] * 4 + [dp] * 4
     lib.ssd_oracle_causal_conv1d.restype = ctypes.c_int
+    lib.ssd_oracle_gdn_fwd_h.argtypes = [i64] * 6 + [dp] * 8
+    lib.ssd_oracle_gdn_fwd_h.restype = ctypes.c_int
+    lib.ssd_oracle_gdn_fwd_o.argtypes = [i64] * 6 + [dp] * 6
+    lib.ssd_oracle_gdn_fwd_o.restype = ctypes.c_int
     return lib
 
 
@@ -155,3 +161,34 @@ def causal_conv1d(x, weight, bias=None, lib=None):
     if rc != 0:
         raise ValueError(f"ssd_oracle_causal_conv1d failed with code {rc}")
     return out
+
+
+def gdn_fwd_h(k, w, u, g, h0=None, chunk: int = 64, lib=None):
+    """Gated DeltaNet chunk_fwd_h (fp64): k, w [B, T, H, K], u [B, T, H, V], g [B, T, H]
+    (in-chunk inclusive cumulative log gate), h0 [B, H, K, V] or None.  Returns
+    ``(h [B, H, NT, K, V], v_new [B, T, H, V], final_state [B, H, K, V])``."""
+    lib = lib or load()
+    k, w, u, g, h0 = map(_f64, (k, w, u, g, h0))
+    B, T, H, K = k.shape
+    V = u.shape[3]
+    NT = -(-T // chunk)
+    h = np.zeros((B, H, NT, K, V)); v_new = np.zeros((B, T, H, V)); fin = np.zeros((B, H, K, V))
+    rc = lib.ssd_oracle_gdn_fwd_h(B, T, H, K, V, chunk, _ptr(k), _ptr(w), _ptr(u), _ptr(g), _ptr(h0),
+                                  _ptr(h), _ptr(v_new), _ptr(fin))
+    if rc != 0:
+        raise ValueError(f"ssd_oracle_gdn_fwd_h failed with code {rc}")
+    return h, v_new, fin
+
+
+def gdn_fwd_o(q, k, v_new, h, g, chunk: int = 64, lib=None):
+    """Gated DeltaNet chunk_fwd_o (fp64): returns o [B, T, H, V]."""
+    lib = lib or load()
+    q, k, v_new, h, g = map(_f64, (q, k, v_new, h, g))
+    B, T, H, K = q.shape
+    V = v_new.shape[3]
+    o = np.zeros((B, T, H, V))
+    rc = lib.ssd_oracle_gdn_fwd_o(B, T, H, K, V, chunk, _ptr(q), _ptr(k), _ptr(v_new), _ptr(h), _ptr(g),
+                                  _ptr(o))
+    if rc != 0:
+        raise ValueError(f"ssd_oracle_gdn_fwd_o failed with code {rc}")
+    return o

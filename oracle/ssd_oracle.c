@@ -272,3 +272,113 @@ int ssd_oracle_causal_conv1d(int64_t batch, int64_t dim, int64_t seqlen, int64_t
     }
     return ORACLE_OK;
 }
+
+/*
+ * Gated DeltaNet chunk kernels -- the survey's NEXT-3 workload, a second
+ * chunked recurrence with the shape of fwd_pass_state / compute_out.
+ *
+ * [P3] Helion hackathon gallery, the "GDN chunk_fwd_h" and "GDN chunk_fwd_o"
+ * entries, chunk size C.  Layouts: k, w, q [B, T, H, K]; u, v_new, o
+ * [B, T, H, V]; g [B, T, H] = the in-chunk inclusive cumulative log gate
+ * (natural log, <= 0); h [B, H, NT, K, V] the state at each chunk start;
+ * h0, final_state [B, H, K, V] (h0 may be NULL: zero state).  g_last is g at
+ * the chunk's last valid token (a ragged last chunk ends at T).
+ *
+ * ssd_oracle_gdn_fwd_h, per chunk in order, the page's five steps:
+ *   (1) store h; (2) v_new = u - w @ h; (3) gate: v_gated[t] = v_new[t] *
+ *   exp(g_last - g_t); (4) decay: h *= exp(g_last); (5) h += k^T @ v_gated.
+ * Returns 0 on success.
+ */
+int ssd_oracle_gdn_fwd_h(int64_t batch, int64_t seqlen, int64_t nheads, int64_t kdim, int64_t vdim,
+                         int64_t chunk, const double* k, const double* w, const double* u,
+                         const double* g, const double* h0, double* h, double* v_new,
+                         double* final_state) {
+    if (batch < 0 || seqlen < 0 || nheads < 1 || kdim < 1 || vdim < 1 || chunk < 1) return ORACLE_BAD_ARGS;
+    if (!k || !w || !u || !g || !h || !v_new) return ORACLE_BAD_ARGS;
+    const int64_t H = nheads, K = kdim, V = vdim, T = seqlen, NT = (T + chunk - 1) / chunk;
+    double* S = (double*)malloc((size_t)(K * V) * sizeof(double));
+    double* vg = (double*)malloc((size_t)(chunk * V) * sizeof(double));
+    if (!S || !vg) { free(S); free(vg); return ORACLE_NO_MEMORY; }
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t hh = 0; hh < H; ++hh) {
+            if (h0) memcpy(S, h0 + (b * H + hh) * K * V, (size_t)(K * V) * sizeof(double));
+            else memset(S, 0, (size_t)(K * V) * sizeof(double));
+            for (int64_t c = 0; c < NT; ++c) {
+                const int64_t t0 = c * chunk, t1 = (t0 + chunk < T) ? t0 + chunk : T;
+                /* (1) store the chunk-start state */
+                memcpy(h + ((b * H + hh) * NT + c) * K * V, S, (size_t)(K * V) * sizeof(double));
+                const double g_last = g[(b * T + t1 - 1) * H + hh];
+                for (int64_t t = t0; t < t1; ++t) {
+                    const double* wt = w + ((b * T + t) * H + hh) * K;
+                    const double* ut = u + ((b * T + t) * H + hh) * V;
+                    double* vt = v_new + ((b * T + t) * H + hh) * V;
+                    const double gate = exp(g_last - g[(b * T + t) * H + hh]);
+                    for (int64_t v = 0; v < V; ++v) {
+                        /* (2) v_new = u - w @ h */
+                        double acc = 0.0;
+                        for (int64_t kk = 0; kk < K; ++kk) acc += wt[kk] * S[kk * V + v];
+                        vt[v] = ut[v] - acc;
+                        /* (3) gate */
+                        vg[(t - t0) * V + v] = vt[v] * gate;
+                    }
+                }
+                /* (4) decay, then (5) h += k^T @ v_gated */
+                const double decay = exp(g_last);
+                for (int64_t kk = 0; kk < K; ++kk)
+                    for (int64_t v = 0; v < V; ++v) {
+                        double acc = S[kk * V + v] * decay;
+                        for (int64_t t = t0; t < t1; ++t)
+                            acc += k[((b * T + t) * H + hh) * K + kk] * vg[(t - t0) * V + v];
+                        S[kk * V + v] = acc;
+                    }
+            }
+            if (final_state)
+                memcpy(final_state + (b * H + hh) * K * V, S, (size_t)(K * V) * sizeof(double));
+        }
+    }
+    free(S);
+    free(vg);
+    return ORACLE_OK;
+}
+
+/*
+ * ssd_oracle_gdn_fwd_o, per chunk, the page's three products:
+ *   inter[t] = (q_t @ h) * exp(g_t);
+ *   intra[i] = sum_{j <= i} (q_i . k_j) exp(g_i - g_j) v_new[j]   (the causal mask keeps j = i);
+ *   o = inter + intra.
+ * h is the chunk-start state from ssd_oracle_gdn_fwd_h.  Returns 0 on success.
+ */
+int ssd_oracle_gdn_fwd_o(int64_t batch, int64_t seqlen, int64_t nheads, int64_t kdim, int64_t vdim,
+                         int64_t chunk, const double* q, const double* k, const double* v_new,
+                         const double* h, const double* g, double* o) {
+    if (batch < 0 || seqlen < 0 || nheads < 1 || kdim < 1 || vdim < 1 || chunk < 1) return ORACLE_BAD_ARGS;
+    if (!q || !k || !v_new || !h || !g || !o) return ORACLE_BAD_ARGS;
+    const int64_t H = nheads, K = kdim, V = vdim, T = seqlen, NT = (T + chunk - 1) / chunk;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t hh = 0; hh < H; ++hh) {
+            for (int64_t c = 0; c < NT; ++c) {
+                const int64_t t0 = c * chunk, t1 = (t0 + chunk < T) ? t0 + chunk : T;
+                const double* S = h + ((b * H + hh) * NT + c) * K * V;
+                for (int64_t i = t0; i < t1; ++i) {
+                    const double* qi = q + ((b * T + i) * H + hh) * K;
+                    const double gi = g[(b * T + i) * H + hh];
+                    double* oi = o + ((b * T + i) * H + hh) * V;
+                    for (int64_t v = 0; v < V; ++v) {
+                        double inter = 0.0;
+                        for (int64_t kk = 0; kk < K; ++kk) inter += qi[kk] * S[kk * V + v];
+                        oi[v] = inter * exp(gi);
+                    }
+                    for (int64_t j = t0; j <= i; ++j) {
+                        const double* kj = k + ((b * T + j) * H + hh) * K;
+                        double qk = 0.0;
+                        for (int64_t kk = 0; kk < K; ++kk) qk += qi[kk] * kj[kk];
+                        const double a = qk * exp(gi - g[(b * T + j) * H + hh]);
+                        const double* vj = v_new + ((b * T + j) * H + hh) * V;
+                        for (int64_t v = 0; v < V; ++v) oi[v] += a * vj[v];
+                    }
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}

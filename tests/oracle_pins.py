@@ -241,7 +241,91 @@ def pin_conv1d_impulse_and_causality(lib):
     np.testing.assert_allclose(out1, x2 * w1[None, :, :] + b1[None, :, None], rtol=1e-15, atol=1e-15)
 
 
+# --- Gated DeltaNet chunk kernels (Helion hackathon gallery, "GDN chunk_fwd_h" and
+# "GDN chunk_fwd_o": per chunk store h, v_new = u - w h, gate exp(g_last - g_t),
+# h *= exp(g_last), h += k^T v_gated; o = (q h) exp(g) + causal((q k^T) exp(g_i - g_j)) v_new)
+
+def _gdn_problem(seed, B=2, T=11, H=2, K=3, V=4, chunk=4, w_zero=False, k_zero=False):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, T, H, K))
+    k = np.zeros((B, T, H, K)) if k_zero else rng.standard_normal((B, T, H, K)) / 2
+    w = np.zeros((B, T, H, K)) if w_zero else rng.standard_normal((B, T, H, K)) / 4
+    u = rng.standard_normal((B, T, H, V))
+    gamma = -np.abs(rng.normal(0.2, 0.1, (B, T, H)))        # per-token log gates (<= 0)
+    g = np.zeros_like(gamma)                                 # in-chunk inclusive cumsum
+    for t in range(T):
+        g[:, t] = gamma[:, t] + (g[:, t - 1] if t % chunk else 0.0)
+    h0 = rng.standard_normal((B, H, K, V))
+    return q, k, w, u, gamma, g, h0
+
+
+def pin_gdn_linear_attention(lib):
+    """With w = 0 there is no delta correction (v_new = u) and the two kernels are
+    gated linear attention: token by token, S_t = exp(gamma_t) S_{t-1} + k_t u_t^T
+    and o_t = q_t^T S_t, whatever the chunk size (brute force on a tiny problem)."""
+    for chunk in (1, 3, 4, 16):
+        q, k, w, u, gamma, g, h0 = _gdn_problem(21, chunk=chunk, w_zero=True)
+        h, v_new, fin = oracle.gdn_fwd_h(k, w, u, g, h0, chunk=chunk, lib=lib)
+        o = oracle.gdn_fwd_o(q, k, v_new, h, g, chunk=chunk, lib=lib)
+        np.testing.assert_array_equal(v_new, u)
+        B, T, H, K = q.shape
+        for b in range(B):
+            for hh in range(H):
+                S = h0[b, hh].copy()
+                for t in range(T):
+                    S = math.exp(gamma[b, t, hh]) * S + np.outer(k[b, t, hh], u[b, t, hh])
+                    np.testing.assert_allclose(o[b, t, hh], q[b, t, hh] @ S, rtol=1e-12, atol=1e-12)
+                np.testing.assert_allclose(fin[b, hh], S, rtol=1e-12, atol=1e-12)
+
+
+def pin_gdn_hand_example(lib):
+    """K = V = 1, one chunk of two tokens, worked by hand: h0 = 2, k = (1, 1),
+    w = (0.5, 0.25), u = (3, 1), g = (-0.1, -0.3), q = (1, 2):
+    v_new = (2, 0.5); final = 2e^-0.3 + 2e^-0.2 + 0.5;
+    o = (2e^-0.1 + 2, 4e^-0.3 + 4e^-0.2 + 1)."""
+    sh = lambda a: np.array(a, float).reshape(1, 2, 1, 1)
+    k, w, u, q = sh([1, 1]), sh([0.5, 0.25]), sh([3, 1]), sh([1, 2])
+    g = np.array([-0.1, -0.3]).reshape(1, 2, 1)
+    h0 = np.array(2.0).reshape(1, 1, 1, 1)
+    h, v_new, fin = oracle.gdn_fwd_h(k, w, u, g, h0, chunk=2, lib=lib)
+    o = oracle.gdn_fwd_o(q, k, v_new, h, g, chunk=2, lib=lib)
+    e = math.exp
+    np.testing.assert_allclose(h.ravel(), [2.0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(v_new.ravel(), [2.0, 0.5], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(fin.ravel(), [2 * e(-0.3) + 2 * e(-0.2) + 0.5], rtol=1e-15)
+    np.testing.assert_allclose(o.ravel(), [2 * e(-0.1) + 2, 4 * e(-0.3) + 4 * e(-0.2) + 1],
+                               rtol=1e-15)
+
+
+def pin_gdn_k_zero_and_linearity(lib):
+    """With k = 0 the state only decays: h_c = h0 exp(sum of the earlier chunks'
+    g_last) and v_new = u - w h_c.  For fixed k, w, g the map (u, h0) -> (h, v_new,
+    final) is linear."""
+    chunk = 4
+    q, k, w, u, gamma, g, h0 = _gdn_problem(22, chunk=chunk, k_zero=True)
+    h, v_new, fin = oracle.gdn_fwd_h(k, w, u, g, h0, chunk=chunk, lib=lib)
+    B, T, H, K = k.shape
+    for c in range(h.shape[2]):
+        past = np.zeros((B, H))
+        for cc in range(c):
+            past = past + g[:, min(cc * chunk + chunk, T) - 1]
+        hc = h0 * np.exp(past)[:, :, None, None]
+        np.testing.assert_allclose(h[:, :, c], hc, rtol=1e-12, atol=1e-12)
+        for t in range(c * chunk, min(c * chunk + chunk, T)):
+            np.testing.assert_allclose(v_new[:, t], u[:, t] - np.einsum("bhk,bhkv->bhv", w[:, t], hc),
+                                       rtol=1e-12, atol=1e-12)
+    p1 = _gdn_problem(23, chunk=chunk); p2 = _gdn_problem(24, chunk=chunk)
+    _, k, w, u1, _, g, h01 = p1
+    u2, h02 = p2[3], p2[6]
+    r1 = oracle.gdn_fwd_h(k, w, u1, g, h01, chunk=chunk, lib=lib)
+    r2 = oracle.gdn_fwd_h(k, w, u2, g, h02, chunk=chunk, lib=lib)
+    r3 = oracle.gdn_fwd_h(k, w, 2 * u1 - u2, g, 2 * h01 - h02, chunk=chunk, lib=lib)
+    for a1, a2, a3 in zip(r1, r2, r3):
+        np.testing.assert_allclose(a3, 2 * a1 - a2, rtol=1e-10, atol=1e-10)
+
+
 ALL_PINS = [pin_hand_example, pin_chunked_closed_form, pin_linear_attention, pin_dt_zero,
             pin_geometric, pin_D_isolation, pin_split_composition, pin_linearity,
             pin_checkpoints, pin_chunk_cumsum, pin_conv1d_hand_example, pin_conv1d_library,
-            pin_conv1d_impulse_and_causality]
+            pin_conv1d_impulse_and_causality, pin_gdn_linear_attention, pin_gdn_hand_example,
+            pin_gdn_k_zero_and_linearity]

@@ -38,6 +38,14 @@ MUTANTS = [
      "acc += weight[d * width + (width - 1 - k)] * xr[ts];"),
     ("conv_dropped_bias", "double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
     ("conv_padding_drops_first", "if (ts >= 0) acc", "if (ts > 0) acc"),
+    ("gdn_delta_sign", "vt[v] = ut[v] - acc;", "vt[v] = ut[v] + acc;"),
+    ("gdn_gate_inverted", "const double gate = exp(g_last - g[(b * T + t) * H + hh]);",
+     "const double gate = exp(g[(b * T + t) * H + hh] - g_last);"),
+    ("gdn_no_state_decay", "double acc = S[kk * V + v] * decay;", "double acc = S[kk * V + v];"),
+    ("gdn_g_last_first_token", "const double g_last = g[(b * T + t1 - 1) * H + hh];",
+     "const double g_last = g[(b * T + t0) * H + hh];"),
+    ("gdn_o_mask_drops_diagonal", "for (int64_t j = t0; j <= i; ++j) {", "for (int64_t j = t0; j < i; ++j) {"),
+    ("gdn_o_inter_undecayed", "oi[v] = inter * exp(gi);", "oi[v] = inter;"),
 ]
 
 
