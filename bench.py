@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="time ssd_step (one token per stream) on the decode configuration "
                          "instead of the forward pass")
+    ap.add_argument("--gdn", action="store_true",
+                    help="time the Gated DeltaNet chunk kernels (chunk_fwd_h + chunk_fwd_o) "
+                         "instead of the forward pass")
     ap.add_argument("--conv1d", action="store_true",
                     help="time the depthwise causal conv1d on the Mamba-2 block's xBC shape "
                          "instead of the forward pass")
@@ -388,6 +391,112 @@ def conv1d_main(args):
     return 0
 
 
+# Gated DeltaNet configuration for --gdn: 4 sequences of 4096 tokens, 16 heads,
+# K = V = 128, chunk 64, fp32 (the gallery's kernels use C = 64 and K/V 64-128).
+GDN = dict(B=4, T=4096, H=16, K=128, V=128, chunk=64)
+GDN_METRIC = "Gated DeltaNet chunk_fwd_h + chunk_fwd_o tokens/s on 1 GB300 and % of fp32 CUDA-core peak"
+# fp32 FMA peak: 152 SMs x 128 lanes x 2 flop x the 2070 MHz maximum SM clock
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def gdn_main(args):
+    import torch
+    import state_space_sequence_chunk_gb300 as ssd
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    B, T, H, K, V, C = (GDN[k] for k in ("B", "T", "H", "K", "V", "chunk"))
+    rng = np.random.default_rng(20261202 + 13)
+    f32 = lambda a: a.astype(np.float32)
+    q = f32(rng.standard_normal((B, T, H, K)) / np.sqrt(K))
+    k = f32(rng.standard_normal((B, T, H, K)) / np.sqrt(K))
+    w = f32(rng.standard_normal((B, T, H, K)) / np.sqrt(K) * 0.5)
+    u = f32(rng.standard_normal((B, T, H, V)))
+    gamma = -np.abs(rng.normal(0.05, 0.03, (B, T, H)))
+    g = np.zeros_like(gamma)
+    for t in range(T):
+        g[:, t] = gamma[:, t] + (g[:, t - 1] if t % C else 0.0)
+    g = f32(g)
+    h0 = f32(rng.standard_normal((B, H, K, V)) * 0.1)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    tq, tk, tw, tu, tg, th0 = map(dev, (q, k, w, u, g, h0))
+
+    def step():
+        h, v_new, fin = ssd.gdn_chunk_fwd_h(tk, tw, tu, tg, th0, chunk=C)
+        return ssd.gdn_chunk_fwd_o(tq, tk, v_new, h, tg, chunk=C)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for s0, s1 in evs:
+        flush.fill_(1)
+        s0.record(stream)
+        step()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b2) for a, b2 in evs)
+    host = {n: torch.from_numpy(a).pin_memory() for n, a in (("q", q), ("k", k), ("w", w), ("u", u), ("g", g))}
+    dev_in = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
+    o_h = torch.empty((B, T, H, V), dtype=torch.float32).pin_memory()
+
+    def e2e():
+        for n, t in host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        h, v_new, _ = ssd.gdn_chunk_fwd_h(dev_in["k"], dev_in["w"], dev_in["u"], dev_in["g"], th0, chunk=C)
+        o_h.copy_(ssd.gdn_chunk_fwd_o(dev_in["q"], dev_in["k"], v_new, h, dev_in["g"], chunk=C),
+                  non_blocking=True)
+
+    for _ in range(2):
+        e2e()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    for s0, s1 in eev:
+        flush.fill_(1)
+        s0.record(stream)
+        e2e()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in eev)
+    clocks = sampler.stop()
+    NT = -(-T // C)
+    macs = B * H * NT * (2 * C * K * V + C * K * V + C * (C + 1) // 2 * (K + V))
+    achieved = 2 * macs / (ms * 1e-3) / 1e12
+    line = {
+        "metric": GDN_METRIC, "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "gdn_chunk_f32", "B": B, "T": T, "H": H, "K": K, "V": V, "chunk": C,
+                   "l2": "flushed before every step"},
+        "roofline": {"bound": "alu", "kernel": "gdn_fwd_h + gdn_fwd_o", "achieved": achieved,
+                     "peak": FP32_PEAK_TFLOPS, "peak_kind": "derived (fp32 FMA lanes x max clock)",
+                     "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+                     "algorithmic_flops": 2 * macs},
+        "e2e": {"value": B * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": sum(t.numel() * 4 for t in host.values()),
+                "d2h_bytes_per_step": o_h.numel() * 4},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        Ts = 256   # a bounded sample: one head of one sequence, 256 tokens
+        t0 = time.perf_counter()
+        hs, vns, _ = oracle.gdn_fwd_h(k[:1, :Ts, :1], w[:1, :Ts, :1], u[:1, :Ts, :1], g[:1, :Ts, :1],
+                                      h0[:1, :1], chunk=C)
+        oracle.gdn_fwd_o(q[:1, :Ts, :1], k[:1, :Ts, :1], vns, hs, g[:1, :Ts, :1], chunk=C)
+        t_cpu = time.perf_counter() - t0
+        full = t_cpu * (B * H) * (T / Ts)
+        line["cpu_baseline"] = {"value": B * T / full, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"1 of {B * H} (sequence, head) pairs, {Ts} of {T} tokens, "
+                                          f"fp64, single thread; {t_cpu:.2f} s, projected {full:.0f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def decode_main(args):
     """ssd_step timed like the forward pass: W untimed steps, K timed steps with an
     L2 flush before each, CUDA events on the launching stream.  The state stays in
@@ -487,6 +596,8 @@ def main():
         return decode_main(args)
     if args.conv1d:
         return conv1d_main(args)
+    if args.gdn:
+        return gdn_main(args)
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, w)

@@ -232,6 +232,46 @@ typedef struct {
 ssd_status ssd_causal_conv1d(const ssd_conv_dims* d, const void* x, const float* weight,
                              const float* bias, void* out, void* stream);
 
+/* Sizes of the Gated DeltaNet chunk kernels: q, k, w [batch, seqlen, nheads,
+ * kdim]; u, v_new, o [batch, seqlen, nheads, vdim]; g [batch, seqlen, nheads];
+ * h [batch, nheads, nchunks, kdim, vdim] with nchunks = ceil(seqlen / chunk);
+ * h0, final_state [batch, nheads, kdim, vdim].  All fp32. */
+typedef struct {
+    int64_t batch, seqlen, nheads, kdim, vdim, chunk;
+    int32_t dtype;      /* SSD_F32 only */
+    int32_t reserved;   /* must be 0 */
+} ssd_gdn_dims;
+
+/*
+ * ssd_gdn_chunk_fwd_h -- Gated DeltaNet state recurrence over chunks (Helion
+ * hackathon gallery, "GDN chunk_fwd_h").  g is the in-chunk inclusive
+ * cumulative log gate and g_last its value at the chunk's last token; per
+ * (b, head), for each chunk in order:
+ *   h[b, head, c] = S;  v_new = u - w S;  v_gated[t] = v_new[t] exp(g_last - g_t);
+ *   S <- exp(g_last) S + k^T v_gated.
+ * S starts at h0 (or 0 if NULL); final_state (may be NULL) receives the last S.
+ *   d        4 <= kdim <= 128 with kdim % 4 == 0; 1 <= vdim <= 128;
+ *            chunk in {16, 32, 64}; nheads >= 1;
+ *            batch >= 0; seqlen >= 0 (else SSD_ERR_SHAPE; SSD_ERR_DTYPE unless fp32).
+ *   k, w, u, g   inputs (required).   h, v_new   outputs (required).
+ * Device pointers, 16-byte aligned; outputs must not overlap inputs or each
+ * other (SSD_ERR_ALIAS).  Asynchronous on `stream`.
+ */
+ssd_status ssd_gdn_chunk_fwd_h(const ssd_gdn_dims* d, const float* k, const float* w,
+                               const float* u, const float* g, const float* h0, float* h,
+                               float* v_new, float* final_state, void* stream);
+
+/*
+ * ssd_gdn_chunk_fwd_o -- Gated DeltaNet chunk outputs ("GDN chunk_fwd_o"),
+ * every chunk independent:
+ *   o[t] = exp(g_t) q_t h[b, head, c] + sum_{j <= t in the chunk} (q_t . k_j) exp(g_t - g_j) v_new[j].
+ * Inputs q, k, v_new, h (from ssd_gdn_chunk_fwd_h), g; output o.  Same rules
+ * as ssd_gdn_chunk_fwd_h.
+ */
+ssd_status ssd_gdn_chunk_fwd_o(const ssd_gdn_dims* d, const float* q, const float* k,
+                               const float* v_new, const float* h, const float* g, float* o,
+                               void* stream);
+
 /* Size of the fixed device scratch buffer used by ssd_fwd_noalloc: 32 MiB. */
 #define SSD_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
 

@@ -34,7 +34,7 @@ EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
            "ssd_fwd_pass_state_scratch_bytes", "ssd_compute_out", "ssd_fwd_noalloc",
            "ssd_take_device_errors", "ssd_debug_withhold_handoffs", "ssd_step",
-           "ssd_causal_conv1d"]
+           "ssd_causal_conv1d", "ssd_gdn_chunk_fwd_h", "ssd_gdn_chunk_fwd_o"]
 
 
 class SSDError(RuntimeError):
@@ -48,6 +48,12 @@ class SSDError(RuntimeError):
 class ConvDims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
                 ("width", ctypes.c_int64), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("kdim", ctypes.c_int64), ("vdim", ctypes.c_int64), ("chunk", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Dims(ctypes.Structure):
@@ -100,6 +106,10 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_step.restype = ctypes.c_int
         lib.ssd_causal_conv1d.argtypes = [ctypes.POINTER(ConvDims)] + [vp] * 5
         lib.ssd_causal_conv1d.restype = ctypes.c_int
+        lib.ssd_gdn_chunk_fwd_h.argtypes = [ctypes.POINTER(GdnDims)] + [vp] * 9
+        lib.ssd_gdn_chunk_fwd_h.restype = ctypes.c_int
+        lib.ssd_gdn_chunk_fwd_o.argtypes = [ctypes.POINTER(GdnDims)] + [vp] * 7
+        lib.ssd_gdn_chunk_fwd_o.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -231,6 +241,42 @@ def ssd_compute_out(x, B, C, Gcs, dtT, hiddens, D=None, chunk_size: int = 256):
     _check(lib.ssd_compute_out(ctypes.byref(dims), _ptr(x), _ptr(B), _ptr(C), _ptr(Gcs), _ptr(dtT),
                                _ptr(hiddens), _ptr(D), _ptr(y), _stream()))
     return y
+
+
+def _gdn_dims(k, vdim, chunk, *tensors):
+    if k.dim() != 4:
+        raise ValueError("k must be a [B, T, H, K] tensor")
+    for t in (k,) + tensors:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"the Gated DeltaNet kernels take float32 tensors, got {t.dtype}")
+    B, T, H, K = k.shape
+    return GdnDims(B, T, H, K, vdim, int(chunk), SSD_F32, 0)
+
+
+def gdn_chunk_fwd_h(k, w, u, g, h0=None, chunk: int = 64, return_final_state: bool = True):
+    """Gated DeltaNet state recurrence over chunks: returns ``(h [B, H, NT, K, V],
+    v_new [B, T, H, V], final_state [B, H, K, V] or None)``; all fp32."""
+    lib = load_library()
+    d = _gdn_dims(k, u.shape[3], chunk, w, u, g, h0)
+    B, T, H, K = k.shape
+    V = u.shape[3]
+    NT = -(-T // chunk)
+    h = torch.empty((B, H, NT, K, V), dtype=torch.float32, device=k.device)
+    v_new = torch.empty_like(u)
+    fin = torch.empty((B, H, K, V), dtype=torch.float32, device=k.device) if return_final_state else None
+    _check(lib.ssd_gdn_chunk_fwd_h(ctypes.byref(d), _ptr(k), _ptr(w), _ptr(u), _ptr(g), _ptr(h0),
+                                   _ptr(h), _ptr(v_new), _ptr(fin), _stream()))
+    return h, v_new, fin
+
+
+def gdn_chunk_fwd_o(q, k, v_new, h, g, chunk: int = 64):
+    """Gated DeltaNet chunk outputs: returns o [B, T, H, V] (fp32)."""
+    lib = load_library()
+    d = _gdn_dims(k, v_new.shape[3], chunk, q, v_new, h, g)
+    o = torch.empty_like(v_new)
+    _check(lib.ssd_gdn_chunk_fwd_o(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v_new), _ptr(h), _ptr(g),
+                                   _ptr(o), _stream()))
+    return o
 
 
 def causal_conv1d(x, weight, bias=None):

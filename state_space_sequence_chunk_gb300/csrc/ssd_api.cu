@@ -249,6 +249,70 @@ ssd_status ssd_causal_conv1d(const ssd_conv_dims* d, const void* x, const float*
     return from_cuda(launch_causal_conv1d(p, x, weight, bias, out, (cudaStream_t)stream));
 }
 
+static ssd_status make_gdn(const ssd_gdn_dims* d, GdnProblem* p) {
+    if (!d) return SSD_ERR_NULL;
+    if (d->dtype != SSD_F32) return SSD_ERR_DTYPE;
+    if (d->reserved != 0 || d->batch < 0 || d->seqlen < 0 || d->nheads < 1 || d->kdim < 4 ||
+        d->kdim > 128 || d->kdim % 4 != 0 || d->vdim < 1 || d->vdim > 128 ||
+        (d->chunk != 16 && d->chunk != 32 && d->chunk != 64))
+        return SSD_ERR_SHAPE;
+    p->B = d->batch; p->T = d->seqlen; p->H = d->nheads; p->K = d->kdim; p->V = d->vdim;
+    p->C = d->chunk;
+    p->NT = (p->T + p->C - 1) / p->C;
+    if (p->NT > 65535 || p->B * p->H > (1LL << 30) || p->B * p->T * p->H * 128 > (1LL << 40))
+        return SSD_ERR_SHAPE;
+    return SSD_OK;
+}
+
+ssd_status ssd_gdn_chunk_fwd_h(const ssd_gdn_dims* d, const float* k, const float* w,
+                               const float* u, const float* g, const float* h0, float* h,
+                               float* v_new, float* final_state, void* stream) {
+    GdnProblem p;
+    ssd_status s = make_gdn(d, &p);
+    if (s != SSD_OK) return s;
+    if (p.B == 0) return SSD_OK;
+    // with no tokens the inputs are not read: only the state passes through
+    if (p.T > 0 && (!k || !w || !u || !g || !h || !v_new)) return SSD_ERR_NULL;
+    if (!aligned16(k) || !aligned16(w) || !aligned16(u) || !aligned16(g) || !aligned16(h0) ||
+        !aligned16(h) || !aligned16(v_new) || !aligned16(final_state))
+        return SSD_ERR_ALIGN;
+    const size_t kb = (size_t)(p.B * p.T * p.H * p.K) * 4, vb = (size_t)(p.B * p.T * p.H * p.V) * 4;
+    const size_t sb = (size_t)(p.B * p.H * p.K * p.V) * 4;
+    const Range in[] = {rng(k, kb), rng(w, kb), rng(u, vb), rng(g, (size_t)(p.B * p.T * p.H) * 4),
+                        rng(h0, sb)};
+    const Range out[] = {rng(h, sb * (size_t)p.NT), rng(v_new, vb), rng(final_state, sb)};
+    for (const Range& o : out) {
+        for (const Range& r : in)
+            if (overlap(o, r)) return SSD_ERR_ALIAS;
+    }
+    if (overlap(out[0], out[1]) || overlap(out[0], out[2]) || overlap(out[1], out[2]))
+        return SSD_ERR_ALIAS;
+    if ((s = check_arch()) != SSD_OK) return s;
+    return from_cuda(launch_gdn_fwd_h(p, k, w, u, g, h0, h, v_new, final_state,
+                                      (cudaStream_t)stream));
+}
+
+ssd_status ssd_gdn_chunk_fwd_o(const ssd_gdn_dims* d, const float* q, const float* k,
+                               const float* v_new, const float* h, const float* g, float* o,
+                               void* stream) {
+    GdnProblem p;
+    ssd_status s = make_gdn(d, &p);
+    if (s != SSD_OK) return s;
+    if (p.B == 0 || p.T == 0) return SSD_OK;
+    if (!q || !k || !v_new || !h || !g || !o) return SSD_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v_new) || !aligned16(h) || !aligned16(g) ||
+        !aligned16(o))
+        return SSD_ERR_ALIGN;
+    const size_t kb = (size_t)(p.B * p.T * p.H * p.K) * 4, vb = (size_t)(p.B * p.T * p.H * p.V) * 4;
+    const size_t hb = (size_t)(p.B * p.H * p.NT * p.K * p.V) * 4;
+    const Range in[] = {rng(q, kb), rng(k, kb), rng(v_new, vb), rng(h, hb),
+                        rng(g, (size_t)(p.B * p.T * p.H) * 4)};
+    for (const Range& r : in)
+        if (overlap(rng(o, vb), r)) return SSD_ERR_ALIAS;
+    if ((s = check_arch()) != SSD_OK) return s;
+    return from_cuda(launch_gdn_fwd_o(p, q, k, v_new, h, g, o, (cudaStream_t)stream));
+}
+
 ssd_status ssd_step(const ssd_dims* d, const void* x, const float* dt, const float* A,
                     const void* B, const void* C, const float* D, float* state, void* y,
                     void* stream) {

@@ -66,6 +66,17 @@ struct ConvProblem {
 cudaError_t launch_causal_conv1d(const ConvProblem& p, const void* x, const float* weight,
                                  const float* bias, void* out, cudaStream_t stream);
 
+// Gated DeltaNet chunk kernels (ssd_gdn_chunk_fwd_h / _o), sizes after validation.
+struct GdnProblem {
+    int64_t B, T, H, K, V, C, NT;
+};
+cudaError_t launch_gdn_fwd_h(const GdnProblem& p, const float* k, const float* w, const float* u,
+                             const float* g, const float* h0, float* h, float* v_new,
+                             float* final_state, cudaStream_t stream);
+cudaError_t launch_gdn_fwd_o(const GdnProblem& p, const float* q, const float* k,
+                             const float* v_new, const float* h, const float* g, float* o,
+                             cudaStream_t stream);
+
 // The token-by-token recurrence over p.L tokens from `state` (in place).
 cudaError_t launch_ssd_step(const Problem& p, const void* x, const float* dt, const float* A,
                             const void* B, const void* C, const float* D, float* state, void* y,

@@ -189,6 +189,24 @@ def test_conv1d_validation(lib):
     assert conv(cd(), a[0], a[1], None, a[3]) in (0, 6, 7)
 
 
+def test_gdn_validation(lib):
+    a = _fwd_args(9)
+    gd = lambda **kw: ssd.GdnDims(*[dict(batch=1, seqlen=128, nheads=2, kdim=64, vdim=64, chunk=64,
+                                          dtype=ssd.SSD_F32, reserved=0)[k] if k not in kw else kw[k]
+                                     for k, _ in ssd.GdnDims._fields_])
+    fh = lambda d, *args: lib.ssd_gdn_chunk_fwd_h(ctypes.byref(d), *args, None)
+    fo = lambda d, *args: lib.ssd_gdn_chunk_fwd_o(ctypes.byref(d), *args, None)
+    assert fh(gd(dtype=ssd.SSD_BF16), *a[:8]) == 3
+    assert fh(gd(chunk=48), *a[:8]) == 2
+    assert fh(gd(kdim=129), *a[:8]) == 2
+    assert fh(gd(), None, *a[1:8]) == 1
+    assert fh(gd(), *a[:5], ctypes.c_void_p(a[0].value + 64), *a[6:8]) == 8   # h inside k
+    assert fh(gd(), *a[:2], ctypes.c_void_p(a[2].value + 4), *a[3:8]) == 4
+    assert fo(gd(), *a[:5], ctypes.c_void_p(a[2].value)) == 8                  # o over v_new
+    assert fo(gd(), None, *a[1:6]) == 1
+    assert fo(gd(batch=0), *a[:6]) == 0
+
+
 def test_binding_raises_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="CUDA library not found"):
         saved = ssd._lib

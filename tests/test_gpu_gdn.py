@@ -1,0 +1,64 @@
+"""Gated DeltaNet chunk kernels (Helion hackathon gallery, "GDN chunk_fwd_h" /
+"GDN chunk_fwd_o") against the step-by-step fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import state_space_sequence_chunk_gb300 as ssd
+from harness import TOL, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def gdn_inputs(B, T, H, K, V, chunk, seed, with_h0=True):
+    """Seeded inputs with the pages' conventions: per-token log gates <= 0 summed
+    within each chunk (inclusive), keys and WY rows scaled so the state stays O(1)."""
+    rng = np.random.default_rng(seed)
+    q = (rng.standard_normal((B, T, H, K)) / np.sqrt(K)).astype(np.float32)
+    k = (rng.standard_normal((B, T, H, K)) / np.sqrt(K)).astype(np.float32)
+    w = (rng.standard_normal((B, T, H, K)) / np.sqrt(K) * 0.5).astype(np.float32)
+    u = rng.standard_normal((B, T, H, V)).astype(np.float32)
+    gamma = -np.abs(rng.normal(0.05, 0.03, (B, T, H)))
+    g = np.zeros_like(gamma)
+    for t in range(T):
+        g[:, t] = gamma[:, t] + (g[:, t - 1] if t % chunk else 0.0)
+    g = g.astype(np.float32)
+    h0 = rng.standard_normal((B, H, K, V)).astype(np.float32) * 0.1 if with_h0 else None
+    return q, k, w, u, g, h0
+
+
+@pytest.mark.parametrize("B,T,H,K,V,chunk,with_h0", [
+    (2, 300, 3, 128, 128, 64, True),    # ragged last chunk, full K and V tiles
+    (1, 256, 2, 64, 32, 32, False),     # no initial state
+    (2, 100, 2, 16, 48, 16, True),      # V not a multiple of the 32-column tile
+    (1, 7, 1, 32, 64, 64, True),        # shorter than one chunk
+])
+def test_gdn_matches_oracle(B, T, H, K, V, chunk, with_h0):
+    q, k, w, u, g, h0 = gdn_inputs(B, T, H, K, V, chunk, seed=T + K)
+    dev = lambda a: None if a is None else torch.from_numpy(a).cuda()
+    h, v_new, fin = ssd.gdn_chunk_fwd_h(dev(k), dev(w), dev(u), dev(g), dev(h0), chunk=chunk)
+    o = ssd.gdn_chunk_fwd_o(dev(q), dev(k), v_new, h, dev(g), chunk=chunk)
+    torch.cuda.synchronize()
+    h_ref, vn_ref, fin_ref = oracle.gdn_fwd_h(k, w, u, g, h0, chunk=chunk)
+    o_ref = oracle.gdn_fwd_o(q, k, vn_ref, h_ref, g, chunk=chunk)
+    assert rel_err(h.cpu().numpy(), h_ref) < TOL["f32"]
+    assert rel_err(v_new.cpu().numpy(), vn_ref) < TOL["f32"]
+    assert rel_err(fin.cpu().numpy(), fin_ref) < TOL["f32"]
+    assert rel_err(o.cpu().numpy(), o_ref) < TOL["f32"]
+
+
+def test_gdn_binding_rejects_other_dtypes():
+    q, k, w, u, g, h0 = gdn_inputs(1, 64, 1, 16, 16, 64, seed=4)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    with pytest.raises(TypeError):
+        ssd.gdn_chunk_fwd_h(dev(k), dev(w).double(), dev(u), dev(g), dev(h0), chunk=64)
+
+
+def test_gdn_empty_sequence_passes_the_state():
+    q, k, w, u, g, h0 = gdn_inputs(1, 0, 2, 32, 32, 64, seed=3)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    h, v_new, fin = ssd.gdn_chunk_fwd_h(dev(k), dev(w), dev(u), dev(g), dev(h0), chunk=64)
+    torch.cuda.synchronize()
+    assert h.numel() == 0 and v_new.numel() == 0
+    assert torch.equal(fin.cpu(), torch.from_numpy(h0))
