@@ -96,6 +96,25 @@ def byte_model(w: synth.Workload) -> dict:
     }
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's figure (the job's time is set by its last rank); a
+    no-op on one rank.  The ranks are independent replicas, so this reduction of
+    the timings is the only collective in the benchmark."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own replica of the workload
+    (weak scaling), so the job does world x tokens per step in the slowest rank's time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def launches_per_step(w: synth.Workload, sms: int) -> int:
     """Kernels one ssd_fwd enqueues: three, or five when fwd_pass_state takes
     its two-pass form for long chains (same rule as the library's launcher)."""
@@ -663,13 +682,9 @@ def main():
         s1.record(stream)
     sync_all()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.tokens / (ms_per_step * 1e-3)
+    value = job_throughput(world, w.tokens, ms_per_step)
 
     # per-kernel breakdown through the three step entry points (same launches)
     gb, hb = ssd.ssd_intermediate_bytes(dims)
@@ -737,11 +752,7 @@ def main():
         e2e_step()
         s1.record(stream)
     sync_all()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in eev), world, dev)
     clocks = sampler.stop()
 
     if rank == 0:
@@ -764,7 +775,7 @@ def main():
                          "traffic": traffic, "algorithmic_bytes": model[dom]},
             "kernels_ms": kms,
             "method_roofline_frac": sum(model.values()) / (ms_per_step * 1e-3) / 1e9 / peak,
-            "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": job_throughput(world, w.tokens, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step(w, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
             "clocks": clocks,
