@@ -480,6 +480,20 @@ def gdn_main(args):
         s1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in eev)
+    # per-kernel breakdown (same launches, L2 flushed before each)
+    h1, vn1, _ = ssd.gdn_chunk_fwd_h(tk, tw, tu, tg, th0, chunk=C)
+    per = {"gdn_fwd_h": [], "gdn_fwd_o": []}
+    for _ in range(5):
+        for name, fn in (("gdn_fwd_h", lambda: ssd.gdn_chunk_fwd_h(tk, tw, tu, tg, th0, chunk=C)),
+                         ("gdn_fwd_o", lambda: ssd.gdn_chunk_fwd_o(tq, tk, vn1, h1, tg, chunk=C))):
+            flush.fill_(1)
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+            per[name].append((a0, a1))
+    torch.cuda.synchronize()
+    kms = {n: statistics.mean(a.elapsed_time(b2) for a, b2 in v) for n, v in per.items()}
     clocks = sampler.stop()
     NT = -(-T // C)
     macs = B * H * NT * (2 * C * K * V + C * K * V + C * (C + 1) // 2 * (K + V))
@@ -497,6 +511,7 @@ def gdn_main(args):
         "e2e": {"value": B * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": sum(t.numel() * 4 for t in host.values()),
                 "d2h_bytes_per_step": o_h.numel() * 4},
+        "kernels_ms": kms,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }

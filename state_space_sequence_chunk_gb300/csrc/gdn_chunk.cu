@@ -13,13 +13,13 @@
 // h [B, H, NT, K, V]; h0, final [B, H, K, V]; all fp32 (the pages run these
 // products in fp32 / TF32).
 //
-// This first GB300 version runs on the CUDA cores in fp32.  A CTA owns a
-// 32-column tile of V (lane = column), stages the chunk's K-wide rows of k, w
-// (or q, k) in shared memory, and keeps its state tile in shared memory;
-// every inner product reads one operand as a warp-wide broadcast and the
-// other conflict-free.  chunk_fwd_h walks its chunks in order (one CTA per
-// (batch, head, V tile)); chunk_fwd_o is one CTA per (batch, head, chunk,
-// V tile).
+// This GB300 version runs on the CUDA cores in fp32.  A CTA owns a 32-column
+// tile of V, stages the chunk's rows of k and w (or q and k) in shared memory
+// -- transposed where an operand is read as four consecutive rows -- and keeps
+// its state tile there.  Each thread computes a 4 x 4 or 4 x 2 register tile,
+// so that every 16-byte shared-memory read feeds several FMAs.  chunk_fwd_h
+// walks its chunks in order (one CTA per (batch, head, V tile)); chunk_fwd_o
+// is one CTA per (batch, head, chunk, V tile).
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -29,91 +29,146 @@ constexpr int kGdnThreads = 256;   // 8 warps
 constexpr int kVT = 32;            // V columns per CTA (one per lane)
 constexpr int kWarps = kGdnThreads / 32;
 
+// Transposed staging of a chunk's rows [t][K] into xT[kk][t] (pitch C + 4: the
+// 4-row reads below are 16-byte aligned, and the transposing stores -- t
+// fastest across a warp -- hit 32 distinct banks).
+// A thread's share of a [C][K] tile is at most C * K / 4 / threads <= 8 vectors
+// (K <= 128, C <= 64): all its loads are issued before the first store.
+constexpr int kMaxVecPerThread = 8;
+template <int C>
+__device__ __forceinline__ void stage_transposed(const float* __restrict__ src, float* xT, int b,
+                                                 int T, int t0, int nt, int H, int hh, int K) {
+    const int K4 = K >> 2;
+    float4 v[kMaxVecPerThread];
+#pragma unroll
+    for (int r = 0; r < kMaxVecPerThread; ++r) {
+        const int i = threadIdx.x + r * kGdnThreads, t = i % C, k4 = i / C;
+        v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < C * K4 && t < nt)
+            v[r] = __ldg(reinterpret_cast<const float4*>(src + ((int64_t)(b * T + t0 + t) * H + hh) * K) + k4);
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxVecPerThread; ++r) {
+        const int i = threadIdx.x + r * kGdnThreads, t = i % C, k4 = i / C;
+        if (i < C * K4) {
+            xT[(4 * k4 + 0) * (C + 4) + t] = v[r].x;
+            xT[(4 * k4 + 1) * (C + 4) + t] = v[r].y;
+            xT[(4 * k4 + 2) * (C + 4) + t] = v[r].z;
+            xT[(4 * k4 + 3) * (C + 4) + t] = v[r].w;
+        }
+    }
+}
+
 template <int C>
 __global__ void __launch_bounds__(kGdnThreads)
 gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
                  const float* __restrict__ u, const float* __restrict__ g,
                  const float* __restrict__ h0, float* __restrict__ h, float* __restrict__ v_new,
                  float* __restrict__ final_state, int T, int H, int K, int V, int NT) {
-    extern __shared__ float sm[];
-    float* ks = sm;                 // [C][K]
-    float* ws = ks + C * K;         // [C][K]
-    float* S = ws + C * K;          // [K][32]
-    float* vg = S + K * kVT;        // [C][32]
+    extern __shared__ __align__(16) float sm[];
+    constexpr int CP = C + 4;
+    float* ks = sm;                 // [C][K]   k rows (row-major)
+    float* wT = ks + C * K;         // [K][C+4] w, transposed
+    float* S = wT + K * CP;         // [K][32]  the state tile
+    float* vg = S + K * kVT;        // [C][32]  gated v_new
     float* gs = vg + C * kVT;       // [C]
     const int bh = blockIdx.x, b = bh / H, hh = bh - b * H;
     const int v0 = blockIdx.y * kVT, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int v = v0 + lane;
-    const bool vok = v < V;
+    const int K4 = K >> 2;
+    // thread maps: (2) 4 tokens x 2 columns; (4)(5) 4 state rows x 4 columns
+    const int tt = threadIdx.x >> 4, tv2 = threadIdx.x & 15;
+    const int tk = threadIdx.x >> 3, tv4 = threadIdx.x & 7;
     for (int kk = warp; kk < K; kk += kWarps)
-        S[kk * kVT + lane] = (h0 != nullptr && vok) ? h0[((int64_t)bh * K + kk) * V + v] : 0.f;
+        S[kk * kVT + lane] = (h0 != nullptr && v0 + lane < V) ? h0[((int64_t)bh * K + kk) * V + v0 + lane] : 0.f;
     for (int c = 0; c < NT; ++c) {
         const int t0 = c * C, nt = min(C, T - t0);
-        __syncthreads();   // the previous chunk's readers of ks / ws are done
-        // rows of K floats, 16-byte vectors, several loads in flight per thread
-        const int K4 = K >> 2;
-#pragma unroll 4
-        for (int i = threadIdx.x; i < nt * K4; i += kGdnThreads) {
-            const int t = i / K4, k4 = i - t * K4;
-            const int64_t src = ((int64_t)(b * T + t0 + t) * H + hh) * K + 4 * k4;
-            reinterpret_cast<float4*>(ks)[i] = __ldg(reinterpret_cast<const float4*>(k + src));
-            reinterpret_cast<float4*>(ws)[i] = __ldg(reinterpret_cast<const float4*>(w + src));
+        __syncthreads();   // the previous chunk's readers are done
+        {
+            float4 v[kMaxVecPerThread];
+#pragma unroll
+            for (int r = 0; r < kMaxVecPerThread; ++r) {
+                const int i = threadIdx.x + r * kGdnThreads, t = i / K4, k4 = i - t * K4;
+                v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < C * K4 && t < nt)
+                    v[r] = __ldg(reinterpret_cast<const float4*>(k + ((int64_t)(b * T + t0 + t) * H + hh) * K) + k4);
+            }
+#pragma unroll
+            for (int r = 0; r < kMaxVecPerThread; ++r) {
+                const int i = threadIdx.x + r * kGdnThreads;
+                if (i < C * K4) reinterpret_cast<float4*>(ks)[i] = v[r];
+            }
         }
-        if ((int)threadIdx.x < nt) gs[threadIdx.x] = g[(int64_t)(b * T + t0 + threadIdx.x) * H + hh];
+        stage_transposed<C>(w, wT, b, T, t0, nt, H, hh, K);
+        if ((int)threadIdx.x < C) gs[threadIdx.x] = (int)threadIdx.x < nt ? g[(int64_t)(b * T + t0 + threadIdx.x) * H + hh] : 0.f;
         __syncthreads();
         // (1) the chunk-start state
         float* hc = h + (((int64_t)bh * NT + c) * K) * V;
-        if (vok)
-            for (int kk = warp; kk < K; kk += kWarps) hc[(int64_t)kk * V + v] = S[kk * kVT + lane];
+        if (v0 + lane < V)
+            for (int kk = warp; kk < K; kk += kWarps) hc[(int64_t)kk * V + v0 + lane] = S[kk * kVT + lane];
         const float g_last = gs[nt - 1];
-        // (2) v_new = u - w h, (3) gate; tokens warp, warp + 8, ...
-        float acc[C / kWarps];
-#pragma unroll
-        for (int i = 0; i < C / kWarps; ++i) acc[i] = 0.f;
-        for (int kk = 0; kk < K; ++kk) {
-            const float s = S[kk * kVT + lane];
-#pragma unroll
-            for (int i = 0; i < C / kWarps; ++i) acc[i] = fmaf(ws[(warp + kWarps * i) * K + kk], s, acc[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < C / kWarps; ++i) {
-            const int t = warp + kWarps * i;
-            if (t < nt) {
-                const int64_t row = (int64_t)(b * T + t0 + t) * H + hh;
-                const float vn = vok ? u[row * V + v] - acc[i] : 0.f;
-                if (vok) v_new[row * V + v] = vn;
-                vg[t * kVT + lane] = vn * expf(g_last - gs[t]);
-            }
-        }
-        __syncthreads();
-        // (4) decay and (5) h += k^T v_gated; state rows warp, warp + 8, ...
-        const float decay = expf(g_last);
-        for (int kb = warp; kb < K; kb += kWarps * 4) {
-            float a4[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int kk = kb + kWarps * r;
-                a4[r] = kk < K ? S[kk * kVT + lane] * decay : 0.f;
-            }
-            for (int t = 0; t < nt; ++t) {
-                const float x = vg[t * kVT + lane];
+        // (2) v_new = u - w S for tokens 4 tt .. 4 tt + 3, columns 2 tv2, 2 tv2 + 1; (3) gate
+        if (4 * tt < C) {
+            float a[4][2] = {};
+            #pragma unroll 4
+            for (int kk = 0; kk < K; ++kk) {
+                const float4 wv = *reinterpret_cast<const float4*>(wT + kk * CP + 4 * tt);
+                const float2 sv = *reinterpret_cast<const float2*>(S + kk * kVT + 2 * tv2);
+                const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const int kk = kb + kWarps * r;
-                    if (kk < K) a4[r] = fmaf(ks[t * K + kk], x, a4[r]);
+                    a[r][0] = fmaf(wr[r], sv.x, a[r][0]);
+                    a[r][1] = fmaf(wr[r], sv.y, a[r][1]);
                 }
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                const int kk = kb + kWarps * r;
-                if (kk < K) S[kk * kVT + lane] = a4[r];
+                const int t = 4 * tt + r;
+                if (t < nt) {
+                    const int64_t row = (int64_t)(b * T + t0 + t) * H + hh;
+                    const float gate = expf(g_last - gs[t]);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int v = v0 + 2 * tv2 + q;
+                        const float vn = v < V ? u[row * V + v] - a[r][q] : 0.f;
+                        if (v < V) v_new[row * V + v] = vn;
+                        vg[t * kVT + 2 * tv2 + q] = vn * gate;
+                    }
+                } else {
+                    vg[t * kVT + 2 * tv2] = 0.f;
+                    vg[t * kVT + 2 * tv2 + 1] = 0.f;
+                }
             }
+        }
+        __syncthreads();
+        // (4) decay and (5) S += k^T v_gated for state rows 4 tk .. 4 tk + 3, columns 4 tv4 ..
+        if (4 * tk < K) {
+            const float decay = expf(g_last);
+            float a[4][4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float4 sv = *reinterpret_cast<const float4*>(S + (4 * tk + r) * kVT + 4 * tv4);
+                a[r][0] = sv.x * decay; a[r][1] = sv.y * decay; a[r][2] = sv.z * decay; a[r][3] = sv.w * decay;
+            }
+            #pragma unroll 4
+            for (int t = 0; t < nt; ++t) {
+                const float4 kv = *reinterpret_cast<const float4*>(ks + t * K + 4 * tk);
+                const float4 xv = *reinterpret_cast<const float4*>(vg + t * kVT + 4 * tv4);
+                const float kr[4] = {kv.x, kv.y, kv.z, kv.w}, xr[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) a[r][q] = fmaf(kr[r], xr[q], a[r][q]);
+            }
+            // every thread owns distinct S entries and all reads of S are done (barrier above)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                *reinterpret_cast<float4*>(S + (4 * tk + r) * kVT + 4 * tv4) = make_float4(a[r][0], a[r][1], a[r][2], a[r][3]);
         }
     }
     __syncthreads();
-    if (final_state != nullptr && vok)
+    if (final_state != nullptr && v0 + lane < V)
         for (int kk = warp; kk < K; kk += kWarps)
-            final_state[((int64_t)bh * K + kk) * V + v] = S[kk * kVT + lane];
+            final_state[((int64_t)bh * K + kk) * V + v0 + lane] = S[kk * kVT + lane];
 }
 
 template <int C>
@@ -122,57 +177,117 @@ gdn_fwd_o_kernel(const float* __restrict__ q, const float* __restrict__ k,
                  const float* __restrict__ v_new, const float* __restrict__ h,
                  const float* __restrict__ g, float* __restrict__ o, int T, int H, int K, int V,
                  int NT) {
-    extern __shared__ float sm[];
-    const int KP = K + 1;               // padded k rows: lanes read different rows
-    float* qs = sm;                     // [C][K]
-    float* ks = qs + C * K;             // [C][K + 1]
-    float* hs = ks + C * KP;            // [K][32]
+    extern __shared__ __align__(16) float sm[];
+    constexpr int CP = C + 4;
+    float* qT = sm;                     // [K][C+4] q, transposed
+    float* kT = qT + K * CP;            // [K][C+4] k, transposed
+    float* hs = kT + K * CP;            // [K][32]
     float* vs = hs + K * kVT;           // [C][32]
-    float* As = vs + C * kVT;           // [C][C + 1]
-    float* gs = As + C * (C + 1);       // [C]
+    float* AT = vs + C * kVT;           // [C][C+4] A, transposed: AT[j][i]
+    float* gs = AT + C * CP;            // [C]
     const int bh = blockIdx.x, b = bh / H, hh = bh - b * H, c = blockIdx.y;
     const int v0 = blockIdx.z * kVT, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int v = v0 + lane;
-    const bool vok = v < V;
     const int t0 = c * C, nt = min(C, T - t0);
-    const int K4 = K >> 2;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < nt * K4; i += kGdnThreads) {
-        const int t = i / K4, k4 = i - t * K4;
-        const int64_t src = ((int64_t)(b * T + t0 + t) * H + hh) * K + 4 * k4;
-        reinterpret_cast<float4*>(qs)[i] = __ldg(reinterpret_cast<const float4*>(q + src));
-        const float4 kv = __ldg(reinterpret_cast<const float4*>(k + src));
-        float* kd = ks + t * KP + 4 * k4;
-        kd[0] = kv.x; kd[1] = kv.y; kd[2] = kv.z; kd[3] = kv.w;
-    }
+    stage_transposed<C>(q, qT, b, T, t0, nt, H, hh, K);
+    stage_transposed<C>(k, kT, b, T, t0, nt, H, hh, K);
     const float* hc = h + (((int64_t)bh * NT + c) * K) * V;
-#pragma unroll 4
-    for (int kk = warp; kk < K; kk += kWarps) hs[kk * kVT + lane] = vok ? __ldg(hc + (int64_t)kk * V + v) : 0.f;
-#pragma unroll 4
-    for (int t = warp; t < nt; t += kWarps)
-        vs[t * kVT + lane] = vok ? __ldg(v_new + ((int64_t)(b * T + t0 + t) * H + hh) * V + v) : 0.f;
-    if ((int)threadIdx.x < nt) gs[threadIdx.x] = g[(int64_t)(b * T + t0 + threadIdx.x) * H + hh];
+    {
+        // all of this thread's h and v_new loads in flight before the stores
+        constexpr int kHRows = 128 / kWarps, kVRows = C / kWarps;
+        const bool vok = v0 + lane < V;
+        float hv[kHRows], xv[kVRows];
+#pragma unroll
+        for (int r = 0; r < kHRows; ++r) {
+            const int kk = warp + kWarps * r;
+            hv[r] = (kk < K && vok) ? __ldg(hc + (int64_t)kk * V + v0 + lane) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < kVRows; ++r) {
+            const int t = warp + kWarps * r;
+            xv[r] = (t < nt && vok) ? __ldg(v_new + ((int64_t)(b * T + t0 + t) * H + hh) * V + v0 + lane) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < kHRows; ++r) {
+            const int kk = warp + kWarps * r;
+            if (kk < K) hs[kk * kVT + lane] = hv[r];
+        }
+#pragma unroll
+        for (int r = 0; r < kVRows; ++r) vs[(warp + kWarps * r) * kVT + lane] = xv[r];
+    }
+    if ((int)threadIdx.x < C) gs[threadIdx.x] = (int)threadIdx.x < nt ? g[(int64_t)(b * T + t0 + threadIdx.x) * H + hh] : 0.f;
     __syncthreads();
-    // A[i][j] = (q_i . k_j) exp(g_i - g_j) for j <= i, else 0; rows warp + 8a, columns lane + 32b
-    for (int i = warp; i < nt; i += kWarps) {
-        for (int j0 = 0; j0 < nt; j0 += 32) {
-            const int j = j0 + lane;
-            float a = 0.f;
-            if (j <= i) {
-                for (int kk = 0; kk < K; ++kk) a = fmaf(qs[i * K + kk], ks[j * KP + kk], a);
-                a *= expf(gs[i] - gs[j]);
+    // A = (q k^T) o exp(g_i - g_j), j <= i: 4 x 4 tiles (rows 4 ti, columns 4 tj)
+    {
+        const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+        if (4 * ti < C && 4 * tj < C) {
+            float a[4][4] = {};
+            if (4 * tj <= 4 * ti + 3) {   // tiles wholly above the diagonal stay zero
+                #pragma unroll 4
+                for (int kk = 0; kk < K; ++kk) {
+                    const float4 qv = *reinterpret_cast<const float4*>(qT + kk * CP + 4 * ti);
+                    const float4 kv = *reinterpret_cast<const float4*>(kT + kk * CP + 4 * tj);
+                    const float qr[4] = {qv.x, qv.y, qv.z, qv.w}, kr[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int s2 = 0; s2 < 4; ++s2) a[r][s2] = fmaf(qr[r], kr[s2], a[r][s2]);
+                }
             }
-            if (j < C) As[i * (C + 1) + j] = a;
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) {
+                const int j = 4 * tj + s2;
+                float col[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = 4 * ti + r;
+                    col[r] = (j <= i && i < nt) ? a[r][s2] * expf(gs[i] - gs[j]) : 0.f;
+                }
+                *reinterpret_cast<float4*>(AT + j * CP + 4 * ti) = make_float4(col[0], col[1], col[2], col[3]);
+            }
         }
     }
     __syncthreads();
-    // o[i] = exp(g_i) q_i h + sum_{j <= i} A[i][j] v_new[j]
-    for (int i = warp; i < nt; i += kWarps) {
-        float inter = 0.f;
-        for (int kk = 0; kk < K; ++kk) inter = fmaf(qs[i * K + kk], hs[kk * kVT + lane], inter);
-        float intra = 0.f;
-        for (int j = 0; j <= i; ++j) intra = fmaf(As[i * (C + 1) + j], vs[j * kVT + lane], intra);
-        if (vok) o[((int64_t)(b * T + t0 + i) * H + hh) * V + v] = inter * expf(gs[i]) + intra;
+    // o[i] = exp(g_i) q_i h + sum_{j <= i} A[i][j] v_new[j]: rows 4 ti, columns 2 tv
+    {
+        const int ti = threadIdx.x >> 4, tv = threadIdx.x & 15;
+        if (4 * ti < C) {
+            float in[4][2] = {}, ia[4][2] = {};
+            #pragma unroll 4
+            for (int kk = 0; kk < K; ++kk) {
+                const float4 qv = *reinterpret_cast<const float4*>(qT + kk * CP + 4 * ti);
+                const float2 hv = *reinterpret_cast<const float2*>(hs + kk * kVT + 2 * tv);
+                const float qr[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    in[r][0] = fmaf(qr[r], hv.x, in[r][0]);
+                    in[r][1] = fmaf(qr[r], hv.y, in[r][1]);
+                }
+            }
+            const int jmax = min(nt, 4 * ti + 4);
+            #pragma unroll 4
+            for (int j = 0; j < jmax; ++j) {
+                const float4 av = *reinterpret_cast<const float4*>(AT + j * CP + 4 * ti);
+                const float2 xv = *reinterpret_cast<const float2*>(vs + j * kVT + 2 * tv);
+                const float ar[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    ia[r][0] = fmaf(ar[r], xv.x, ia[r][0]);
+                    ia[r][1] = fmaf(ar[r], xv.y, ia[r][1]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = 4 * ti + r;
+                if (i < nt) {
+                    const float eg = expf(gs[i]);
+#pragma unroll
+                    for (int qq = 0; qq < 2; ++qq) {
+                        const int v = v0 + 2 * tv + qq;
+                        if (v < V) o[((int64_t)(b * T + t0 + i) * H + hh) * V + v] = in[r][qq] * eg + ia[r][qq];
+                    }
+                }
+            }
+        }
     }
 }
 
@@ -184,7 +299,7 @@ cudaError_t launch_c(const GdnProblem& p, bool fwd_h, const float* q, const floa
     const unsigned vtiles = (unsigned)((V + kVT - 1) / kVT);
     cudaError_t e;
     if (fwd_h) {
-        const size_t smem = (size_t)(2 * C * K + K * kVT + C * kVT + C) * sizeof(float);
+        const size_t smem = (size_t)(C * K + K * (C + 4) + K * kVT + C * kVT + C) * sizeof(float);
         auto kern = gdn_fwd_h_kernel<C>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
             cudaSuccess)
@@ -193,7 +308,7 @@ cudaError_t launch_c(const GdnProblem& p, bool fwd_h, const float* q, const floa
             k, w, u, g, h0, h, v_new, final_state, T, H, K, V, NT);
     } else {
         const size_t smem =
-            (size_t)(C * K + C * (K + 1) + K * kVT + C * kVT + C * (C + 1) + C) * sizeof(float);
+            (size_t)(2 * K * (C + 4) + K * kVT + C * kVT + C * (C + 4) + C) * sizeof(float);
         auto kern = gdn_fwd_o_kernel<C>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
             cudaSuccess)
