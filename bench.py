@@ -116,8 +116,11 @@ def job_throughput(world: int, tokens_per_rank: int, ms_per_step: float) -> floa
 
 
 def launches_per_step(w: synth.Workload, sms: int) -> int:
-    """Kernels one ssd_fwd enqueues: three, or five when fwd_pass_state takes
-    its two-pass form for long chains (same rule as the library's launcher)."""
+    """Kernels one ssd_fwd enqueues: three for bf16, or five when fwd_pass_state
+    takes its two-pass form for long chains (same rule as the library's
+    launcher); four for fp32, whose fwd_pass_state is chunk products + scan."""
+    if w.dtype != "bf16":
+        return 4
     hpg = w.nheads // w.ngroups
     nc = -(-w.seqlen // w.chunk)
     if (w.dtype == "bf16" and w.dstate <= 128 and w.headdim <= 64 and w.nheads % 2 == 0

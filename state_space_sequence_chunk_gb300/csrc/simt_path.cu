@@ -12,86 +12,114 @@ namespace {
 constexpr int kThreads = 256;
 
 // ---------------------------------------------------------------------------
-// fwd_pass_state: one CTA per (16 rows of P, batch*head).  Thread t owns row
-// p = t / 16 of the tile and state columns n = t % 16 + 16 k.  Chunks are walked
-// in order; each chunk is consumed in sub-chunks of 32 tokens staged in shared
-// memory.  Per chunk: store S as the chunk's start state, then
-//   S <- 2^{g_last} S + sum_q x[q][p] * (dt_q 2^{g_last - g_q}) * B[q][n].
+// fwd_pass_state on the CUDA cores (fp32 inputs, whose hiddens are fp32), in
+// two kernels so that the chunks run in parallel:
+//   fps_chunk_products: per (16 rows of P, chunk, batch*head), the chunk's
+//     product D_c[p][n] = sum_q x[q][p] (dt_q 2^{g_last - g_q}) B[q][n], written
+//     into that chunk's slot of hiddens (same size: [n][p], fp32);
+//   fps_state_scan: per (state element, batch*head), over the chunks in order,
+//     hiddens[c] <- S (replacing D_c), S <- 2^{g_last} S + D_c, from S = init.
+// This is "Kernel 2: fwd_pass_state" with its loop over chunks split at the
+// only serial step (the state update is linear in S); thread t of the
+// products kernel owns row p = t / 16 and state columns n = t % 16 + 16 k.
 // ---------------------------------------------------------------------------
 constexpr int kPT = 16;    // rows of P per CTA
 constexpr int kSub = 32;   // tokens per staged sub-chunk
+constexpr int kMaxN = 256;
 
-template <typename T>
 __global__ void __launch_bounds__(kThreads)
-fwd_pass_state_simt(const T* __restrict__ x, const T* __restrict__ B,
-                    const float* __restrict__ Gcs, const float* __restrict__ dtT,
-                    const float* init, T* __restrict__ hiddens, float* final_state,
-                    int L, int H, int P, int N, int G, int Q, int nc, int Lp, int hpg) {
+fps_chunk_products(const float* __restrict__ x, const float* __restrict__ B,
+                   const float* __restrict__ Gcs, const float* __restrict__ dtT,
+                   float* __restrict__ hiddens, int L, int H, int P, int N, int G, int Q, int nc,
+                   int Lp, int hpg) {
     extern __shared__ float sm[];
     float* xs = sm;                    // [kSub][kPT]
     float* bs = xs + kSub * kPT;       // [kSub][N]
     float* sc = bs + kSub * N;         // [kSub] per-token scale
-
-    const int p0 = blockIdx.x * kPT;
-    const int bh = blockIdx.y, bidx = bh / H, h = bh % H, grp = h / hpg;
+    const int p0 = blockIdx.x * kPT, c = blockIdx.y;
+    const int bh = blockIdx.z, bidx = bh / H, h = bh % H, grp = h / hpg;
     const int tid = threadIdx.x, pl = tid / 16, nl = tid % 16;
-    const int p = p0 + pl;
     const int nper = N / 16;
-
-    float S[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        S[k] = 0.f;
-        if (k < nper && init) S[k] = init[(((int64_t)bidx * H + h) * P + p) * N + nl + 16 * k];
-    }
     const float* grow = Gcs + (int64_t)bh * Lp;
     const float* drow = dtT + (int64_t)bh * Lp;
-
-    for (int c = 0; c < nc; ++c) {
-        // chunk-start state
-        // chunk-start state, stored transposed: hiddens[b, h, c, n, p]
-        T* hrow = hiddens + (((int64_t)bidx * H + h) * nc + c) * (int64_t)N * P + p;
+    const int t0 = c * Q;
+    const float glast = grow[t0 + Q - 1];  // padded tokens repeat the last real value
+    float acc[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-            if (k < nper) hrow[(int64_t)(nl + 16 * k) * P] = from_f32<T>(S[k]);
-
-        const int t0 = c * Q;
-        const float glast = grow[t0 + Q - 1];  // padded tokens repeat the last real value
-        float acc[16];
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    for (int s0 = 0; s0 < Q; s0 += kSub) {
+        __syncthreads();
+        // loads: x 2 per thread, B up to kSub * kMaxN / threads = 32 per thread, all in flight
+        {
+            constexpr int kXPer = kSub * kPT / kThreads, kBPer = kSub * kMaxN / kThreads;
+            float xv[kXPer], bv[kBPer];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-
-        for (int s0 = 0; s0 < Q; s0 += kSub) {
-            __syncthreads();
-            for (int i = tid; i < kSub * kPT; i += kThreads) {
-                const int q = i / kPT, pp = i % kPT, tg = t0 + s0 + q;
-                xs[i] = tg < L ? to_f32(x[(((int64_t)bidx * L + tg) * H + h) * P + p0 + pp]) : 0.f;
+            for (int r = 0; r < kXPer; ++r) {
+                const int i = tid + r * kThreads, q = i / kPT, pp = i % kPT, tg = t0 + s0 + q;
+                xv[r] = tg < L ? x[(((int64_t)bidx * L + tg) * H + h) * P + p0 + pp] : 0.f;
             }
-            for (int i = tid; i < kSub * N; i += kThreads) {
-                const int q = i / N, n = i % N, tg = t0 + s0 + q;
-                bs[i] = tg < L ? to_f32(B[(((int64_t)bidx * L + tg) * G + grp) * N + n]) : 0.f;
+#pragma unroll
+            for (int r = 0; r < kBPer; ++r) {
+                const int i = tid + r * kThreads, q = i / N, n = i % N, tg = t0 + s0 + q;
+                bv[r] = (i < kSub * N && tg < L) ? B[(((int64_t)bidx * L + tg) * G + grp) * N + n] : 0.f;
             }
+#pragma unroll
+            for (int r = 0; r < kXPer; ++r) xs[tid + r * kThreads] = xv[r];
+#pragma unroll
+            for (int r = 0; r < kBPer; ++r)
+                if (tid + r * kThreads < kSub * N) bs[tid + r * kThreads] = bv[r];
             if (tid < kSub) {
                 const int tq = t0 + s0 + tid;
                 sc[tid] = drow[tq] * exp2f(glast - grow[tq]);
             }
-            __syncthreads();
-            for (int q = 0; q < kSub; ++q) {
-                const float xv = xs[q * kPT + pl] * sc[q];
+        }
+        __syncthreads();
+        for (int q = 0; q < kSub; ++q) {
+            const float xv = xs[q * kPT + pl] * sc[q];
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    if (k < nper) acc[k] = fmaf(xv, bs[q * N + nl + 16 * k], acc[k]);
+            for (int k = 0; k < 16; ++k)
+                if (k < nper) acc[k] = fmaf(xv, bs[q * N + nl + 16 * k], acc[k]);
+        }
+    }
+    // D_c into the chunk's hiddens slot, [n][p]
+    float* hrow = hiddens + (((int64_t)bidx * H + h) * nc + c) * (int64_t)N * P + p0 + pl;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        if (k < nper) hrow[(int64_t)(nl + 16 * k) * P] = acc[k];
+}
+
+// One thread per state element (n, p) of one (batch, head): f = n P + p, so
+// the hiddens slots are read and written coalesced.  Eight chunks' products
+// are loaded before their serial fma chain.
+constexpr int kScanBatch = 8;
+__global__ void __launch_bounds__(kThreads)
+fps_state_scan(const float* __restrict__ Gcs, const float* init, float* __restrict__ hiddens,
+               float* final_state, int H, int P, int N, int Q, int nc, int Lp) {
+    const int f = blockIdx.x * kThreads + threadIdx.x, bh = blockIdx.y;
+    if (f >= P * N) return;
+    const int n = f / P, p = f - n * P;
+    const int64_t sidx = ((int64_t)bh * P + p) * N + n;
+    float S = init != nullptr ? init[sidx] : 0.f;
+    float* hb = hiddens + (int64_t)bh * nc * N * P + f;
+    const float* grow = Gcs + (int64_t)bh * Lp + Q - 1;
+    for (int c0 = 0; c0 < nc; c0 += kScanBatch) {
+        float Dv[kScanBatch], gl[kScanBatch];
+#pragma unroll
+        for (int i = 0; i < kScanBatch; ++i) {
+            const int c = c0 + i;
+            Dv[i] = c < nc ? hb[(int64_t)c * N * P] : 0.f;
+            gl[i] = c < nc ? grow[(int64_t)c * Q] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kScanBatch; ++i) {
+            const int c = c0 + i;
+            if (c < nc) {
+                hb[(int64_t)c * N * P] = S;
+                S = fmaf(exp2f(gl[i]), S, Dv[i]);
             }
         }
-        const float e = exp2f(glast);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) S[k] = fmaf(e, S[k], acc[k]);
     }
-    if (final_state) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            if (k < nper) final_state[(((int64_t)bidx * H + h) * P + p) * N + nl + 16 * k] = S[k];
-    }
+    if (final_state != nullptr) final_state[sidx] = S;
 }
 
 // ---------------------------------------------------------------------------
@@ -146,8 +174,11 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
     const T* hbase = hiddens + (((int64_t)bidx * H + h) * nc + c) * (int64_t)P * N;
     for (int n0 = 0; n0 < N; n0 += 32) {
         __syncthreads();
+        // consecutive threads read consecutive p of one state column (coalesced);
+        // the odd row stride keeps the transposed smem writes conflict-free
+#pragma unroll 4
         for (int i = tid; i < P * 32; i += kThreads) {
-            const int pp = i / 32, nn = i % 32;
+            const int nn = i / P, pp = i % P;
             hs[pp * 33 + nn] = (n0 + nn < N) ? to_f32(hbase[(int64_t)(n0 + nn) * P + pp]) : 0.f;
         }
         __syncthreads();
@@ -169,10 +200,12 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
     // intra-chunk term, key blocks j0 <= i0
     for (int j0 = 0; j0 <= i0; j0 += kRows) {
         __syncthreads();
+#pragma unroll 4
         for (int i = tid; i < kRows * N; i += kThreads) {
             const int r = i / N, n = i % N, tg = t0 + j0 + r;
             bs[r * NS + n] = tg < L ? to_f32(B[(((int64_t)bidx * L + tg) * G + grp) * N + n]) : 0.f;
         }
+#pragma unroll 4
         for (int i = tid; i < kRows * P; i += kThreads) {
             const int r = i / P, pp = i % P, tg = t0 + j0 + r;
             xs[i] = tg < L ? to_f32(x[(((int64_t)bidx * L + tg) * H + h) * P + pp]) : 0.f;
@@ -211,18 +244,21 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
     }
 }
 
-template <typename T>
 cudaError_t launch_fps(const Problem& p, const void* x, const void* B, const float* Gcs,
-                       const float* dtT, const float* init, void* hid, float* fin,
-                       cudaStream_t stream) {
+                      const float* dtT, const float* init, void* hid, float* fin,
+                      cudaStream_t stream) {
     const size_t smem = (size_t)(kSub * kPT + kSub * p.N + kSub) * sizeof(float);
-    auto kern = fwd_pass_state_simt<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(fps_chunk_products, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(p.P / kPT), (unsigned)(p.b * p.H));
-    kern<<<grid, kThreads, smem, stream>>>((const T*)x, (const T*)B, Gcs, dtT, init, (T*)hid,
-                                           fin, (int)p.L, (int)p.H, (int)p.P, (int)p.N,
-                                           (int)p.G, (int)p.Q, (int)p.nc, (int)p.Lp, (int)p.hpg);
+    fps_chunk_products<<<dim3((unsigned)(p.P / kPT), (unsigned)p.nc, (unsigned)(p.b * p.H)), kThreads,
+                         smem, stream>>>((const float*)x, (const float*)B, Gcs, dtT, (float*)hid,
+                                         (int)p.L, (int)p.H, (int)p.P, (int)p.N, (int)p.G, (int)p.Q,
+                                         (int)p.nc, (int)p.Lp, (int)p.hpg);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fps_state_scan<<<dim3((unsigned)((p.P * p.N + kThreads - 1) / kThreads), (unsigned)(p.b * p.H)),
+                     kThreads, 0, stream>>>(Gcs, init, (float*)hid, fin, (int)p.H, (int)p.P,
+                                            (int)p.N, (int)p.Q, (int)p.nc, (int)p.Lp);
     return cudaGetLastError();
 }
 
@@ -259,7 +295,7 @@ cudaError_t launch_fwd_pass_state(const Problem& p, const void* x, const void* B
         return launch_fwd_pass_state_tc(p, x, B, Gcs, dtT, init, hiddens, final_state, scratch,
                                         stream);
     }
-    return launch_fps<float>(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
+    return launch_fps(p, x, B, Gcs, dtT, init, hiddens, final_state, stream);
 }
 
 cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, const void* C,
