@@ -93,6 +93,12 @@ __device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t v) {
 __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
+// One 32-byte store (eight 32-bit words); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
 // Barrier among `n` threads (a multiple of 32) on hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -119,7 +125,6 @@ template <int Q>
 __global__ void __launch_bounds__(kThreads, 1)
 compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_h,
-               const __grid_constant__ CUtensorMap tm_y,
                const float* __restrict__ Gcs, const float* __restrict__ dtT,
                const float* __restrict__ D, __nv_bfloat16* __restrict__ y, int L, int H, int P,
                int nc, int Lp, int hpg, int units) {
@@ -553,21 +558,34 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     if (i < Q && t < L) {
                         const uint8_t* xr = st + i * kRowBytes;
                         __nv_bfloat16* yr = y + (((int64_t)ui.b * L + t) * H + ui.h) * P;
+                        // 32 bytes (16 columns) per store where the row is 32-byte aligned
+                        const bool a32 = (reinterpret_cast<uintptr_t>(yr) & 31) == 0;
 #pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            if (ch * 8 < P) {
-                                const int off = (ch ^ (i & 7)) << 4;
-                                const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
-                                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                                uint32_t ow[4];
+                        for (int c2 = 0; c2 < 4; ++c2) {
+                            if (c2 * 16 < P) {   // P is a multiple of 16
+                                uint32_t ow[8];
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int p0 = ch * 8 + 2 * e;
-                                    const uint32_t* vv = p0 < 32 ? v0 : v1;
-                                    ow[e] = pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
+                                for (int hh = 0; hh < 2; ++hh) {
+                                    const int ch = 2 * c2 + hh;
+                                    const int off = (ch ^ (i & 7)) << 4;
+                                    const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
+                                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int p0 = ch * 8 + 2 * e;
+                                        const uint32_t* vv = p0 < 32 ? v0 : v1;
+                                        ow[4 * hh + e] =
+                                            pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
                                                       __uint_as_float(vv[(p0 & 31) + 1]) + dh * bf16hi(xw[e]));
+                                    }
                                 }
-                                *reinterpret_cast<uint4*>(yr + ch * 8) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                                __nv_bfloat16* dst = yr + c2 * 16;
+                                if (a32) {
+                                    st_global_v8(dst, ow);
+                                } else {
+                                    reinterpret_cast<uint4*>(dst)[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                                    reinterpret_cast<uint4*>(dst)[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+                                }
                             }
                         }
                     }
@@ -592,7 +610,7 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
                      const float* Gcs, const float* dtT, const void* hid, const float* D, void* y,
                      cudaStream_t stream) {
     using Cfg = CoCfg<Q>;
-    CUtensorMap tx, tc, tb, th, ty;
+    CUtensorMap tx, tc, tb, th;
     const uint64_t xd[4] = {(uint64_t)p.P, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
     const uint64_t xs[3] = {(uint64_t)p.P * 2, (uint64_t)p.H * p.P * 2,
                             (uint64_t)p.L * p.H * p.P * 2};
@@ -610,8 +628,7 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     if (!encode_tmap_4d(&tx, bf, x, xd, xs, box_x, sw) ||
         !encode_tmap_4d(&tc, bf, C, bd, bs, box_x, sw) ||
         !encode_tmap_4d(&tb, bf, B, bd, bs, box_b, sw) ||
-        !encode_tmap_4d(&th, bf, hid, hd, hs, box_h, sw) ||
-        !encode_tmap_4d(&ty, bf, y, xd, xs, box_b, sw))
+        !encode_tmap_4d(&th, bf, hid, hd, hs, box_h, sw))
         return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -632,7 +649,7 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.chained ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, tx, tc, tb, th, ty, Gcs, dtT, D, (__nv_bfloat16*)y, (int)p.L,
+    e = cudaLaunchKernelEx(&cfg, kern, tx, tc, tb, th, Gcs, dtT, D, (__nv_bfloat16*)y, (int)p.L,
                            (int)p.H, (int)p.P, (int)p.nc, (int)p.Lp, (int)p.hpg, (int)units);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -276,3 +276,24 @@ def test_errors_are_raised():
     with pytest.raises(ssd.SSDError, match="SSD_ERR_ALIAS"):
         ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=64,
                     out=dev["x"])
+
+
+@pytest.mark.parametrize("headdim", [64, 16])
+def test_output_at_16_byte_offset(headdim):
+    """y may start on any 16-byte boundary: an output 16 bytes past a 32-byte
+    boundary (where the 32-byte row stores cannot be used) holds exactly the
+    values of an aligned one."""
+    w = small(seqlen=300, nheads=4, ngroups=2, headdim=headdim, dstate=128, chunk=128,
+              dtype="bf16", batch=2)
+    dev = to_device(synth.make_inputs(w), "bf16")
+    y_ref, _ = ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                           chunk_size=128, return_final_state=False)
+    n = dev["x"].numel()
+    flat = torch.full((n + 16,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y_off = flat[8:8 + n].view(dev["x"].shape)
+    assert y_off.data_ptr() % 32 == 16
+    ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], chunk_size=128,
+                return_final_state=False, out=y_off)
+    torch.cuda.synchronize()
+    assert torch.equal(y_off, y_ref)
+    assert torch.isnan(flat[:8]).all() and torch.isnan(flat[8 + n:]).all()
