@@ -13,13 +13,14 @@
 // h [B, H, NT, K, V]; h0, final [B, H, K, V]; all fp32 (the pages run these
 // products in fp32 / TF32).
 //
-// This GB300 version runs on the CUDA cores in fp32.  A CTA owns a 32-column
-// tile of V, stages the chunk's rows of k and w (or q and k) in shared memory
-// -- transposed where an operand is read as four consecutive rows -- and keeps
-// its state tile there.  Each thread computes a 4 x 4 or 4 x 2 register tile,
-// so that every 16-byte shared-memory read feeds several FMAs.  chunk_fwd_h
-// walks its chunks in order (one CTA per (batch, head, V tile)); chunk_fwd_o
-// is one CTA per (batch, head, chunk, V tile).
+// This GB300 version runs on the CUDA cores in fp32.  A CTA owns a tile of V
+// columns (32 for chunk_fwd_h, 64 for chunk_fwd_o), stages the chunk's rows of
+// k and w (or q and k) in shared memory -- transposed where an operand is read
+// as four consecutive rows -- and keeps its state tile there.  Each thread
+// computes a 4 x 4 or 4 x 2 register tile, so that every 16-byte shared-memory
+// read feeds several FMAs.  chunk_fwd_h walks its chunks in order (one CTA per
+// (batch, head, V tile)); chunk_fwd_o is one CTA per (batch, head, chunk, V
+// tile).
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -171,6 +172,14 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
             final_state[((int64_t)bh * K + kk) * V + v0 + lane] = S[kk * kVT + lane];
 }
 
+// chunk_fwd_o: one CTA per (batch, head, chunk, 64-column half of V).  The
+// chunk's masked q k^T is computed once per CTA (twice per chunk for V = 128,
+// against four times with 32-column tiles) and the o tile is a 4 x 4 register
+// tile per thread.  The h half-tile [K][64] is loaded into registers while
+// q k^T is computed, and is stored into the space of the transposed k once
+// q k^T no longer needs it.
+constexpr int kVO = 64;                 // V columns per chunk_fwd_o CTA
+constexpr int kHPerThread = 128 * kVO / kGdnThreads;   // 32: h values a thread carries (K <= 128)
 template <int C>
 __global__ void __launch_bounds__(kGdnThreads)
 gdn_fwd_o_kernel(const float* __restrict__ q, const float* __restrict__ k,
@@ -179,40 +188,39 @@ gdn_fwd_o_kernel(const float* __restrict__ q, const float* __restrict__ k,
                  int NT) {
     extern __shared__ __align__(16) float sm[];
     constexpr int CP = C + 4;
+    const int KH = K * (CP > kVO ? CP : kVO);
     float* qT = sm;                     // [K][C+4] q, transposed
-    float* kT = qT + K * CP;            // [K][C+4] k, transposed
-    float* hs = kT + K * CP;            // [K][32]
-    float* vs = hs + K * kVT;           // [C][32]
-    float* AT = vs + C * kVT;           // [C][C+4] A, transposed: AT[j][i]
+    float* kT = qT + K * CP;            // [K][C+4] k, transposed (A phase) ...
+    float* hs = kT;                     // ... then [K][64] h (o phase)
+    float* vs = kT + KH;                // [C][64]
+    float* AT = vs + C * kVO;           // [C][C+4] A, transposed: AT[j][i]
     float* gs = AT + C * CP;            // [C]
     const int bh = blockIdx.x, b = bh / H, hh = bh - b * H, c = blockIdx.y;
-    const int v0 = blockIdx.z * kVT, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int v0 = blockIdx.z * kVO;
     const int t0 = c * C, nt = min(C, T - t0);
+    // this thread's column of the h and v_new tiles, and its first row
+    const int col = threadIdx.x & (kVO - 1), row0 = threadIdx.x / kVO;
+    constexpr int kRowStep = kGdnThreads / kVO;   // 4
+    const bool cok = v0 + col < V;
+    const float* hc = h + (((int64_t)bh * NT + c) * K) * V + v0 + col;
+    float hv[kHPerThread];
+#pragma unroll
+    for (int r = 0; r < kHPerThread; ++r) {
+        const int kk = row0 + kRowStep * r;
+        hv[r] = (kk < K && cok) ? __ldg(hc + (int64_t)kk * V) : 0.f;
+    }
     stage_transposed<C>(q, qT, b, T, t0, nt, H, hh, K);
     stage_transposed<C>(k, kT, b, T, t0, nt, H, hh, K);
-    const float* hc = h + (((int64_t)bh * NT + c) * K) * V;
     {
-        // all of this thread's h and v_new loads in flight before the stores
-        constexpr int kHRows = 128 / kWarps, kVRows = C / kWarps;
-        const bool vok = v0 + lane < V;
-        float hv[kHRows], xv[kVRows];
-#pragma unroll
-        for (int r = 0; r < kHRows; ++r) {
-            const int kk = warp + kWarps * r;
-            hv[r] = (kk < K && vok) ? __ldg(hc + (int64_t)kk * V + v0 + lane) : 0.f;
-        }
+        constexpr int kVRows = C / kRowStep;
+        float xv[kVRows];
 #pragma unroll
         for (int r = 0; r < kVRows; ++r) {
-            const int t = warp + kWarps * r;
-            xv[r] = (t < nt && vok) ? __ldg(v_new + ((int64_t)(b * T + t0 + t) * H + hh) * V + v0 + lane) : 0.f;
+            const int t = row0 + kRowStep * r;
+            xv[r] = (t < nt && cok) ? __ldg(v_new + ((int64_t)(b * T + t0 + t) * H + hh) * V + v0 + col) : 0.f;
         }
 #pragma unroll
-        for (int r = 0; r < kHRows; ++r) {
-            const int kk = warp + kWarps * r;
-            if (kk < K) hs[kk * kVT + lane] = hv[r];
-        }
-#pragma unroll
-        for (int r = 0; r < kVRows; ++r) vs[(warp + kWarps * r) * kVT + lane] = xv[r];
+        for (int r = 0; r < kVRows; ++r) vs[(row0 + kRowStep * r) * kVO + col] = xv[r];
     }
     if ((int)threadIdx.x < C) gs[threadIdx.x] = (int)threadIdx.x < nt ? g[(int64_t)(b * T + t0 + threadIdx.x) * H + hh] : 0.f;
     __syncthreads();
@@ -236,54 +244,65 @@ gdn_fwd_o_kernel(const float* __restrict__ q, const float* __restrict__ k,
 #pragma unroll
             for (int s2 = 0; s2 < 4; ++s2) {
                 const int j = 4 * tj + s2;
-                float col[4];
+                float cl[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int i = 4 * ti + r;
-                    col[r] = (j <= i && i < nt) ? a[r][s2] * expf(gs[i] - gs[j]) : 0.f;
+                    cl[r] = (j <= i && i < nt) ? a[r][s2] * expf(gs[i] - gs[j]) : 0.f;
                 }
-                *reinterpret_cast<float4*>(AT + j * CP + 4 * ti) = make_float4(col[0], col[1], col[2], col[3]);
+                *reinterpret_cast<float4*>(AT + j * CP + 4 * ti) = make_float4(cl[0], cl[1], cl[2], cl[3]);
             }
         }
     }
+    __syncthreads();   // every read of kT is done: h takes its place
+#pragma unroll
+    for (int r = 0; r < kHPerThread; ++r) {
+        const int kk = row0 + kRowStep * r;
+        if (kk < K) hs[kk * kVO + col] = hv[r];
+    }
     __syncthreads();
-    // o[i] = exp(g_i) q_i h + sum_{j <= i} A[i][j] v_new[j]: rows 4 ti, columns 2 tv
+    // o[i] = exp(g_i) q_i h + sum_{j <= i} A[i][j] v_new[j]: rows 4 ti, columns 4 tv
     {
         const int ti = threadIdx.x >> 4, tv = threadIdx.x & 15;
         if (4 * ti < C) {
-            float in[4][2] = {}, ia[4][2] = {};
+            float in[4][4] = {}, ia[4][4] = {};
             #pragma unroll 4
             for (int kk = 0; kk < K; ++kk) {
                 const float4 qv = *reinterpret_cast<const float4*>(qT + kk * CP + 4 * ti);
-                const float2 hv = *reinterpret_cast<const float2*>(hs + kk * kVT + 2 * tv);
-                const float qr[4] = {qv.x, qv.y, qv.z, qv.w};
+                const float4 hv4 = *reinterpret_cast<const float4*>(hs + kk * kVO + 4 * tv);
+                const float qr[4] = {qv.x, qv.y, qv.z, qv.w}, hr[4] = {hv4.x, hv4.y, hv4.z, hv4.w};
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    in[r][0] = fmaf(qr[r], hv.x, in[r][0]);
-                    in[r][1] = fmaf(qr[r], hv.y, in[r][1]);
-                }
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2) in[r][s2] = fmaf(qr[r], hr[s2], in[r][s2]);
             }
             const int jmax = min(nt, 4 * ti + 4);
             #pragma unroll 4
             for (int j = 0; j < jmax; ++j) {
                 const float4 av = *reinterpret_cast<const float4*>(AT + j * CP + 4 * ti);
-                const float2 xv = *reinterpret_cast<const float2*>(vs + j * kVT + 2 * tv);
-                const float ar[4] = {av.x, av.y, av.z, av.w};
+                const float4 xv = *reinterpret_cast<const float4*>(vs + j * kVO + 4 * tv);
+                const float ar[4] = {av.x, av.y, av.z, av.w}, xr[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    ia[r][0] = fmaf(ar[r], xv.x, ia[r][0]);
-                    ia[r][1] = fmaf(ar[r], xv.y, ia[r][1]);
-                }
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2) ia[r][s2] = fmaf(ar[r], xr[s2], ia[r][s2]);
             }
+            const int vc = v0 + 4 * tv;   // this thread's first column
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int i = 4 * ti + r;
                 if (i < nt) {
                     const float eg = expf(gs[i]);
+                    float* orow = o + ((int64_t)(b * T + t0 + i) * H + hh) * V;
+                    float ov[4];
 #pragma unroll
-                    for (int qq = 0; qq < 2; ++qq) {
-                        const int v = v0 + 2 * tv + qq;
-                        if (v < V) o[((int64_t)(b * T + t0 + i) * H + hh) * V + v] = in[r][qq] * eg + ia[r][qq];
+                    for (int s2 = 0; s2 < 4; ++s2) ov[s2] = in[r][s2] * eg + ia[r][s2];
+                    if ((V & 3) == 0 && vc + 3 < V) {
+                        *reinterpret_cast<float4*>(orow + vc) = make_float4(ov[0], ov[1], ov[2], ov[3]);
+                    } else {
+#pragma unroll
+                        for (int s2 = 0; s2 < 4; ++s2)
+                            if (vc + s2 < V) orow[vc + s2] = ov[s2];
                     }
                 }
             }
@@ -307,13 +326,15 @@ cudaError_t launch_c(const GdnProblem& p, bool fwd_h, const float* q, const floa
         kern<<<dim3((unsigned)(p.B * p.H), vtiles), kGdnThreads, smem, stream>>>(
             k, w, u, g, h0, h, v_new, final_state, T, H, K, V, NT);
     } else {
+        const int kh = K * ((C + 4) > kVO ? (C + 4) : kVO);
         const size_t smem =
-            (size_t)(2 * K * (C + 4) + K * kVT + C * kVT + C * (C + 4) + C) * sizeof(float);
+            (size_t)(K * (C + 4) + kh + C * kVO + C * (C + 4) + C) * sizeof(float);
         auto kern = gdn_fwd_o_kernel<C>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
             cudaSuccess)
             return e;
-        kern<<<dim3((unsigned)(p.B * p.H), (unsigned)NT, vtiles), kGdnThreads, smem, stream>>>(
+        const unsigned vhalves = (unsigned)((V + kVO - 1) / kVO);
+        kern<<<dim3((unsigned)(p.B * p.H), (unsigned)NT, vhalves), kGdnThreads, smem, stream>>>(
             q, k, v_new, h, g, o, T, H, K, V, NT);
     }
     return cudaGetLastError();

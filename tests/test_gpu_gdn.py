@@ -33,6 +33,8 @@ def gdn_inputs(B, T, H, K, V, chunk, seed, with_h0=True):
     (1, 256, 2, 64, 32, 32, False),     # no initial state
     (2, 100, 2, 16, 48, 16, True),      # V not a multiple of the 32-column tile
     (1, 7, 1, 32, 64, 64, True),        # shorter than one chunk
+    (1, 130, 2, 32, 37, 32, True),      # V not a multiple of 4 (scalar loads and stores)
+    (1, 200, 2, 128, 100, 64, False),   # two V halves of chunk_fwd_o, the second partial
 ])
 def test_gdn_matches_oracle(B, T, H, K, V, chunk, with_h0):
     q, k, w, u, g, h0 = gdn_inputs(B, T, H, K, V, chunk, seed=T + K)
