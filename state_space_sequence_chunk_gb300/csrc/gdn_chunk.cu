@@ -27,6 +27,10 @@ namespace ssd {
 namespace {
 
 constexpr int kGdnThreads = 256;   // 8 warps
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 constexpr int kVT = 32;            // V columns per CTA (one per lane)
 constexpr int kWarps = kGdnThreads / 32;
 
@@ -101,6 +105,32 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
         }
         stage_transposed<C>(w, wT, b, T, t0, nt, H, hh, K);
         if ((int)threadIdx.x < C) gs[threadIdx.x] = (int)threadIdx.x < nt ? g[(int64_t)(b * T + t0 + threadIdx.x) * H + hh] : 0.f;
+        // this thread's u values for (2), issued with the staging loads
+        float uv[4][2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * tt + r;
+            const int64_t row = (int64_t)(b * T + t0 + t) * H + hh;
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int v = v0 + 2 * tv2 + q2;
+                uv[r][q2] = (4 * tt < C && t < nt && v < V) ? __ldg(u + row * V + v) : 0.f;
+            }
+        }
+        // the next chunk's rows of k, w, u and g into L2 while this one is computed
+        if (c + 1 < NT) {
+            const int tn0 = t0 + C, ntn = min(C, T - tn0);
+            const int kl = (K + 31) / 32;           // 128-byte lines of a k or w row
+            const int per = 2 * kl + 2;
+            for (int i = threadIdx.x; i < ntn * per; i += kGdnThreads) {
+                const int t = i / per, j = i - t * per;
+                const int64_t row = (int64_t)(b * T + tn0 + t) * H + hh;
+                const float* ptr = j < kl ? k + row * K + 32 * j
+                                 : j < 2 * kl ? w + row * K + 32 * (j - kl)
+                                 : j == 2 * kl ? u + row * V + v0 : g + row;
+                prefetch_l2(ptr);
+            }
+        }
         __syncthreads();
         // (1) the chunk-start state
         float* hc = h + (((int64_t)bh * NT + c) * K) * V;
@@ -130,7 +160,7 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         const int v = v0 + 2 * tv2 + q;
-                        const float vn = v < V ? u[row * V + v] - a[r][q] : 0.f;
+                        const float vn = v < V ? uv[r][q] - a[r][q] : 0.f;
                         if (v < V) v_new[row * V + v] = vn;
                         vg[t * kVT + 2 * tv2 + q] = vn * gate;
                     }
