@@ -1,0 +1,65 @@
+"""The number of this library's kernels one ssd_fwd launches, as seen by the
+CUDA profiler, equals the count bench.py reports as ``gpu_launches`` per step
+(``launches_per_step``): three for bf16, five when fwd_pass_state takes its
+two-pass form for long chains, four for fp32 (chunk products and scan)."""
+import re
+
+import pytest
+import torch
+
+import bench
+import state_space_sequence_chunk_gb300 as ssd
+from state_space_sequence_chunk_gb300 import synth
+from harness import small, to_device
+
+pytestmark = pytest.mark.gpu
+
+OURS = re.compile(r"chunk_cumsum_kernel|fwd_pass_state|fps_chunk_products|fps_state_scan|"
+                  r"compute_out_(tc|simt)")
+
+CASES = {
+    "bf16, short chains": small(seqlen=1000, nheads=4, ngroups=2, headdim=64, dstate=128,
+                                chunk=128, dtype="bf16", batch=2),
+    "bf16, long chains (two passes)": small(seqlen=64 * 64, nheads=2, ngroups=1, headdim=64,
+                                            dstate=128, chunk=64, dtype="bf16", init_std=0.0),
+    "bf16, P = 128 (one-head kernel, CUDA-core compute_out)": small(seqlen=300, headdim=128,
+                                                                     dstate=64, dtype="bf16"),
+    "fp32": small(seqlen=500, headdim=32, dstate=16, chunk=64, dtype="f32"),
+}
+
+
+def _kernel_counts(fn):
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    counts = {}
+    for e in prof.key_averages():
+        counts[e.key] = counts.get(e.key, 0) + e.count
+    return counts
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_launches_per_step_matches_the_profiler(name):
+    w = CASES[name]
+    dev = to_device(synth.make_inputs(w), w.dtype)
+
+    def step():
+        ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                    dev["init_state"], chunk_size=w.chunk)
+
+    step()   # the first call loads the module
+    torch.cuda.synchronize()
+    probe = torch.ones(4, device="cuda")
+    seen = lambda c: any("mul" in k.lower() or "elementwise" in k.lower() for k in c)
+    # the process's first profiling session may start recording late: take a
+    # second one if the first saw not even the probe kernel
+    for _ in range(2):
+        counts = _kernel_counts(lambda: (probe.mul_(2.0), step()))
+        if seen(counts):
+            break
+    if not seen(counts):
+        pytest.skip("the profiler records no CUDA kernels here")
+    ours = sum(n for k, n in counts.items() if OURS.search(k))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ours == bench.launches_per_step(w, sms), counts
