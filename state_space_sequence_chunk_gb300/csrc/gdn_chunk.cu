@@ -64,6 +64,11 @@ __device__ __forceinline__ void stage_transposed(const float* __restrict__ src, 
     }
 }
 
+// chunk_fwd_h: the chunk walk is software-pipelined.  A chunk's rows of k and
+// w, its g values and this thread's u values are loaded into registers while
+// the previous chunk's state update (4)-(5) runs, and stored into shared
+// memory once that update no longer reads k; the L2 prefetch one chunk further
+// ahead turns those loads into L2 hits.
 template <int C>
 __global__ void __launch_bounds__(kGdnThreads)
 gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
@@ -83,30 +88,25 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
     // thread maps: (2) 4 tokens x 2 columns; (4)(5) 4 state rows x 4 columns
     const int tt = threadIdx.x >> 4, tv2 = threadIdx.x & 15;
     const int tk = threadIdx.x >> 3, tv4 = threadIdx.x & 7;
-    for (int kk = warp; kk < K; kk += kWarps)
-        S[kk * kVT + lane] = (h0 != nullptr && v0 + lane < V) ? h0[((int64_t)bh * K + kk) * V + v0 + lane] : 0.f;
-    for (int c = 0; c < NT; ++c) {
+
+    // registers of the chunk being loaded
+    float4 kv[kMaxVecPerThread], wv[kMaxVecPerThread];
+    float uv[4][2], gv = 0.f;
+    auto issue = [&](int c) {   // loads of chunk c
         const int t0 = c * C, nt = min(C, T - t0);
-        __syncthreads();   // the previous chunk's readers are done
-        {
-            float4 v[kMaxVecPerThread];
 #pragma unroll
-            for (int r = 0; r < kMaxVecPerThread; ++r) {
-                const int i = threadIdx.x + r * kGdnThreads, t = i / K4, k4 = i - t * K4;
-                v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < C * K4 && t < nt)
-                    v[r] = __ldg(reinterpret_cast<const float4*>(k + ((int64_t)(b * T + t0 + t) * H + hh) * K) + k4);
-            }
-#pragma unroll
-            for (int r = 0; r < kMaxVecPerThread; ++r) {
-                const int i = threadIdx.x + r * kGdnThreads;
-                if (i < C * K4) reinterpret_cast<float4*>(ks)[i] = v[r];
-            }
+        for (int r = 0; r < kMaxVecPerThread; ++r) {
+            const int i = threadIdx.x + r * kGdnThreads;
+            const int tk_ = i / K4, k4 = i - tk_ * K4;      // k: row-major
+            kv[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < C * K4 && tk_ < nt)
+                kv[r] = __ldg(reinterpret_cast<const float4*>(k + ((int64_t)(b * T + t0 + tk_) * H + hh) * K) + k4);
+            const int tw = i % C, kw4 = i / C;              // w: transposed below
+            wv[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < C * K4 && tw < nt)
+                wv[r] = __ldg(reinterpret_cast<const float4*>(w + ((int64_t)(b * T + t0 + tw) * H + hh) * K) + kw4);
         }
-        stage_transposed<C>(w, wT, b, T, t0, nt, H, hh, K);
-        if ((int)threadIdx.x < C) gs[threadIdx.x] = (int)threadIdx.x < nt ? g[(int64_t)(b * T + t0 + threadIdx.x) * H + hh] : 0.f;
-        // this thread's u values for (2), issued with the staging loads
-        float uv[4][2];
+        gv = ((int)threadIdx.x < nt) ? __ldg(g + (int64_t)(b * T + t0 + threadIdx.x) * H + hh) : 0.f;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 4 * tt + r;
@@ -117,7 +117,7 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
                 uv[r][q2] = (4 * tt < C && t < nt && v < V) ? __ldg(u + row * V + v) : 0.f;
             }
         }
-        // the next chunk's rows of k, w, u and g into L2 while this one is computed
+        // chunk c + 1 into L2
         if (c + 1 < NT) {
             const int tn0 = t0 + C, ntn = min(C, T - tn0);
             const int kl = (K + 31) / 32;           // 128-byte lines of a k or w row
@@ -131,7 +131,30 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
                 prefetch_l2(ptr);
             }
         }
-        __syncthreads();
+    };
+    auto commit = [&]() {       // the loaded chunk into shared memory
+#pragma unroll
+        for (int r = 0; r < kMaxVecPerThread; ++r) {
+            const int i = threadIdx.x + r * kGdnThreads;
+            if (i < C * K4) {
+                reinterpret_cast<float4*>(ks)[i] = kv[r];
+                const int tw = i % C, kw4 = i / C;
+                wT[(4 * kw4 + 0) * CP + tw] = wv[r].x;
+                wT[(4 * kw4 + 1) * CP + tw] = wv[r].y;
+                wT[(4 * kw4 + 2) * CP + tw] = wv[r].z;
+                wT[(4 * kw4 + 3) * CP + tw] = wv[r].w;
+            }
+        }
+        if ((int)threadIdx.x < C) gs[threadIdx.x] = gv;
+    };
+
+    if (NT > 0) issue(0);
+    for (int kk = warp; kk < K; kk += kWarps)
+        S[kk * kVT + lane] = (h0 != nullptr && v0 + lane < V) ? h0[((int64_t)bh * K + kk) * V + v0 + lane] : 0.f;
+    if (NT > 0) commit();
+    for (int c = 0; c < NT; ++c) {
+        const int t0 = c * C, nt = min(C, T - t0);
+        __syncthreads();   // chunk c is in shared memory; S is up to date
         // (1) the chunk-start state
         float* hc = h + (((int64_t)bh * NT + c) * K) * V;
         if (v0 + lane < V)
@@ -142,9 +165,9 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
             float a[4][2] = {};
             #pragma unroll 4
             for (int kk = 0; kk < K; ++kk) {
-                const float4 wv = *reinterpret_cast<const float4*>(wT + kk * CP + 4 * tt);
+                const float4 wq = *reinterpret_cast<const float4*>(wT + kk * CP + 4 * tt);
                 const float2 sv = *reinterpret_cast<const float2*>(S + kk * kVT + 2 * tv2);
-                const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
+                const float wr[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     a[r][0] = fmaf(wr[r], sv.x, a[r][0]);
@@ -170,7 +193,8 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
                 }
             }
         }
-        __syncthreads();
+        __syncthreads();   // vg is complete; S and wT are no longer read
+        if (c + 1 < NT) issue(c + 1);   // in flight during (4)-(5)
         // (4) decay and (5) S += k^T v_gated for state rows 4 tk .. 4 tk + 3, columns 4 tv4 ..
         if (4 * tk < K) {
             const float decay = expf(g_last);
@@ -182,9 +206,9 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
             }
             #pragma unroll 4
             for (int t = 0; t < nt; ++t) {
-                const float4 kv = *reinterpret_cast<const float4*>(ks + t * K + 4 * tk);
+                const float4 kq = *reinterpret_cast<const float4*>(ks + t * K + 4 * tk);
                 const float4 xv = *reinterpret_cast<const float4*>(vg + t * kVT + 4 * tv4);
-                const float kr[4] = {kv.x, kv.y, kv.z, kv.w}, xr[4] = {xv.x, xv.y, xv.z, xv.w};
+                const float kr[4] = {kq.x, kq.y, kq.z, kq.w}, xr[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -194,6 +218,10 @@ gdn_fwd_h_kernel(const float* __restrict__ k, const float* __restrict__ w,
 #pragma unroll
             for (int r = 0; r < 4; ++r)
                 *reinterpret_cast<float4*>(S + (4 * tk + r) * kVT + 4 * tv4) = make_float4(a[r][0], a[r][1], a[r][2], a[r][3]);
+        }
+        if (c + 1 < NT) {
+            __syncthreads();   // every read of ks, gs and vg for chunk c is done
+            commit();
         }
     }
     __syncthreads();
