@@ -57,3 +57,18 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(12.5, 1) == 12.5
     assert bench.job_throughput(1, 1000, 2.0) == pytest.approx(5e5)
+
+
+def test_launches_per_step_by_workload():
+    """The per-step launch count bench.py reports: three kernels for bf16, five
+    when fwd_pass_state takes its two-pass form (long chains: at least 64
+    chunks and at most half a chain per range), four for fp32."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from state_space_sequence_chunk_gb300 import synth
+    W = synth.WORKLOADS
+    assert bench.launches_per_step(W["mamba2_layer_bf16"], 152) == 3     # 16 chunks per chain
+    assert bench.launches_per_step(W["short_streams_bf16"], 152) == 3    # 4 chunks per chain
+    assert bench.launches_per_step(W["long_context_bf16"], 152) == 5     # 256 chunks, 12 chains
+    assert bench.launches_per_step(W["tiny_fp32"], 152) == 4
+    assert bench.launches_per_step(W["small_fp32"], 152) == 4
