@@ -274,8 +274,8 @@ int ssd_oracle_causal_conv1d(int64_t batch, int64_t dim, int64_t seqlen, int64_t
 }
 
 /*
- * Gated DeltaNet chunk kernels -- the survey's NEXT-3 workload, a second
- * chunked recurrence with the shape of fwd_pass_state / compute_out.
+ * Gated DeltaNet chunk kernels -- a second chunked recurrence with the shape
+ * of fwd_pass_state / compute_out.
  *
  * [P3] Helion hackathon gallery, the "GDN chunk_fwd_h" and "GDN chunk_fwd_o"
  * entries, chunk size C.  Layouts: k, w, q [B, T, H, K]; u, v_new, o
