@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 3
+#define SSD_ABI_VERSION 4
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
@@ -310,6 +310,53 @@ ssd_status ssd_gdn_chunk_fwd_o(const ssd_gdn_dims* d, const float* q, const floa
 ssd_status ssd_fwd_noalloc(const ssd_dims* d, const void* x, const float* dt, const float* A,
                            const void* B, const void* C, const float* D,
                            const float* init_state, void* y, float* final_state, void* stream);
+
+/* Device bytes ssd_fwd_host needs as `staging` for `d` cut into `nslices`
+ * batch slices (1 <= nslices <= min(batch, 64)); 0 if `d` or nslices is
+ * invalid or the batch is empty. */
+size_t ssd_fwd_host_staging_bytes(const ssd_dims* d, int nslices);
+
+/*
+ * ssd_fwd_host -- ssd_fwd on host buffers, with the host-device copies of one
+ * part of the batch overlapping the computation of another.
+ *
+ * The batch is cut into nslices contiguous slices of ceil(batch / nslices)
+ * elements (the last may be shorter).  For each slice in turn: its inputs are
+ * copied to the device on streams[1], ssd_fwd runs on it on streams[0], and
+ * its y and final_state are copied back on streams[2].  Two staging slots
+ * alternate, so slice k + 1's inputs travel while slice k is computed and
+ * slice k - 1's outputs travel back.  Every (batch, head) is an independent
+ * recurrence, so each slice is an ssd_fwd problem of its own; its arithmetic
+ * per (batch, head) is that of ssd_fwd on the slice.
+ *
+ *   d, A, D, and the meaning and layout of every tensor: as ssd_fwd, but x,
+ *     dt, A, B, C, D, init_state, y and final_state are HOST pointers.  They
+ *     should be page-locked (cudaHostAlloc, or pinned by the caller's
+ *     framework): pageable memory makes each copy synchronous and removes the
+ *     overlap.  final_state may be init_state itself (updated in place); other
+ *     overlaps of an output with an input give SSD_ERR_ALIAS.
+ *   staging     device buffer, 256-byte aligned, of at least
+ *               ssd_fwd_host_staging_bytes(d, nslices) bytes: two slots, each
+ *               with the device copies of one slice's tensors and its ssd_fwd
+ *               workspace, and A and D.  Caller-owned.
+ *   nslices     1 <= nslices <= min(batch, 64) (else SSD_ERR_SHAPE).
+ *   streams     three cudaStream_t values: compute (the caller's stream),
+ *               copy-in and copy-out.  They may coincide (the work then runs
+ *               in order without overlap).
+ * Ordering: the copies start after the work enqueued on streams[0] before the
+ * call; the call makes streams[0] wait for its last copy, so work enqueued on
+ * streams[0] after the call (or a synchronisation of it) sees y and
+ * final_state complete in host memory.  The call returns once everything is
+ * enqueued.  It creates and releases CUDA events; it allocates no memory.
+ * Errors: the validation of ssd_fwd, plus SSD_ERR_WORKSPACE (staging too
+ * small), SSD_ERR_ALIGN (staging), SSD_ERR_NULL, SSD_ERR_CUDA (a copy or an
+ * event failed; the work already enqueued still completes before streams[0]
+ * moves on).
+ */
+ssd_status ssd_fwd_host(const ssd_dims* d, const void* x, const float* dt, const float* A,
+                        const void* B, const void* C, const float* D, const float* init_state,
+                        void* y, float* final_state, void* staging, size_t staging_bytes,
+                        int nslices, void* const* streams);
 
 #ifdef __cplusplus
 }

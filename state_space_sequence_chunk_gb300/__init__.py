@@ -34,7 +34,8 @@ EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
            "ssd_fwd_pass_state_scratch_bytes", "ssd_compute_out", "ssd_fwd_noalloc",
            "ssd_take_device_errors", "ssd_debug_withhold_handoffs", "ssd_step",
-           "ssd_causal_conv1d", "ssd_gdn_chunk_fwd_h", "ssd_gdn_chunk_fwd_o"]
+           "ssd_causal_conv1d", "ssd_gdn_chunk_fwd_h", "ssd_gdn_chunk_fwd_o",
+           "ssd_fwd_host_staging_bytes", "ssd_fwd_host"]
 
 
 class SSDError(RuntimeError):
@@ -110,6 +111,10 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_gdn_chunk_fwd_h.restype = ctypes.c_int
         lib.ssd_gdn_chunk_fwd_o.argtypes = [ctypes.POINTER(GdnDims)] + [vp] * 7
         lib.ssd_gdn_chunk_fwd_o.restype = ctypes.c_int
+        lib.ssd_fwd_host_staging_bytes.argtypes = [dp, ctypes.c_int]
+        lib.ssd_fwd_host_staging_bytes.restype = sz
+        lib.ssd_fwd_host.argtypes = [dp] + [vp] * 10 + [sz, ctypes.c_int, ctypes.POINTER(vp)]
+        lib.ssd_fwd_host.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -193,6 +198,61 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_size: int = 256,
     _check(lib.ssd_fwd(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                        _ptr(init_state), _ptr(y), _ptr(fin), _ptr(workspace),
                        ctypes.c_size_t(workspace.numel()), _stream()))
+    return y, fin
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors must be contiguous host (CPU) tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_copy_streams = {}
+
+
+def ssd_fwd_host_staging_bytes(dims: Dims, nslices: int) -> int:
+    return int(load_library().ssd_fwd_host_staging_bytes(ctypes.byref(dims), int(nslices)))
+
+
+def ssd_fwd_host(x, dt, A, B, C, D=None, init_state=None, chunk_size: int = 256,
+                 return_final_state: bool = True, nslices: int = None, staging=None, out=None,
+                 final_out=None, device=None):
+    """ssd_fwd on HOST tensors (pinned, for the copies to overlap): the batch is
+    cut into ``nslices`` slices whose host-device copies overlap the other
+    slices' computation.  The compute runs on torch's current stream of
+    ``device`` (default: the current CUDA device); two copy streams are kept
+    per device.  Returns host tensors ``(y, final_state)``; they are complete
+    once that stream has reached the end of the call (synchronise it before
+    reading them).  ``staging`` (uint8 CUDA tensor) may be given to reuse it.
+    """
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    dims = dims_for(x, B, chunk_size)
+    b = x.shape[0]
+    if nslices is None:
+        nslices = max(1, min(b, 4))
+    y = out if out is not None else torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    fin = None
+    if return_final_state:
+        fin = final_out if final_out is not None else torch.empty(
+            (b, x.shape[2], x.shape[3], B.shape[3]), dtype=torch.float32, pin_memory=True)
+    if b == 0:
+        return y, fin
+    nbytes = ssd_fwd_host_staging_bytes(dims, nslices)
+    if staging is None:
+        staging = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        if dev.index not in _copy_streams:
+            _copy_streams[dev.index] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        s_in, s_out = _copy_streams[dev.index]
+        streams = (ctypes.c_void_p * 3)(torch.cuda.current_stream(dev).cuda_stream,
+                                        s_in.cuda_stream, s_out.cuda_stream)
+        _check(lib.ssd_fwd_host(ctypes.byref(dims), _host_ptr(x), _host_ptr(dt), _host_ptr(A),
+                                _host_ptr(B), _host_ptr(C), _host_ptr(D), _host_ptr(init_state),
+                                _host_ptr(y), _host_ptr(fin), _ptr(staging),
+                                ctypes.c_size_t(staging.numel()), int(nslices), streams))
     return y, fin
 
 

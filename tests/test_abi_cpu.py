@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.ssd_abi_version() == 3
+    assert lib.ssd_abi_version() == 4
     for code in range(0, 9):
         s = lib.ssd_status_string(code)
         assert s and s != b"unknown status"
@@ -215,3 +215,36 @@ def test_binding_raises_without_library(tmp_path):
             ssd.load_library(str(tmp_path / "nope.so"))
         finally:
             ssd._lib = saved
+
+
+def test_fwd_host_validation(lib):
+    """ssd_fwd_host rejects bad slices, buffers and overlaps before anything is
+    enqueued (host pointers here are fake and never dereferenced)."""
+    d = dims()
+    b = d.batch
+    a = _fwd_args(10)
+    streams = (ctypes.c_void_p * 3)(None, None, None)
+    need = lib.ssd_fwd_host_staging_bytes(ctypes.byref(d), min(b, 2))
+    assert need > 0
+    assert lib.ssd_fwd_host_staging_bytes(ctypes.byref(d), 0) == 0
+    assert lib.ssd_fwd_host_staging_bytes(ctypes.byref(d), b + 1) == 0
+    assert lib.ssd_fwd_host_staging_bytes(ctypes.byref(d), 65) == 0
+    args = a[:9] + [a[9], ctypes.c_size_t(need)]
+    host = lambda *v: lib.ssd_fwd_host(ctypes.byref(d), *v)
+    assert host(*args, 0, streams) == 2                     # nslices < 1
+    assert host(*args, b + 1, streams) == 2                 # more slices than batch elements
+    assert host(*args, 1, None) == 1                        # no streams
+    small = a[:9] + [a[9], ctypes.c_size_t(need - 1)]
+    assert host(*small, min(b, 2), streams) == 5            # staging too small
+    odd = a[:9] + [ctypes.c_void_p(a[9].value + 16), ctypes.c_size_t(need)]
+    assert host(*odd, min(b, 2), streams) == 4              # staging not 256-byte aligned
+    over = list(args); over[7] = ctypes.c_void_p(a[0].value + 64)   # y inside x
+    assert host(*over, min(b, 2), streams) == 8
+    # the last slice may hold fewer batch elements: its workspace fits the slot's
+    for L in (300, 64 * 128):          # single pass, and a two-pass candidate
+        for bb in range(1, 9):
+            for nb in range(1, bb):
+                lo, hi = dims(seqlen=L), dims(seqlen=L)
+                lo.batch, hi.batch = nb, bb
+                assert lib.ssd_fwd_workspace_bytes(ctypes.byref(lo)) <= \
+                    lib.ssd_fwd_workspace_bytes(ctypes.byref(hi))
