@@ -17,7 +17,8 @@
  * Conventions for every entry point
  * ---------------------------------
  *  - All tensor pointers are DEVICE pointers (the current CUDA device), to
- *    contiguous row-major arrays in the layouts given below, 16-byte aligned.
+ *    contiguous row-major arrays in the layouts given below, 16-byte aligned
+ *    (except ssd_fwd_host, whose tensors are in host memory).
  *    The caller owns every buffer; the library allocates no device memory and
  *    keeps no per-call state.  Inputs are only read.
  *  - Letters: b = batch, L = seqlen, H = nheads, P = headdim, N = dstate,
