@@ -72,3 +72,15 @@ def test_launches_per_step_by_workload():
     assert bench.launches_per_step(W["long_context_bf16"], 152) == 5     # 256 chunks, 12 chains
     assert bench.launches_per_step(W["tiny_fp32"], 152) == 4
     assert bench.launches_per_step(W["small_fp32"], 152) == 4
+
+
+def test_cpu_baseline_reports_one_core_and_all_cores():
+    """bench.py's cpu_baseline: the oracle on one core and on every core, each
+    projected to the whole workload, with the thread count it used."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from state_space_sequence_chunk_gb300 import synth
+    w = synth.WORKLOADS["tiny_fp32"]
+    r = bench.cpu_baseline(w, synth.make_inputs(w), 0.5)
+    assert r["kind"] == "oracle" and r["cores"] == 1 and r["value"] > 0
+    assert r["all_cores"]["cores"] == (os.cpu_count() or 1) and r["all_cores"]["value"] > 0
