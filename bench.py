@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=list(synth.WORKLOADS) + list(synth.CONTEXT_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -687,7 +688,7 @@ def main():
         return conv1d_main(args)
     if args.gdn:
         return gdn_main(args)
-    w = synth.WORKLOADS[args.workload]
+    w = synth.workload(args.workload)
     if args.impl == "reference":
         return reference_arm(args, w)
 

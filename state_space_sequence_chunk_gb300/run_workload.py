@@ -21,11 +21,12 @@ from state_space_sequence_chunk_gb300 import synth
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", default="mamba2_layer_bf16", choices=list(synth.WORKLOADS))
+    ap.add_argument("--workload", default="mamba2_layer_bf16",
+                    choices=list(synth.WORKLOADS) + list(synth.CONTEXT_WORKLOADS))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")
     args = ap.parse_args(argv)
-    w = synth.WORKLOADS[args.workload]
+    w = synth.workload(args.workload)
     Q = args.chunk or w.chunk
     inp = synth.make_inputs(w)
     dev = torch.device("cuda")

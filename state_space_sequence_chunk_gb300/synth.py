@@ -139,6 +139,23 @@ WORKLOADS = {
 }
 
 
+# Context shape beside the five: the pages' own example problem ("Accelerating
+# Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA CUDA Tile",
+# section "Mamba-2 Forward Pass Benchmarks: cuTile vs Triton on NVIDIA B300":
+# batch 4, 16384 tokens, 1 group, 8 heads, state 128, head 64, chunk 128, bf16
+# with an fp32 state).  The page does not print how its sample inputs are
+# drawn; they follow the recipe above, with a zero initial state.
+CONTEXT_WORKLOADS = {
+    "pages_example_bf16": Workload("pages_example_bf16", 4, 16384, 8, 64, 128, 1, 128, "bf16",
+                                   seed=20261202 + 5),
+}
+
+
+def workload(name: str) -> Workload:
+    """A workload of either table by name."""
+    return WORKLOADS[name] if name in WORKLOADS else CONTEXT_WORKLOADS[name]
+
+
 def make_inputs(w: Workload) -> dict:
     """Draw every input of workload ``w``.
 

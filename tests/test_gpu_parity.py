@@ -139,6 +139,22 @@ def test_workload(name):
     assert np.all(np.isfinite(y))
 
 
+def test_pages_example_shape():
+    """The pages' own example problem (b4, 16384 tokens, H8, P64, N128, G1,
+    chunk 128, bf16): 128 chunks per chain, so fwd_pass_state takes its
+    two-pass form; sampled (batch, head) slices against the oracle."""
+    w = synth.CONTEXT_WORKLOADS["pages_example_bf16"]
+    inp = synth.make_inputs(w)
+    y, fin = gpu_fwd(to_device(inp, w.dtype), w.chunk)
+    bh = [(0, 0), (1, 3), (3, 7)]
+    refs = oracle_fwd(inp, bh=bh)
+    ey = rel_err(np.stack([y[b, :, h] for b, h in bh]), np.stack([r[0][0, :, 0] for r in refs]))
+    ef = rel_err(np.stack([fin[b, h] for b, h in bh]), np.stack([r[1][0, 0] for r in refs]))
+    print(f"\npages_example_bf16: y rel err {ey:.3e}, final_state rel err {ef:.3e}")
+    assert ey < TOL["bf16"] and ef < TOL["bf16"]
+    assert np.all(np.isfinite(y))
+
+
 # --- properties -----------------------------------------------------------------
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
