@@ -40,8 +40,21 @@
  *    enqueued; on an error the call returns a status != SSD_OK and launches
  *    nothing.  A failure reported by the CUDA runtime while enqueuing returns
  *    SSD_ERR_CUDA.  Nothing throws across this ABI.
+ *  - Timeouts: every wait inside the tensor-core kernels (on a pipeline
+ *    barrier, or on the state that another CTA hands on) is bounded, about
+ *    1 s of SM clock; a wait that gives up ends its kernel early, with
+ *    undefined outputs, instead of hanging the GPU.  Calls are asynchronous,
+ *    so such a failure cannot be returned by the call that enqueued it: the
+ *    kernel raises a page-locked host word at its end, and the FIRST launching
+ *    call on that device that starts after the failed kernel has finished
+ *    returns SSD_ERR_TIMEOUT (after validating its arguments) and enqueues
+ *    nothing.  Reporting it synchronises the device and clears the record, so
+ *    the call after that runs normally.  ssd_take_device_errors() reads and
+ *    clears the same record on demand.  The first launching call in a process
+ *    page-locks that host word once (make it before any stream capture); if
+ *    that fails, only ssd_take_device_errors() reports timeouts.
  *  - Supported sizes: dtype SSD_F32 or SSD_BF16 (x, B, C, y share it);
- *    Q in {64, 128, 256}; P in {16, 32, ..., 128} (multiple of 16);
+ *    Q in {64, 128, 256}; P in {16, 32, ..., 256} (multiple of 16);
  *    N in {16, 32, ..., 256} (multiple of 16); H % G == 0; batch >= 0 and
  *    seqlen >= 0 (an empty problem enqueues at most a copy of init_state to
  *    final_state).  The device must be compute capability 10.3.
@@ -56,7 +69,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 4
+#define SSD_ABI_VERSION 5
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
@@ -69,7 +82,8 @@ typedef enum {
     SSD_ERR_WORKSPACE = 5,  /* workspace smaller than ssd_fwd_workspace_bytes()   */
     SSD_ERR_ARCH = 6,       /* the current device is not compute capability 10.3  */
     SSD_ERR_CUDA = 7,       /* the CUDA runtime reported an error                 */
-    SSD_ERR_ALIAS = 8       /* an output overlaps an input                        */
+    SSD_ERR_ALIAS = 8,      /* an output overlaps an input                        */
+    SSD_ERR_TIMEOUT = 9     /* a bounded wait in an earlier launch gave up        */
 } ssd_status;
 
 /* Problem sizes.  `dtype` is an ssd_dtype: the element type of x, B, C, y and
@@ -166,11 +180,11 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
 
 /*
  * ssd_take_device_errors -- read and clear the device-side error words of the
- * tensor-core kernels.  Every wait inside those kernels is bounded; a wait
- * that gives up (it never should) sets a bit and the kernel ends early with
- * undefined output instead of hanging.  Bit 0: fwd_pass_state, bit 1:
- * compute_out.  Synchronises the current device; returns 0xFFFFFFFF if the
- * words cannot be read.
+ * tensor-core kernels (and the host record behind SSD_ERR_TIMEOUT).  Every
+ * wait inside those kernels is bounded; a wait that gives up (it never should)
+ * sets a bit and the kernel ends early with undefined output instead of
+ * hanging.  Bit 0: fwd_pass_state, bit 1: compute_out.  Synchronises the
+ * current device; returns 0xFFFFFFFF if the words cannot be read.
  */
 unsigned int ssd_take_device_errors(void);
 

@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libssd.so")
 SSD_F32, SSD_BF16 = 0, 1
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE",
           4: "SSD_ERR_ALIGN", 5: "SSD_ERR_WORKSPACE", 6: "SSD_ERR_ARCH", 7: "SSD_ERR_CUDA",
-          8: "SSD_ERR_ALIAS"}
+          8: "SSD_ERR_ALIAS", 9: "SSD_ERR_TIMEOUT"}
 EXPORTS = ["ssd_abi_version", "ssd_status_string", "ssd_fwd_workspace_bytes",
            "ssd_intermediate_bytes", "ssd_fwd", "ssd_chunk_cumsum", "ssd_fwd_pass_state",
            "ssd_fwd_pass_state_scratch_bytes", "ssd_compute_out", "ssd_fwd_noalloc",

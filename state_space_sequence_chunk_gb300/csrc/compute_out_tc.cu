@@ -127,7 +127,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_h,
                const float* __restrict__ Gcs, const float* __restrict__ dtT,
                const float* __restrict__ D, __nv_bfloat16* __restrict__ y, int L, int H, int P,
-               int nc, int Lp, int hpg, int units) {
+               int nc, int Lp, int hpg, int units, unsigned int* host_err) {
     using Cfg = CoCfg<Q>;
     constexpr int NST = Cfg::kStages;
     constexpr int NCB = Cfg::kCBufs;
@@ -598,6 +598,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     }
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) report_timeout_to_host(err, host_err);
     if (warp == 1) {
         __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
         tc_fence_after();
@@ -650,7 +651,8 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     cfg.attrs = attr;
     cfg.numAttrs = p.chained ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, tx, tc, tb, th, Gcs, dtT, D, (__nv_bfloat16*)y, (int)p.L,
-                           (int)p.H, (int)p.P, (int)p.nc, (int)p.Lp, (int)p.hpg, (int)units);
+                           (int)p.H, (int)p.P, (int)p.nc, (int)p.Lp, (int)p.hpg, (int)units,
+                           host_timeout_word());
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

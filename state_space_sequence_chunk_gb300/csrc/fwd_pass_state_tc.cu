@@ -103,6 +103,7 @@ struct FpsParams {
     int nmb, npb, nchains;   // row blocks of N, column blocks of P, chains
     int W;                   // work units: nchains * nc (< 2^31, checked on the host)
     int G;                   // CTAs (ranges)
+    unsigned int* host_err;  // page-locked host word raised when a wait gave up (may be NULL)
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -611,6 +612,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     }
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) report_timeout_to_host(&g_fps_error, q.host_err);
     if (warp == 1) {
         __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
         tc_fence_after();
@@ -1092,6 +1094,7 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     __syncwarp();   // lanes that skipped a role loop wait for its lane 0
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) report_timeout_to_host(&g_fps_error, q.host_err);
     if (warp == 1) {
         __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
         tc_fence_after();
@@ -1250,6 +1253,7 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     q.nmb = (int)((p.N + 127) / 128);
     q.npb = (int)((p.P + 63) / 64);
     q.nchains = (int)chains(p);
+    q.host_err = host_timeout_word();
     if ((int64_t)q.nchains * p.nc >= (int64_t)1 << 31) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.stream = stream;

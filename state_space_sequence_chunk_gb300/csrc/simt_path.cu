@@ -124,7 +124,8 @@ fps_state_scan(const float* __restrict__ Gcs, const float* init, float* __restri
 
 // ---------------------------------------------------------------------------
 // compute_out: one CTA per (32 query rows, chunk, batch*head).  Thread t owns
-// row i = t / 8 and columns p = t % 8 + 8 k.
+// row i = t / 8 and columns p = t % 8 + 8 k, k < KP (KP = 16 covers P <= 128,
+// KP = 32 covers P <= 256).
 //   acc = 2^{g_i} (C_i . h^T)
 //   for each 32-token key block j <= i:
 //       cb[i][j] = C_i . B_j, masked to j <= i and scaled by 2^{g_i - g_j} dt_j
@@ -135,7 +136,7 @@ fps_state_scan(const float* __restrict__ Gcs, const float* init, float* __restri
 // ---------------------------------------------------------------------------
 constexpr int kRows = 32;
 
-template <typename T>
+template <typename T, int KP>
 __global__ void __launch_bounds__(kThreads)
 compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __restrict__ C,
                  const float* __restrict__ Gcs, const float* __restrict__ dtT,
@@ -166,9 +167,9 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
         cs[r * NS + n] = tg < L ? to_f32(C[(((int64_t)bidx * L + tg) * G + grp) * N + n]) : 0.f;
     }
 
-    float acc[16];
+    float acc[KP];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    for (int k = 0; k < KP; ++k) acc[k] = 0.f;
 
     // state term C_i . h^T, h staged 32 state columns at a time
     const T* hbase = hiddens + (((int64_t)bidx * H + h) * nc + c) * (int64_t)P * N;
@@ -186,7 +187,7 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
         for (int nn = 0; nn < nlim; ++nn) {
             const float cv = cs[il * NS + n0 + nn];
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
+            for (int k = 0; k < KP; ++k)
                 if (k < pper) acc[k] = fmaf(cv, hs[(pl + 8 * k) * 33 + nn], acc[k]);
         }
     }
@@ -194,7 +195,7 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
     {
         const float sgi = exp2f(gq[irow]);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] *= sgi;
+        for (int k = 0; k < KP; ++k) acc[k] *= sgi;
     }
 
     // intra-chunk term, key blocks j0 <= i0
@@ -225,7 +226,7 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
         for (int jl = 0; jl < kRows; ++jl) {
             const float w = cb[il * 33 + jl];
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
+            for (int k = 0; k < KP; ++k)
                 if (k < pper) acc[k] = fmaf(w, xs[jl * P + pl + 8 * k], acc[k]);
         }
     }
@@ -235,7 +236,7 @@ compute_out_simt(const T* __restrict__ x, const T* __restrict__ B, const T* __re
         const float dv = D ? D[h] : 0.f;
         const int64_t base = (((int64_t)bidx * L + tg) * H + h) * P;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < KP; ++k) {
             if (k < pper) {
                 const int pp = pl + 8 * k;
                 y[base + pp] = from_f32<T>(acc[k] + dv * to_f32(x[base + pp]));
@@ -269,7 +270,7 @@ cudaError_t launch_co(const Problem& p, const void* x, const void* B, const void
     const int NS = (int)p.N + 1;
     const size_t smem = (size_t)(2 * kRows * NS + p.P * 33 + kRows * p.P + kRows * 33 + 2 * p.Q) *
                         sizeof(float);
-    auto kern = compute_out_simt<T>;
+    auto kern = p.P > 128 ? compute_out_simt<T, 32> : compute_out_simt<T, 16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.Q / kRows), (unsigned)p.nc, (unsigned)(p.b * p.H));

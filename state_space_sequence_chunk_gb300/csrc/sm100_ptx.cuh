@@ -80,6 +80,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     return true;
 }
 
+// Called by one thread at the very end of a launch: if a bounded wait of this
+// kernel's module has given up (its device error word is set), raise the
+// page-locked host word `host_word` (may be NULL), so that the host learns of
+// it without synchronising.
+__device__ __forceinline__ void report_timeout_to_host(const unsigned int* err,
+                                                       unsigned int* host_word) {
+    if (host_word != nullptr && *reinterpret_cast<const volatile unsigned int*>(err) != 0u) {
+        *reinterpret_cast<volatile unsigned int*>(host_word) = 1u;
+        __threadfence_system();
+    }
+}
+
 // ---------------------------------------------------------------------------
 // cp.async (LSU path global -> shared copies, completion on an mbarrier)
 // ---------------------------------------------------------------------------

@@ -2,6 +2,8 @@
 // layout and the three launches, all enqueued on the caller's stream.
 #include <string.h>
 
+#include <mutex>
+
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -21,7 +23,7 @@ ssd_status make_problem(const ssd_dims* d, Problem* p) {
     if (d->batch < 0 || d->seqlen < 0) return SSD_ERR_SHAPE;
     if (d->nheads < 1 || d->ngroups < 1 || d->nheads % d->ngroups != 0) return SSD_ERR_SHAPE;
     if (d->chunk_size != 64 && d->chunk_size != 128 && d->chunk_size != 256) return SSD_ERR_SHAPE;
-    if (d->headdim < 16 || d->headdim > 128 || d->headdim % 16 != 0) return SSD_ERR_SHAPE;
+    if (d->headdim < 16 || d->headdim > 256 || d->headdim % 16 != 0) return SSD_ERR_SHAPE;
     if (d->dstate < 16 || d->dstate > 256 || d->dstate % 16 != 0) return SSD_ERR_SHAPE;
     // keep every element index and grid dimension comfortably inside int range
     if (d->batch > 65535 || d->seqlen > (1LL << 24) || d->nheads > 4096) return SSD_ERR_SHAPE;
@@ -73,7 +75,80 @@ ssd_status from_cuda(cudaError_t e) {
     return SSD_ERR_CUDA;
 }
 
+// One page of host memory, page-locked and mapped into every device's address
+// space on first use: word `dev` is raised by a tensor-core kernel on device
+// `dev` whose bounded wait gave up (report_timeout_to_host), so that the next
+// call learns of it without synchronising.
+constexpr int kMaxTimeoutDevices = 1024;
+alignas(4096) unsigned int g_timeout_page[kMaxTimeoutDevices];
+std::once_flag g_timeout_once;
+unsigned int* g_timeout_dev = nullptr;   // device-usable address of g_timeout_page
+
+unsigned int* timeout_page() {
+    std::call_once(g_timeout_once, [] {
+        if (cudaHostRegister(g_timeout_page, sizeof(g_timeout_page),
+                             cudaHostRegisterPortable | cudaHostRegisterMapped) == cudaSuccess) {
+            void* d = nullptr;
+            if (cudaHostGetDevicePointer(&d, g_timeout_page, 0) == cudaSuccess)
+                g_timeout_dev = static_cast<unsigned int*>(d);
+        }
+        cudaGetLastError();   // a failed registration only disables the early report
+    });
+    return g_timeout_dev;
+}
+
+// Read and clear the kernels' device error words and the host word of the
+// current device; returns the error bits (~0u if they cannot be read).
+unsigned int take_errors() {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return ~0u;
+    }
+    const unsigned int a = take_fwd_pass_state_error(), b = take_compute_out_error();
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxTimeoutDevices)
+        reinterpret_cast<volatile unsigned int*>(g_timeout_page)[dev] = 0u;
+    else
+        cudaGetLastError();
+    if (a == ~0u || b == ~0u) return ~0u;
+    return (a ? 1u : 0u) | (b ? 2u : 0u);
+}
+
+// Checks made after the arguments are validated and before anything is
+// enqueued: the device's compute capability, then whether a bounded wait in
+// an earlier launch on this device has given up (reported once, as
+// SSD_ERR_TIMEOUT; reporting it synchronises the device and clears the record).
+ssd_status pre_launch() {
+    const ssd_status s = check_arch();
+    if (s != SSD_OK) return s;
+    return timeout_pending();
+}
+
 }  // namespace
+
+ssd_status timeout_pending() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SSD_ERR_CUDA;
+    }
+    if (timeout_page() == nullptr || dev < 0 || dev >= kMaxTimeoutDevices) return SSD_OK;
+    if (reinterpret_cast<volatile unsigned int*>(g_timeout_page)[dev] == 0u) return SSD_OK;
+    take_errors();
+    return SSD_ERR_TIMEOUT;
+}
+
+unsigned int* host_timeout_word() {
+    unsigned int* page = timeout_page();
+    int dev = 0;
+    if (page == nullptr || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
+        dev >= kMaxTimeoutDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return page + dev;
+}
+
 }  // namespace ssd
 
 using namespace ssd;
@@ -82,15 +157,7 @@ extern "C" {
 
 int ssd_abi_version(void) { return SSD_ABI_VERSION; }
 
-unsigned int ssd_take_device_errors(void) {
-    if (cudaDeviceSynchronize() != cudaSuccess) {
-        cudaGetLastError();
-        return ~0u;
-    }
-    const unsigned int a = take_fwd_pass_state_error(), b = take_compute_out_error();
-    if (a == ~0u || b == ~0u) return ~0u;
-    return (a ? 1u : 0u) | (b ? 2u : 0u);
-}
+unsigned int ssd_take_device_errors(void) { return take_errors(); }
 
 ssd_status ssd_debug_withhold_handoffs(int on) {
     return from_cuda(set_fwd_pass_state_withhold(on ? 1u : 0u));
@@ -107,6 +174,9 @@ const char* ssd_status_string(ssd_status s) {
         case SSD_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
         case SSD_ERR_CUDA: return "the CUDA runtime reported an error";
         case SSD_ERR_ALIAS: return "an output overlaps an input";
+        case SSD_ERR_TIMEOUT:
+            return "a bounded wait in a kernel of an earlier call gave up; that call's outputs "
+                   "are undefined (nothing was enqueued by this call)";
     }
     return "unknown status";
 }
@@ -147,7 +217,7 @@ ssd_status ssd_chunk_cumsum(const ssd_dims* d, const float* dt, const float* A, 
     for (const Range& r : in)
         if (overlap(r, rng(Gcs, gb)) || overlap(r, rng(dtT, gb))) return SSD_ERR_ALIAS;
     if (overlap(rng(Gcs, gb), rng(dtT, gb))) return SSD_ERR_ALIAS;
-    if ((s = check_arch()) != SSD_OK) return s;
+    if ((s = pre_launch()) != SSD_OK) return s;
     return from_cuda(launch_chunk_cumsum(p, dt, A, Gcs, dtT, nullptr, 0, (cudaStream_t)stream));
 }
 
@@ -163,7 +233,7 @@ ssd_status ssd_fwd_pass_state(const ssd_dims* d, const void* x, const void* B, c
     if (p.L == 0) {
         if (!final_state) return SSD_OK;
         if (!aligned16(final_state) || !aligned16(init_state)) return SSD_ERR_ALIGN;
-        if ((s = check_arch()) != SSD_OK) return s;
+        if ((s = pre_launch()) != SSD_OK) return s;
         cudaError_t e = init_state
             ? (init_state == final_state ? cudaSuccess
                                          : cudaMemcpyAsync(final_state, init_state, sbytes,
@@ -196,7 +266,7 @@ ssd_status ssd_fwd_pass_state(const ssd_dims* d, const void* x, const void* B, c
     for (const Range& r : in)
         if (overlap(r, scr)) return SSD_ERR_ALIAS;
     if (overlap(scr, hid) || overlap(scr, fin)) return SSD_ERR_ALIAS;
-    if ((s = check_arch()) != SSD_OK) return s;
+    if ((s = pre_launch()) != SSD_OK) return s;
     return from_cuda(launch_fwd_pass_state(p, x, B, Gcs, dtT, init_state, hiddens, final_state,
                                            scratch, false, (cudaStream_t)stream));
 }
@@ -219,7 +289,7 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
                         rng(hiddens, hid_bytes(p)), rng(D, (size_t)p.H * 4)};
     for (const Range& r : in)
         if (overlap(r, rng(y, xb))) return SSD_ERR_ALIAS;
-    if ((s = check_arch()) != SSD_OK) return s;
+    if ((s = pre_launch()) != SSD_OK) return s;
     return from_cuda(launch_compute_out(p, x, B, C, Gcs, dtT, hiddens, D, y, (cudaStream_t)stream));
 }
 
@@ -244,7 +314,7 @@ ssd_status ssd_causal_conv1d(const ssd_conv_dims* d, const void* x, const float*
     if (overlap(orr, rng(x, xb)) || overlap(orr, rng(weight, (size_t)(p.dim * p.W) * 4)) ||
         overlap(orr, rng(bias, (size_t)p.dim * 4)))
         return SSD_ERR_ALIAS;
-    ssd_status s = check_arch();
+    ssd_status s = pre_launch();
     if (s != SSD_OK) return s;
     return from_cuda(launch_causal_conv1d(p, x, weight, bias, out, (cudaStream_t)stream));
 }
@@ -287,7 +357,7 @@ ssd_status ssd_gdn_chunk_fwd_h(const ssd_gdn_dims* d, const float* k, const floa
     }
     if (overlap(out[0], out[1]) || overlap(out[0], out[2]) || overlap(out[1], out[2]))
         return SSD_ERR_ALIAS;
-    if ((s = check_arch()) != SSD_OK) return s;
+    if ((s = pre_launch()) != SSD_OK) return s;
     return from_cuda(launch_gdn_fwd_h(p, k, w, u, g, h0, h, v_new, final_state,
                                       (cudaStream_t)stream));
 }
@@ -309,7 +379,7 @@ ssd_status ssd_gdn_chunk_fwd_o(const ssd_gdn_dims* d, const float* q, const floa
                         rng(g, (size_t)(p.B * p.T * p.H) * 4)};
     for (const Range& r : in)
         if (overlap(rng(o, vb), r)) return SSD_ERR_ALIAS;
-    if ((s = check_arch()) != SSD_OK) return s;
+    if ((s = pre_launch()) != SSD_OK) return s;
     return from_cuda(launch_gdn_fwd_o(p, q, k, v_new, h, g, o, (cudaStream_t)stream));
 }
 
@@ -336,7 +406,7 @@ ssd_status ssd_step(const ssd_dims* d, const void* x, const float* dt, const flo
     for (const Range& r : in)
         if (overlap(r, sr) || overlap(r, yr)) return SSD_ERR_ALIAS;
     if (overlap(sr, yr)) return SSD_ERR_ALIAS;
-    if ((s = check_arch()) != SSD_OK) return s;
+    if ((s = pre_launch()) != SSD_OK) return s;
     return from_cuda(launch_ssd_step(p, x, dt, A, B, C, D, state, y, (cudaStream_t)stream));
 }
 
@@ -372,7 +442,7 @@ ssd_status ssd_fwd(const ssd_dims* d, const void* x, const float* dt, const floa
     if (init_state && final_state && init_state != final_state && overlap(in[6], fr))
         return SSD_ERR_ALIAS;
     if (overlap(ws, yr) || overlap(ws, fr) || overlap(yr, fr)) return SSD_ERR_ALIAS;
-    if ((s = check_arch()) != SSD_OK) return s;
+    if ((s = pre_launch()) != SSD_OK) return s;
 
     char* w = (char*)workspace;
     float* Gcs = (float*)w;

@@ -113,6 +113,10 @@ extern "C" ssd_status ssd_fwd_host(const ssd_dims* d, const void* x, const float
         }
         if (hoverlap(yr, fr)) return SSD_ERR_ALIAS;
     }
+    {   // a bounded wait of an earlier launch gave up: report it, enqueue nothing
+        const ssd_status t = ssd::timeout_pending();
+        if (t != SSD_OK) return t;
+    }
 
     const Plan p = plan(d, nslices);
     char* base = (char*)staging;

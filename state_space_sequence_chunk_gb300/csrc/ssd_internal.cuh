@@ -91,6 +91,16 @@ bool compute_out_tc_supports(const Problem& p);
 cudaError_t launch_compute_out_tc(const Problem& p, const void* x, const void* B, const void* C,
                                   const float* Gcs, const float* dtT, const void* hiddens,
                                   const float* D, void* y, cudaStream_t stream);
+// Device-usable address of the current device's page-locked host word through
+// which a tensor-core kernel reports, at its end, that one of its bounded waits
+// gave up (see report_timeout_to_host); NULL if it could not be set up.  The
+// first call page-locks the word (once per process).
+unsigned int* host_timeout_word();
+// SSD_ERR_TIMEOUT if a tensor-core kernel on the current device has raised
+// its host word since the last report (the report synchronises the device and
+// clears the device and host records), else SSD_OK (SSD_ERR_CUDA if the device
+// cannot be queried).
+ssd_status timeout_pending();
 // Read and clear the device-side error word of a kernel module (bit 0: a
 // bounded wait gave up).  Synchronous.
 unsigned int take_fwd_pass_state_error();

@@ -38,8 +38,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.ssd_abi_version() == 4
-    for code in range(0, 9):
+    assert lib.ssd_abi_version() == 5
+    for code in range(0, 10):
         s = lib.ssd_status_string(code)
         assert s and s != b"unknown status"
     assert lib.ssd_status_string(99) == b"unknown status"
@@ -83,12 +83,14 @@ def test_workspace_bytes(lib):
     dodd = dims(seqlen=64 * 128, ngroups=4)   # one head per group: no pairs
     assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(dodd)) == (
         ru(chains_l * 2 * 128 * 64 * 4) + ru((32 + chains_l) * 4))
+    # the largest head and state sizes are accepted (P, N up to 256)
+    assert ssd.ssd_fwd_workspace_bytes(dims(headdim=256, dstate=256)) > 0
     assert ssd.ssd_fwd_workspace_bytes(dims(seqlen=0)) == 0
     assert ssd.ssd_fwd_workspace_bytes(dims(chunk_size=100)) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(chunk_size=96), 2), (dict(headdim=40), 2), (dict(headdim=256), 2),
+    (dict(chunk_size=96), 2), (dict(headdim=40), 2), (dict(headdim=272), 2),
     (dict(dstate=8), 2), (dict(dstate=272), 2), (dict(ngroups=3), 2), (dict(nheads=0), 2),
     (dict(batch=-1), 2), (dict(dtype=5), 3), (dict(reserved=1), 2)])
 def test_bad_shapes_rejected(lib, kw, code):

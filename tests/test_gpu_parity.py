@@ -81,7 +81,10 @@ CASES = [
     ("bf16", 256, 511, 4, 1, 64, 128, False, True),   # ragged, Q = 256
     ("bf16", 256, 4096, 2, 1, 64, 128, True, True),
     ("bf16", 128, 130, 8, 2, 64, 128, True, True),    # 4 heads per group
-    ("bf16", 64, 200, 2, 2, 128, 256, True, True),    # largest P and N
+    ("bf16", 64, 200, 2, 2, 128, 256, True, True),    # P = 128 with the largest N
+    ("bf16", 128, 300, 2, 1, 256, 256, True, True),   # largest P and N
+    ("bf16", 256, 333, 4, 2, 256, 64, False, True),   # largest P, ragged, Q = 256
+    ("f32", 64, 200, 2, 1, 256, 128, True, True),     # largest P, fp32
     ("bf16", 128, 333, 2, 1, 16, 16, True, True),     # smallest P and N
     ("bf16", 64, 150, 2, 1, 48, 48, True, True),      # N splits a warp's state rows
     # no initial state: heads 2k, 2k+1 of one group walk together, sharing B
