@@ -183,8 +183,9 @@ ssd_status ssd_compute_out(const ssd_dims* d, const void* x, const void* B, cons
  * tensor-core kernels (and the host record behind SSD_ERR_TIMEOUT).  Every
  * wait inside those kernels is bounded; a wait that gives up (it never should)
  * sets a bit and the kernel ends early with undefined output instead of
- * hanging.  Bit 0: fwd_pass_state, bit 1: compute_out.  Synchronises the
- * current device; returns 0xFFFFFFFF if the words cannot be read.
+ * hanging.  Bit 0: fwd_pass_state (bf16), bit 1: compute_out (bf16), bit 2:
+ * the TF32 kernels of fp32 inputs.  Synchronises the current device; returns
+ * 0xFFFFFFFF if the words cannot be read.
  */
 unsigned int ssd_take_device_errors(void);
 

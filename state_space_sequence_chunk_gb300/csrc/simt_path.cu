@@ -1,9 +1,13 @@
-// simt_path.cu -- fwd_pass_state and compute_out on the CUDA cores (fp32 FMA).
+// simt_path.cu -- fwd_pass_state and compute_out on the CUDA cores (fp32 FMA),
+// and the dispatch of both steps between these kernels and the tensor-core
+// ones (tcgen05: bf16 in fwd_pass_state_tc.cu / compute_out_tc.cu, TF32 in
+// tf32_path.cu).
 //
 // These are the straightforward tiled forms of steps 2 and 3 of "Accelerating
 // Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA CUDA Tile"
 // (sections "Kernel 2: fwd_pass_state" and "Kernel 3: compute_out"), with all
-// arithmetic in fp32.
+// arithmetic in fp32; they serve the shapes the tensor-core kernels do not
+// (fp32 with N or P above 128, bf16 compute_out with P > 64 or N > 128).
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -249,14 +253,21 @@ cudaError_t launch_fps(const Problem& p, const void* x, const void* B, const flo
                       const float* dtT, const float* init, void* hid, float* fin,
                       cudaStream_t stream) {
     const size_t smem = (size_t)(kSub * kPT + kSub * p.N + kSub) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(fps_chunk_products, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    fps_chunk_products<<<dim3((unsigned)(p.P / kPT), (unsigned)p.nc, (unsigned)(p.b * p.H)), kThreads,
-                         smem, stream>>>((const float*)x, (const float*)B, Gcs, dtT, (float*)hid,
-                                         (int)p.L, (int)p.H, (int)p.P, (int)p.N, (int)p.G, (int)p.Q,
-                                         (int)p.nc, (int)p.Lp, (int)p.hpg);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaError_t e;
+    if (tf32_path_supports(p)) {
+        // the chunk products on the tensor cores (TF32)
+        if ((e = launch_fps_products_tf32(p, x, B, Gcs, dtT, hid, stream)) != cudaSuccess) return e;
+    } else {
+        e = cudaFuncSetAttribute(fps_chunk_products, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        fps_chunk_products<<<dim3((unsigned)(p.P / kPT), (unsigned)p.nc, (unsigned)(p.b * p.H)),
+                             kThreads, smem, stream>>>((const float*)x, (const float*)B, Gcs, dtT,
+                                                       (float*)hid, (int)p.L, (int)p.H, (int)p.P,
+                                                       (int)p.N, (int)p.G, (int)p.Q, (int)p.nc,
+                                                       (int)p.Lp, (int)p.hpg);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     fps_state_scan<<<dim3((unsigned)((p.P * p.N + kThreads - 1) / kThreads), (unsigned)(p.b * p.H)),
                      kThreads, 0, stream>>>(Gcs, init, (float*)hid, fin, (int)p.H, (int)p.P,
                                             (int)p.N, (int)p.Q, (int)p.nc, (int)p.Lp);
@@ -304,6 +315,8 @@ cudaError_t launch_compute_out(const Problem& p, const void* x, const void* B, c
                                const float* D, void* y, cudaStream_t stream) {
     if (compute_out_tc_supports(p))
         return launch_compute_out_tc(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+    if (tf32_path_supports(p))
+        return launch_compute_out_tf32(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
     if (p.dtype == SSD_BF16)
         return launch_co<__nv_bfloat16>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
     return launch_co<float>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);

@@ -104,14 +104,15 @@ unsigned int take_errors() {
         cudaGetLastError();
         return ~0u;
     }
-    const unsigned int a = take_fwd_pass_state_error(), b = take_compute_out_error();
+    const unsigned int a = take_fwd_pass_state_error(), b = take_compute_out_error(),
+                       c = take_tf32_error();
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxTimeoutDevices)
         reinterpret_cast<volatile unsigned int*>(g_timeout_page)[dev] = 0u;
     else
         cudaGetLastError();
-    if (a == ~0u || b == ~0u) return ~0u;
-    return (a ? 1u : 0u) | (b ? 2u : 0u);
+    if (a == ~0u || b == ~0u || c == ~0u) return ~0u;
+    return (a ? 1u : 0u) | (b ? 2u : 0u) | (c ? 4u : 0u);
 }
 
 // Checks made after the arguments are validated and before anything is

@@ -101,6 +101,17 @@ unsigned int* host_timeout_word();
 // clears the device and host records), else SSD_OK (SSD_ERR_CUDA if the device
 // cannot be queried).
 ssd_status timeout_pending();
+// TF32 tensor-core kernels for fp32 inputs (N <= 128, P <= 128): the chunk
+// products of fwd_pass_state (written into the hiddens slots; the state scan
+// follows) and compute_out.
+bool tf32_path_supports(const Problem& p);
+cudaError_t launch_fps_products_tf32(const Problem& p, const void* x, const void* B,
+                                     const float* Gcs, const float* dtT, void* hiddens,
+                                     cudaStream_t stream);
+cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void* B, const void* C,
+                                    const float* Gcs, const float* dtT, const void* hiddens,
+                                    const float* D, void* y, cudaStream_t stream);
+unsigned int take_tf32_error();
 // Read and clear the device-side error word of a kernel module (bit 0: a
 // bounded wait gave up).  Synchronous.
 unsigned int take_fwd_pass_state_error();

@@ -14,8 +14,8 @@ from harness import small, to_device
 
 pytestmark = pytest.mark.gpu
 
-OURS = re.compile(r"chunk_cumsum_kernel|fwd_pass_state|fps_chunk_products|fps_state_scan|"
-                  r"compute_out_(tc|simt)")
+OURS = re.compile(r"chunk_cumsum_kernel|fwd_pass_state|fps_chunk_products|fps_products_tf32|fps_state_scan|"
+                  r"compute_out_(tc|simt|tf32)")
 
 CASES = {
     "bf16, short chains": small(seqlen=1000, nheads=4, ngroups=2, headdim=64, dstate=128,
