@@ -26,10 +26,12 @@
 //  * x, h, C, B and the per-token g, dt vectors arrive by TMA / bulk copies
 //    into a stage ring; B only passes through the ring once per group.
 //
-// Warp roles (640 threads): 0 TMA producer, 1 MMA issuer (and TMEM owner),
-// 2-3 idle, 4-11 two builder warpgroups (C B^T conversion, decay-weighted
-// operands), 12-19 two epilogue warpgroups (slot 0 / slot 1: row scale and
-// y).  A SIMT thread owns TMEM lane (query row) 32*(warp%4) + lane.
+// Warp roles (576 threads): 0-7 two builder warpgroups (C B^T conversion,
+// decay-weighted operands), 8-15 two epilogue warpgroups (slot 0 / slot 1: row
+// scale and y), 16 TMA producer, 17 MMA issuer (and TMEM owner).  A SIMT thread
+// owns TMEM lane (query row) 32*(warp%4) + lane; the SIMT warpgroups come first
+// so that they start on warpgroup boundaries with no idle warps, which leaves
+// 112 registers per thread.
 //
 // Supported here: bf16, P <= 64, N <= 128, Q in {64, 128, 256}.
 #include <cuda.h>
@@ -43,10 +45,13 @@ namespace {
 
 __device__ unsigned int g_co_error;  // bit 0: a bounded wait gave up
 
-constexpr int kThreads = 640;
+constexpr int kThreads = 576;
 constexpr int kRowBytes = 128;
-constexpr int kSimtWarp0 = 4;
+constexpr int kSimtWarp0 = 0;
 constexpr int kSimtThreads = 512;   // 16 SIMT warps
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+
 
 template <int Q>
 struct CoCfg {
@@ -178,14 +183,14 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
+    if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_holder), 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     unsigned int* err = &g_co_error;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ===================== TMA producer =====================
         if (lane == 0) {
             int sc = 0;   // stage ring counter
@@ -241,7 +246,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 ++sc;
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ===================== MMA issuer =====================
         if (lane == 0) {
             constexpr uint32_t kIdescCB = make_idesc(1, 128, Cfg::kBRows, 0, 0);
@@ -340,7 +345,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 ++sc;
             }
         }
-    } else if (warp >= kSimtWarp0) {
+    } else {
         // ===================== SIMT warpgroups =====================
         // Warpgroups 0 and 1 are builders: they convert C B^T once per group and
         // build the decay-weighted operands A of every head.  Warpgroups 2 and 3
@@ -543,40 +548,49 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     // ---- epilogue: y = acc + D x ----
                     mbar_wait(smem_u32(b_ddone + es), use & 1, err, 1u);
                     tc_fence_after();
-                    uint32_t v0[32], v1[32];
-                    __syncwarp();
-                    tmem_ld_x32(acc, v0);
-                    tmem_ld_x32(acc + 32, v1);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(b_accfree + es));
-                    // y = acc + D x, stored straight from registers: each thread
-                    // writes its own row (128 contiguous bytes, 16 at a time).  The
-                    // x row is read from the stage's swizzled tile, after which the
-                    // stage no longer holds anything this head needs.
-                    const int t = ui.c * Q + i;   // token
-                    if (i < Q && t < L) {
-                        const uint8_t* xr = st + i * kRowBytes;
-                        __nv_bfloat16* yr = y + (((int64_t)ui.b * L + t) * H + ui.h) * P;
-                        // 32 bytes (16 columns) per store where the row is 32-byte aligned
-                        const bool a32 = (reinterpret_cast<uintptr_t>(yr) & 31) == 0;
+                    // the A X products are done: this row of x (for D x) is the
+                    // last thing this warpgroup reads from the stage, which then
+                    // goes back to the producer before y is computed and stored
+                    uint4 xrow[8];
+                    {
+                        const uint8_t* xr = st + (i < Q ? i : 0) * kRowBytes;
 #pragma unroll
-                        for (int c2 = 0; c2 < 4; ++c2) {
-                            if (c2 * 16 < P) {   // P is a multiple of 16
+                        for (int ch = 0; ch < 8; ++ch)
+                            xrow[ch] = *reinterpret_cast<const uint4*>(xr + ((ch ^ (i & 7)) << 4));
+                    }
+                    mbar_arrive(smem_u32(b_empty + s));
+                    // y = acc + D x, 32 columns at a time, stored straight from
+                    // registers: each thread writes its own row (128 contiguous
+                    // bytes); 32-byte stores where the row is 32-byte aligned
+                    const int t = ui.c * Q + i;   // token
+                    const bool store = i < Q && t < L;
+                    __nv_bfloat16* yr = y + (((int64_t)ui.b * L + (store ? t : 0)) * H + ui.h) * P;
+                    const bool a32 = (reinterpret_cast<uintptr_t>(yr) & 31) == 0;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[32];
+                        __syncwarp();
+                        tmem_ld_x32(acc + half * 32, v);
+                        tmem_wait_ld();
+                        if (half == 1) {
+                            tc_fence_before();
+                            mbar_arrive(smem_u32(b_accfree + es));
+                        }
+#pragma unroll
+                        for (int c2 = 2 * half; c2 < 2 * half + 2; ++c2) {
+                            if (store && c2 * 16 < P) {   // P is a multiple of 16
                                 uint32_t ow[8];
 #pragma unroll
                                 for (int hh = 0; hh < 2; ++hh) {
                                     const int ch = 2 * c2 + hh;
-                                    const int off = (ch ^ (i & 7)) << 4;
-                                    const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
+                                    const uint4 xv = xrow[ch];
                                     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
-                                        const int p0 = ch * 8 + 2 * e;
-                                        const uint32_t* vv = p0 < 32 ? v0 : v1;
+                                        const int p0 = (ch * 8 + 2 * e) & 31;
                                         ow[4 * hh + e] =
-                                            pack_bf16(__uint_as_float(vv[p0 & 31]) + dh * bf16lo(xw[e]),
-                                                      __uint_as_float(vv[(p0 & 31) + 1]) + dh * bf16hi(xw[e]));
+                                            pack_bf16(__uint_as_float(v[p0]) + dh * bf16lo(xw[e]),
+                                                      __uint_as_float(v[p0 + 1]) + dh * bf16hi(xw[e]));
                                     }
                                 }
                                 __nv_bfloat16* dst = yr + c2 * 16;
@@ -589,9 +603,11 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             }
                         }
                     }
+                } else {
+                    mbar_arrive(smem_u32(b_empty + s));   // no block of this head here
                 }
             }
-            mbar_arrive(smem_u32(b_empty + s));
+            if (builder) mbar_arrive(smem_u32(b_empty + s));
             js += Cfg::kBlocks;
             ++sc;
         }
@@ -599,7 +615,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) report_timeout_to_host(err, host_err);
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         __syncwarp();  // lane 0 ran the MMA loop alone: reconverge before the collective
         tc_fence_after();
         tmem_dealloc(tmem, 512);
