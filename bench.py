@@ -474,9 +474,19 @@ def conv1d_main(args):
 # Gated DeltaNet configuration for --gdn: 4 sequences of 4096 tokens, 16 heads,
 # K = V = 128, chunk 64, fp32 (the gallery's kernels use C = 64 and K/V 64-128).
 GDN = dict(B=4, T=4096, H=16, K=128, V=128, chunk=64)
-GDN_METRIC = "Gated DeltaNet chunk_fwd_h + chunk_fwd_o tokens/s on 1 GB300 and % of fp32 CUDA-core peak"
-# fp32 FMA peak: 152 SMs x 128 lanes x 2 flop x the 2070 MHz maximum SM clock
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+GDN_METRIC = "Gated DeltaNet chunk_fwd_h + chunk_fwd_o tokens/s on 1 GB300 and % of the TF32 tensor peak"
+# Nominal dense tensor rates of GB300 (TF32 1.1, bf16 2.25 PFLOP/s): the TF32 peak
+# is the measured bf16 GEMM rate scaled by their ratio.
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def tf32_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]) * TF32_PER_BF16, \
+                "measured bf16 GEMM rate x nominal TF32/bf16 ratio (1.1/2.25)"
+    return 1900.0 * TF32_PER_BF16, "fallback bf16 rate x nominal TF32/bf16 ratio"
 
 
 def gdn_main(args):
@@ -559,15 +569,16 @@ def gdn_main(args):
     NT = -(-T // C)
     macs = B * H * NT * (2 * C * K * V + C * K * V + C * (C + 1) // 2 * (K + V))
     achieved = 2 * macs / (ms * 1e-3) / 1e12
+    peak_tf, peak_kind_tf = tf32_peak()
     line = {
         "metric": GDN_METRIC, "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "gdn_chunk_f32", "B": B, "T": T, "H": H, "K": K, "V": V, "chunk": C,
                    "l2": "flushed before every step"},
-        "roofline": {"bound": "alu", "kernel": "gdn_fwd_h + gdn_fwd_o", "achieved": achieved,
-                     "peak": FP32_PEAK_TFLOPS, "peak_kind": "derived (fp32 FMA lanes x max clock)",
-                     "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS,
+        "roofline": {"bound": "tensor", "kernel": "gdn_fwd_h + gdn_fwd_o", "achieved": achieved,
+                     "peak": peak_tf, "peak_kind": peak_kind_tf,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tf,
                      # DRAM bytes of both launches of one step
                      "traffic": recorded_traffic("gdn", "gdn_chunk_f32"),
                      "algorithmic_flops": 2 * macs},

@@ -13,7 +13,10 @@
 // h [B, H, NT, K, V]; h0, final [B, H, K, V]; all fp32 (the pages run these
 // products in fp32 / TF32).
 //
-// This GB300 version runs on the CUDA cores in fp32.  A CTA owns a tile of V
+// Shapes with K and V multiples of 16 (up to 128) run on the TF32 tensor cores
+// (tf32_path.cu: the state held in tensor memory for chunk_fwd_h, and the
+// compute_out kernel for chunk_fwd_o).  The kernels below serve the others,
+// on the CUDA cores in fp32.  A CTA owns a tile of V
 // columns (32 for chunk_fwd_h, 64 for chunk_fwd_o), stages the chunk's rows of
 // k and w (or q and k) in shared memory -- transposed where an operand is read
 // as four consecutive rows -- and keeps its state tile there.  Each thread
@@ -413,12 +416,16 @@ cudaError_t launch_any(const GdnProblem& p, bool fwd_h, const float* q, const fl
 cudaError_t launch_gdn_fwd_h(const GdnProblem& p, const float* k, const float* w, const float* u,
                              const float* g, const float* h0, float* h, float* v_new,
                              float* final_state, cudaStream_t stream) {
+    if (gdn_tf32_supports(p) && p.T > 0)   // tensor cores (tf32_path.cu)
+        return launch_gdn_fwd_h_tf32(p, k, w, u, g, h0, h, v_new, final_state, stream);
     return launch_any(p, true, nullptr, k, w, u, g, h0, h, v_new, final_state, nullptr, stream);
 }
 
 cudaError_t launch_gdn_fwd_o(const GdnProblem& p, const float* q, const float* k,
                              const float* v_new, const float* h, const float* g, float* o,
                              cudaStream_t stream) {
+    if (gdn_tf32_supports(p))   // tensor cores (tf32_path.cu)
+        return launch_gdn_fwd_o_tf32(p, q, k, v_new, h, g, o, stream);
     return launch_any(p, false, q, k, nullptr, nullptr, g, nullptr, const_cast<float*>(h),
                       const_cast<float*>(v_new), nullptr, o, stream);
 }

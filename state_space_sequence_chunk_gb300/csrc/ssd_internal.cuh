@@ -112,6 +112,14 @@ cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void*
                                     const float* Gcs, const float* dtT, const void* hiddens,
                                     const float* D, void* y, cudaStream_t stream);
 unsigned int take_tf32_error();
+// Gated DeltaNet on the TF32 tensor cores (K, V multiples of 16, at most 128).
+bool gdn_tf32_supports(const GdnProblem& p);
+cudaError_t launch_gdn_fwd_o_tf32(const GdnProblem& p, const float* q, const float* k,
+                                  const float* v_new, const float* h, const float* g, float* o,
+                                  cudaStream_t stream);
+cudaError_t launch_gdn_fwd_h_tf32(const GdnProblem& p, const float* k, const float* w,
+                                  const float* u, const float* g, const float* h0, float* h,
+                                  float* v_new, float* final_state, cudaStream_t stream);
 // Read and clear the device-side error word of a kernel module (bit 0: a
 // bounded wait gave up).  Synchronous.
 unsigned int take_fwd_pass_state_error();

@@ -308,6 +308,12 @@ __device__ __forceinline__ void put_transposed(uint32_t tile, int rows, int Kdim
     }
 }
 
+// kGdn: the same kernel serves the Gated DeltaNet output chunk_fwd_o (Helion
+// hackathon gallery, "GDN chunk_fwd_o"): o = e^{g} (q h) + causal((q k^T) o
+// e^{g_i - g_j}) v_new -- C -> q, B -> k, x -> v_new, hiddens -> h, y -> o,
+// one "group" per head, no dt (1) and no D; Gcs then points at the natural-log
+// gate g [batch, T, H], scaled by log2(e) on load.
+template <bool kGdn>
 __global__ void __launch_bounds__(kThreads)
 compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
                  const float* __restrict__ C, const float* __restrict__ Gcs,
@@ -343,8 +349,14 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     }
     if (warp == 0) tmem_alloc(smem_u32(tmem_holder), q.tmem_cols);
     for (int i = tid; i < q.Q; i += kThreads) {
-        gv[i] = Gcs[(int64_t)bh * q.Lp + t0 + i];
-        dv[i] = dtT[(int64_t)bh * q.Lp + t0 + i];
+        if (kGdn) {
+            const int t = t0 + i;
+            gv[i] = t < q.L ? Gcs[((int64_t)b * q.L + t) * q.H + h] * kLog2e : 0.f;
+            dv[i] = 1.f;
+        } else {
+            gv[i] = Gcs[(int64_t)bh * q.Lp + t0 + i];
+            dv[i] = dtT[(int64_t)bh * q.Lp + t0 + i];
+        }
     }
     // C_I (rows = query rows) and B_0 (rows = keys)
     put_rows(ct, 128, Cb + (int64_t)(t0 + i0) * bc_stride, bc_stride,
@@ -499,6 +511,355 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     }
 }
 
+// ===========================================================================
+// Gated DeltaNet chunk_fwd_h (Helion hackathon gallery, "GDN chunk_fwd_h"):
+// one CTA per (64-column tile of V, batch*head), walking the chunks in order.
+// The state is held transposed, S^T [v][k], as an fp32 tensor-memory
+// accumulator (lane v of the tile, column k).  Per chunk c:
+//   (a) CUDA cores: h[c] = S (into a shared staging tile), R = tf32(S^T) into
+//       a second region (the A operand of the next product), then
+//       S^T <- e^{g_last} S^T in place;
+//   (b) D1^T = R w^T           M = v, N = the chunk's tokens, K = k
+//                              (B operand: the w rows [t][k], K-major);
+//   (c) CUDA cores: v_new[t][v] = u[t][v] - D1^T[v][t] (in place over the
+//       staged u tile) and A2[v][t] = tf32(v_new e^{g_last - g_t}) over D1^T;
+//   (d) S^T += A2 k            M = v, N = k, K = the chunk's tokens
+//                              (B operand: k^T [k][t], written transposed).
+// Only two warps own the tile's tensor-memory lanes, so the CUDA cores keep
+// global memory off the chain: at the start of chunk c the other two warps
+// request (cp.async) the rows of w (straight into its swizzled operand tile),
+// k and g of chunk c + 1 and the u tile of chunk c; while (b) runs, the staged rows become the next
+// chunk's TF32 tiles and all four warps write h[c] out as 16-byte stores, and
+// while (d) runs they write v_new the same way.  Tokens past the sequence end
+// read as zero rows, so their v_new and gated terms vanish.
+// ===========================================================================
+constexpr int kGdnVt = 64;   // V columns per CTA (TMEM lanes 0..63)
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+struct GdnH {
+    int T, H, K, V, C, NT;
+    int w_bytes, k_bytes;    // one buffer's w tile (C rows x K) and k^T tile (K rows x C)
+    int raw_bytes;           // staging of one chunk's raw k rows: C x (K + 4) fp32
+    uint32_t tmem_cols;
+};
+
+__global__ void __launch_bounds__(kThreads)
+gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
+               const float* __restrict__ u, const float* __restrict__ g,
+               const float* __restrict__ h0, float* __restrict__ hout, float* __restrict__ v_new,
+               float* __restrict__ final_state, const GdnH q, unsigned int* host_err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t s0 = smem_u32(smem);
+    const uint32_t buf_bytes = (uint32_t)(q.w_bytes + q.k_bytes);
+    // raw k rows [C][K + 4]: the pad puts consecutive rows 4 banks apart, so the
+    // transposing reads (lanes take rows) are conflict-free
+    float* kraw = reinterpret_cast<float*>(smem + 2 * buf_bytes);
+    const int kpitch = q.K + 4;
+    float* hst = kraw + q.raw_bytes / 4;                                   // [K][64] h staging
+    float* ubuf = hst + 128 * kGdnVt;                                      // [C][64] u, then v_new
+    float* gstage = ubuf + 64 * kGdnVt;                                    // [64] raw g of a chunk
+    float* gbuf = gstage + 64;                                             // [2][64] gates
+    float* glast_s = gbuf + 2 * 64;                                        // [2] g_last
+    uint64_t* bar = reinterpret_cast<uint64_t*>(glast_s + 2);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int v0 = blockIdx.x * kGdnVt, bh = blockIdx.y, b = bh / q.H, h = bh % q.H;
+    const int v = v0 + tid;                           // this thread's column of V (warps 0, 1)
+    const bool lane_ok = tid < kGdnVt && v < q.V;
+    const bool state_warp = warp < kGdnVt / 32;       // warps whose TMEM lanes hold the tile
+    const int vt = min(kGdnVt, q.V - v0);             // columns of this tile (a multiple of 16)
+    const int v4s = vt / 4;
+    const int64_t tok_stride_k = (int64_t)q.H * q.K, tok_stride_v = (int64_t)q.H * q.V;
+    const float* kb = kmat + (int64_t)b * q.T * tok_stride_k + (int64_t)h * q.K;
+    const float* wb = w + (int64_t)b * q.T * tok_stride_k + (int64_t)h * q.K;
+    const float* ub = u + (int64_t)b * q.T * tok_stride_v + (int64_t)h * q.V + v0;
+    float* vnb = v_new + (int64_t)b * q.T * tok_stride_v + (int64_t)h * q.V + v0;
+    const float* gb = g + (int64_t)b * q.T * q.H + h;
+
+    if (tid == 0) {
+        mbar_init(smem_u32(bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tmem_holder), q.tmem_cols);
+    // asynchronous copies of chunk c: w rows into their swizzled operand tile
+    // (buffer c & 1), raw k rows and g (zero past the end)
+    auto stage_wkg = [&](int c, int i0, int ni) {   // issued by threads [i0, i0 + ni)
+        const int t0 = c * q.C, nv = min(q.C, q.T - t0), k4s = q.K / 4;
+        const uint32_t wt = s0 + (c & 1) * buf_bytes;
+        for (int e = tid - i0; e < q.C * k4s; e += ni) {
+            const int t = e / k4s, k4 = e - t * k4s;
+            const bool in = t < nv;
+            const int64_t off = (int64_t)(t0 + (in ? t : 0)) * tok_stride_k + 4 * k4;
+            cp_async_16(wt + swz(t, 4 * k4, q.C), wb + off, in ? 16u : 0u);
+            cp_async_16(smem_u32(kraw + t * kpitch + 4 * k4), kb + off, in ? 16u : 0u);
+        }
+        for (int t = tid - i0; t < q.C; t += ni)
+            cp_async_4(smem_u32(gstage + t), gb + (int64_t)(t0 + min(t, nv - 1)) * q.H, 4u);
+    };
+    // the u tile of chunk c: [C][vt]
+    auto stage_u = [&](int c, int i0, int ni) {   // issued by threads [i0, i0 + ni)
+        const int t0 = c * q.C, nv = min(q.C, q.T - t0);
+        for (int e = tid - i0; e < q.C * v4s; e += ni) {
+            const int t = e / v4s, v4 = e - t * v4s;
+            const bool in = t < nv;
+            cp_async_16(smem_u32(ubuf + t * kGdnVt + 4 * v4),
+                        ub + (int64_t)(t0 + (in ? t : 0)) * tok_stride_v + 4 * v4, in ? 16u : 0u);
+        }
+    };
+    // staged rows of chunk c -> its TF32 operand tiles (buffer c & 1): w rounded
+    // in place, k transposed; gates gl = g_last, gate[t] = e^{g_last - g_t}
+    // (0 past the end).  Each thread loads 8 vectors before storing any.
+    auto convert = [&](int c) {
+        const uint32_t wt = s0 + (c & 1) * buf_bytes, kt = wt + q.w_bytes;
+        const int k4s = q.K / 4, total = q.C * k4s;
+        for (int e0 = tid; e0 < total; e0 += kThreads * 8) {
+            uint4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = e0 + j * kThreads, t = e / k4s, k4 = e - t * k4s;
+                if (e < total)
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(x[j].x), "=r"(x[j].y), "=r"(x[j].z), "=r"(x[j].w)
+                                 : "r"(wt + swz(t, 4 * k4, q.C)));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = e0 + j * kThreads, t = e / k4s, k4 = e - t * k4s;
+                if (e < total)
+                    st_shared_v4(wt + swz(t, 4 * k4, q.C), to_tf32(__uint_as_float(x[j].x)),
+                                 to_tf32(__uint_as_float(x[j].y)), to_tf32(__uint_as_float(x[j].z)),
+                                 to_tf32(__uint_as_float(x[j].w)));
+            }
+        }
+        for (int t0 = 0; t0 < q.C; t0 += 32) {               // k^T: rows k, lanes take tokens t
+            const int t = t0 + lane;
+            for (int k40 = warp; k40 < k4s; k40 += 4 * 8) {
+                float4 x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int k4 = k40 + 4 * j;
+                    x[j] = (t < q.C && k4 < k4s) ? *reinterpret_cast<const float4*>(kraw + t * kpitch + 4 * k4)
+                                                 : zero4();
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int k4 = k40 + 4 * j;
+                    if (t < q.C && k4 < k4s) {
+                        st_shared_u32(kt + swz(4 * k4 + 0, t, q.K), to_tf32(x[j].x));
+                        st_shared_u32(kt + swz(4 * k4 + 1, t, q.K), to_tf32(x[j].y));
+                        st_shared_u32(kt + swz(4 * k4 + 2, t, q.K), to_tf32(x[j].z));
+                        st_shared_u32(kt + swz(4 * k4 + 3, t, q.K), to_tf32(x[j].w));
+                    }
+                }
+            }
+        }
+        const int nv = min(q.C, q.T - c * q.C);
+        float* gc = gbuf + (c & 1) * 64;
+        const float gl = gstage[nv - 1];
+        for (int t = tid; t < q.C; t += kThreads) gc[t] = t < nv ? expf(gl - gstage[t]) : 0.f;
+        if (tid == 0) glast_s[c & 1] = gl;
+    };
+    if (q.NT > 0) {
+        stage_wkg(0, 0, kThreads);
+        cp_async_wait_all();
+        __syncthreads();
+        convert(0);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t st_col = 0, r_col = 128, d_col = 256;   // S^T, R, D1^T / A2
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // S^T = h0^T (or 0)
+    if (state_warp) {
+        const float* hb0 = h0 ? h0 + (int64_t)bh * q.K * q.V + v : nullptr;
+        for (int k0 = 0; k0 < q.K; k0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                r[e] = __float_as_uint((hb0 && lane_ok) ? hb0[(int64_t)(k0 + e) * q.V] : 0.f);
+            tmem_st_x16(tmem + lane_off + st_col + k0, r);
+        }
+        tmem_wait_st();
+    }
+    const uint32_t idesc1 = make_idesc(2, 128, (uint32_t)q.C, 0, 0);
+    const uint32_t idesc2 = make_idesc(2, 128, (uint32_t)q.K, 0, 0);
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int c = 0; c < q.NT; ++c) {
+        const int t0 = c * q.C, nv = min(q.C, q.T - t0);
+        const float* gc = gbuf + (c & 1) * 64;
+        const uint32_t wt = s0 + (c & 1) * buf_bytes, kt = wt + q.w_bytes;
+        // requests that complete while the chain below runs, issued by the two
+        // warps that hold no lanes of the state while the other two run (a)
+        if (!state_warp) {
+            stage_u(c, 64, kThreads - 64);
+            if (c + 1 < q.NT) stage_wkg(c + 1, 64, kThreads - 64);
+        }
+        const float dec = expf(glast_s[c & 1]);
+        // (a) h[c] = S (staged); R = tf32(S^T); S^T <- e^{g_last} S^T, 32
+        // columns at a time (16 for the last block when K % 32 == 16)
+        if (state_warp) {
+            __syncwarp();
+            for (int k0 = 0; k0 < q.K; k0 += 32) {
+                const int n = min(32, q.K - k0);   // 16 or 32: K is a multiple of 16
+                uint32_t r[32];
+                if (n == 32) {
+                    tmem_ld_x32(tmem + lane_off + st_col + k0, r);
+                } else {
+                    uint32_t r16[16];
+                    tmem_ld_x16(tmem + lane_off + st_col + k0, r16);
+                    tmem_wait_ld();   // before the destination registers are read
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) { r[e] = r16[e]; r[16 + e] = 0u; }
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)   // hst[k][v]: lanes write consecutive words
+                    if (e < n) hst[(k0 + e) * kGdnVt + tid] = __uint_as_float(r[e]);
+                uint32_t rt[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float sv = __uint_as_float(r[e]);
+                    rt[e] = to_tf32(sv);
+                    r[e] = __float_as_uint(sv * dec);
+                }
+                if (n == 32) {
+                    tmem_st_x32(tmem + lane_off + r_col + k0, rt);
+                    tmem_st_x32(tmem + lane_off + st_col + k0, r);
+                } else {
+                    uint32_t a16[16], b16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) { a16[e] = rt[e]; b16[e] = r[e]; }
+                    tmem_st_x16(tmem + lane_off + r_col + k0, a16);
+                    tmem_st_x16(tmem + lane_off + st_col + k0, b16);
+                }
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        // (b) D1^T = R w^T
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            for (int kk = 0; kk < q.K / 8; ++kk)
+                mma_tf32_ts(tmem + d_col, tmem + r_col + kk * 8, kmajor_desc(wt, kk, q.C), idesc1,
+                            kk > 0 ? 1u : 0u);
+            mma_commit(smem_u32(bar));
+        }
+        // meanwhile: h[c] out as 16-byte stores by all four warps
+        if (ok) {
+            float* hc = hout + ((int64_t)bh * q.NT + c) * q.K * q.V + v0;
+            for (int e = tid; e < q.K * v4s; e += kThreads) {
+                const int k = e / v4s, v4 = e - k * v4s;
+                *reinterpret_cast<float4*>(hc + (int64_t)k * q.V + 4 * v4) =
+                    *reinterpret_cast<const float4*>(hst + k * kGdnVt + 4 * v4);
+            }
+        }
+        // ... and the staged rows (landed) become the next chunk's operand
+        // tiles in the other buffer (its last reader, (d) of chunk c - 1, is
+        // complete)
+        cp_async_wait_all();
+        __syncthreads();
+        if (c + 1 < q.NT && ok) convert(c + 1);
+        fence_proxy_async_smem();
+        chain_wait(smem_u32(bar), phase, ok);
+        tc_fence_after();
+        // (c) v_new = u - D1 (over the staged u); A2 = tf32(v_new e^{g_last - g_t}) over D1^T
+        if (state_warp) {
+            __syncwarp();
+            for (int c0 = 0; c0 < q.C; c0 += 32) {
+                const int n = min(32, q.C - c0);   // 16 or 32 (C is 16, 32 or 64)
+                uint32_t r[32];
+                if (n == 32) {
+                    tmem_ld_x32(tmem + lane_off + d_col + c0, r);
+                } else {
+                    uint32_t r16[16];
+                    tmem_ld_x16(tmem + lane_off + d_col + c0, r16);
+                    tmem_wait_ld();   // before the destination registers are read
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) { r[e] = r16[e]; r[16 + e] = 0u; }
+                }
+                // u and the gates into registers first, so that the loads are not
+                // held behind the in-place stores
+                float uv[32], gt[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    uv[e] = e < n ? ubuf[(c0 + e) * kGdnVt + tid] : 0.f;
+                    gt[e] = e < n ? gc[c0 + e] : 0.f;
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float vn = uv[e] - __uint_as_float(r[e]);
+                    if (e < n) ubuf[(c0 + e) * kGdnVt + tid] = vn;
+                    r[e] = to_tf32(vn * gt[e]);   // gate 0 past the end and beyond n
+                }
+                if (n == 32) {
+                    tmem_st_x32(tmem + lane_off + d_col + c0, r);
+                } else {
+                    uint32_t r16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r16[e] = r[e];
+                    tmem_st_x16(tmem + lane_off + d_col + c0, r16);
+                }
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        // (d) S^T += A2 k
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            for (int kk = 0; kk < q.C / 8; ++kk)
+                mma_tf32_ts(tmem + st_col, tmem + d_col + kk * 8, kmajor_desc(kt, kk, q.K), idesc2,
+                            1u);
+            mma_commit(smem_u32(bar));
+        }
+        // meanwhile: v_new of the chunk's real tokens out as 16-byte stores
+        if (ok) {
+            for (int e = tid; e < nv * v4s; e += kThreads) {
+                const int t = e / v4s, v4 = e - t * v4s;
+                *reinterpret_cast<float4*>(vnb + (int64_t)(t0 + t) * tok_stride_v + 4 * v4) =
+                    *reinterpret_cast<const float4*>(ubuf + t * kGdnVt + 4 * v4);
+            }
+        }
+        chain_wait(smem_u32(bar), phase, ok);
+        tc_fence_after();
+        __syncthreads();   // ubuf and hst are read above before the next chunk refills them
+    }
+    // final_state = S
+    if (state_warp && final_state != nullptr) {
+        __syncwarp();
+        float* fs = final_state + (int64_t)bh * q.K * q.V + v;
+        for (int k0 = 0; k0 < q.K; k0 += 16) {
+            uint32_t r[16];
+            tmem_ld_x16(tmem + lane_off + st_col + k0, r);
+            tmem_wait_ld();
+            if (lane_ok && ok) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) fs[(int64_t)(k0 + e) * q.V] = __uint_as_float(r[e]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) report_timeout_to_host(&g_tf32_error, host_err);
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, q.tmem_cols);
+    }
+}
+
 }  // namespace
 
 bool tf32_path_supports(const Problem& p) {
@@ -527,12 +888,11 @@ cudaError_t launch_fps_products_tf32(const Problem& p, const void* x, const void
     return cudaGetLastError();
 }
 
-cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void* B, const void* C,
-                                    const float* Gcs, const float* dtT, const void* hiddens,
-                                    const float* D, void* y, cudaStream_t stream) {
-    CoTf32 q;
-    q.L = (int)p.L; q.H = (int)p.H; q.P = (int)p.P; q.N = (int)p.N; q.G = (int)p.G;
-    q.Q = (int)p.Q; q.nc = (int)p.nc; q.Lp = (int)p.Lp; q.hpg = (int)p.hpg;
+namespace {
+// Tile sizes, TMEM columns and shared memory of compute_out_tf32 for the
+// sizes already in q (L .. hpg); returns the dynamic shared memory per CTA,
+// or -1 if it does not fit.
+int co_tf32_layout(CoTf32& q) {
     q.KB = q.Q < 128 ? q.Q : 128;
     q.nblk = q.Q > 128 ? q.Q / 128 : 1;
     q.scol = (uint32_t)((q.P + 31) / 32 * 32);
@@ -547,14 +907,70 @@ cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void*
     const int smem = q.c_bytes + q.b_bytes + q.h_bytes + (q.x_sep ? q.x_bytes : 0) + extras;
     const int by_tmem = 512 / (int)q.tmem_cols;
     const int smem_cta = std::max(smem, (228 * 1024) / by_tmem - 1024);
-    if (smem_cta > 227 * 1024) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(compute_out_tf32,
+    return smem_cta > 227 * 1024 ? -1 : smem_cta;
+}
+}  // namespace
+
+cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void* B, const void* C,
+                                    const float* Gcs, const float* dtT, const void* hiddens,
+                                    const float* D, void* y, cudaStream_t stream) {
+    CoTf32 q;
+    q.L = (int)p.L; q.H = (int)p.H; q.P = (int)p.P; q.N = (int)p.N; q.G = (int)p.G;
+    q.Q = (int)p.Q; q.nc = (int)p.nc; q.Lp = (int)p.Lp; q.hpg = (int)p.hpg;
+    const int smem_cta = co_tf32_layout(q);
+    if (smem_cta < 0) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(compute_out_tf32<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
     if (e != cudaSuccess) return e;
-    compute_out_tf32<<<dim3((unsigned)q.nblk, (unsigned)p.nc, (unsigned)(p.b * p.H)), kThreads,
-                       (size_t)smem_cta, stream>>>(
+    compute_out_tf32<false><<<dim3((unsigned)q.nblk, (unsigned)p.nc, (unsigned)(p.b * p.H)),
+                              kThreads, (size_t)smem_cta, stream>>>(
         (const float*)x, (const float*)B, (const float*)C, Gcs, dtT, (const float*)hiddens, D,
         (float*)y, q, host_timeout_word());
+    return cudaGetLastError();
+}
+
+bool gdn_tf32_supports(const GdnProblem& p) {
+    return p.K % 16 == 0 && p.V % 16 == 0 && p.K <= 128 && p.V <= 128 && p.NT <= 65535 &&
+           p.B * p.H <= 65535;
+}
+
+cudaError_t launch_gdn_fwd_o_tf32(const GdnProblem& p, const float* qm, const float* k,
+                                  const float* v_new, const float* h, const float* g, float* o,
+                                  cudaStream_t stream) {
+    CoTf32 q;
+    q.L = (int)p.T; q.H = (int)p.H; q.P = (int)p.V; q.N = (int)p.K; q.G = (int)p.H;
+    q.Q = (int)p.C; q.nc = (int)p.NT; q.Lp = 0; q.hpg = 1;
+    const int smem_cta = co_tf32_layout(q);
+    if (smem_cta < 0) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(compute_out_tf32<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
+    if (e != cudaSuccess) return e;
+    // operand roles: C <- q, B <- k, x <- v_new, hiddens <- h, y <- o, Gcs <- g
+    compute_out_tf32<true><<<dim3((unsigned)q.nblk, (unsigned)p.NT, (unsigned)(p.B * p.H)),
+                             kThreads, (size_t)smem_cta, stream>>>(
+        v_new, k, qm, g, nullptr, h, nullptr, o, q, host_timeout_word());
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gdn_fwd_h_tf32(const GdnProblem& p, const float* k, const float* w,
+                                  const float* u, const float* g, const float* h0, float* h,
+                                  float* v_new, float* final_state, cudaStream_t stream) {
+    GdnH q;
+    q.T = (int)p.T; q.H = (int)p.H; q.K = (int)p.K; q.V = (int)p.V; q.C = (int)p.C;
+    q.NT = (int)p.NT;
+    q.w_bytes = up1024(tile_bytes(q.C, q.K));
+    q.k_bytes = up1024(tile_bytes(q.K, q.C));
+    q.raw_bytes = q.C * (q.K + 4) * 4;
+    q.tmem_cols = 512;   // S^T, R (128 columns each) and D1^T / A2: one CTA per SM
+    const int smem = 2 * (q.w_bytes + q.k_bytes) + q.raw_bytes + 128 * kGdnVt * 4 +
+                     64 * kGdnVt * 4 + 64 * 4 + 2 * 64 * 4 + 8 + 64 + 1024;
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gdn_fwd_h_tf32, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem);
+    if (e != cudaSuccess) return e;
+    gdn_fwd_h_tf32<<<dim3((unsigned)((p.V + kGdnVt - 1) / kGdnVt), (unsigned)(p.B * p.H)), kThreads,
+                     (size_t)smem, stream>>>(k, w, u, g, h0, h, v_new, final_state, q,
+                                             host_timeout_word());
     return cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
 """Gated DeltaNet chunk kernels (Helion hackathon gallery, "GDN chunk_fwd_h" /
-"GDN chunk_fwd_o") against the step-by-step fp64 oracle."""
+"GDN chunk_fwd_o") against the step-by-step fp64 oracle: shapes with K and V
+multiples of 16 run on the TF32 tensor cores, the others on the CUDA cores."""
 import numpy as np
 import pytest
 import torch
@@ -35,6 +36,10 @@ def gdn_inputs(B, T, H, K, V, chunk, seed, with_h0=True):
     (1, 7, 1, 32, 64, 64, True),        # shorter than one chunk
     (1, 130, 2, 32, 37, 32, True),      # V not a multiple of 4 (scalar loads and stores)
     (1, 200, 2, 128, 100, 64, False),   # two V halves of chunk_fwd_o, the second partial
+    # K and V multiples of 16: the tensor-core kernels
+    (2, 333, 2, 64, 128, 64, True),     # two 64-column V tiles of chunk_fwd_h, ragged
+    (1, 500, 3, 128, 16, 32, True),     # smallest V, chunk 32
+    (1, 90, 2, 16, 128, 16, False),     # smallest K and chunk
 ])
 def test_gdn_matches_oracle(B, T, H, K, V, chunk, with_h0):
     q, k, w, u, g, h0 = gdn_inputs(B, T, H, K, V, chunk, seed=T + K)
@@ -64,3 +69,50 @@ def test_gdn_empty_sequence_passes_the_state():
     torch.cuda.synchronize()
     assert h.numel() == 0 and v_new.numel() == 0
     assert torch.equal(fin.cpu(), torch.from_numpy(h0))
+
+
+def test_gdn_bench_shape_whole_tensors():
+    """The benchmark's shape (B4, T4096, H16, K = V = 128, chunk 64: each CTA
+    walks 64 chunks on the tensor cores) against the oracle on every output
+    element: h, v_new, final_state and o.  Each (batch, head) is an independent
+    recurrence, so the oracle runs slice by slice on all host cores and the
+    maxima are folded into global ones."""
+    import concurrent.futures as cf
+    import os
+    import threading
+    B, T, H, K, V, C = 4, 4096, 16, 128, 128, 64
+    q, k, w, u, g, h0 = gdn_inputs(B, T, H, K, V, C, seed=4096 + 128)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    h, v_new, fin = ssd.gdn_chunk_fwd_h(dev(k), dev(w), dev(u), dev(g), dev(h0), chunk=C)
+    o = ssd.gdn_chunk_fwd_o(dev(q), dev(k), v_new, h, dev(g), chunk=C)
+    torch.cuda.synchronize()
+    assert ssd.ssd_take_device_errors() == 0
+    h, v_new, fin, o = (t.cpu().numpy() for t in (h, v_new, fin, o))
+    acc = {n: [0.0, 0.0] for n in ("h", "v_new", "final_state", "o")}
+    lock = threading.Lock()
+    lib = oracle.load()
+
+    def fold(name, out, ref):
+        d, m = float(np.max(np.abs(out - ref))), float(np.max(np.abs(ref)))
+        with lock:
+            acc[name][0] = max(acc[name][0], d)
+            acc[name][1] = max(acc[name][1], m)
+
+    def run(bh):
+        b, hh = bh
+        sl = lambda a: a[b:b + 1, :, hh:hh + 1]
+        hr, vr, fr = oracle.gdn_fwd_h(sl(k), sl(w), sl(u), sl(g), h0[b:b + 1, hh:hh + 1],
+                                      chunk=C, lib=lib)
+        orf = oracle.gdn_fwd_o(sl(q), sl(k), vr, hr, sl(g), chunk=C, lib=lib)
+        fold("h", h[b, hh], hr[0, 0])
+        fold("v_new", v_new[b, :, hh], vr[0, :, 0])
+        fold("final_state", fin[b, hh], fr[0, 0])
+        fold("o", o[b, :, hh], orf[0, :, 0])
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        list(ex.map(run, [(b, hh) for b in range(B) for hh in range(H)]))
+    errs = {n: a[0] / a[1] for n, a in acc.items()}
+    print("\ngdn bench shape whole-tensor rel err " +
+          ", ".join(f"{n} {e:.3e}" for n, e in errs.items()))
+    for n, e in errs.items():
+        assert e < TOL["f32"], (n, e)
