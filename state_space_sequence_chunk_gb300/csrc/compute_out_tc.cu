@@ -33,7 +33,9 @@
 // so that they start on warpgroup boundaries with no idle warps, which leaves
 // 112 registers per thread.
 //
-// Supported here: bf16, P <= 64, N <= 128, Q in {64, 128, 256}.
+// Supported here: bf16, P <= 64, and N <= 128 with Q in {64, 128, 256} or
+// N <= 256 with Q in {64, 128} (the state padded to 128 or 256 by the TMA's
+// zero fill).
 #include <cuda.h>
 
 #include "sm100_ptx.cuh"
@@ -53,22 +55,30 @@ constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
 
 
-template <int Q>
+// NS = N padded to 128 or 256 (the state dimension, the K of C B^T and C h^T).
+// NS = 256 serves Q <= 128 only (one 64 KB C buffer and three stages); its B
+// tile (four 64-column atoms) spans two stage slots, atoms 0-1 in the first.
+template <int Q, int NS = 128>
 struct CoCfg {
+    static_assert(NS == 128 || (NS == 256 && Q <= 128), "N = 256 is served for Q <= 128");
     static constexpr int kBlocks = Q > 128 ? 2 : 1;        // 128-row query blocks per chunk
     static constexpr int kBRows = Q < 128 ? Q : 128;        // rows of a key block
     static constexpr int kCRows = Q < 128 ? 128 : Q;        // rows reserved per C atom
-    static constexpr int kNAtoms = 2;                       // N padded to 128 (two 64-wide atoms)
+    static constexpr int kNAtoms = NS / 64;                 // N in 64-wide swizzle atoms
+    static constexpr int kKSteps = NS / 16;                 // K = 16 steps over the state
     static constexpr int kCAtomBytes = kCRows * kRowBytes;
     static constexpr int kCBytes = kNAtoms * kCAtomBytes;
-    static constexpr int kCBufs = Q > 128 ? 1 : 2;
+    static constexpr int kCBufs = (Q > 128 || NS > 128) ? 1 : 2;
     static constexpr int kXBytes = Q * kRowBytes;           // x tile, P padded to 64
-    static constexpr int kHBytes = 128 * kRowBytes;         // h^T: 128 rows of N x 64 of P
+    static constexpr int kHBytes = NS * kRowBytes;          // h^T: NS rows of N x 64 of P
     static constexpr int kVecBytes = Q * 4;
     static constexpr int kStageBytes = ((kXBytes + kHBytes + 2 * kVecBytes) + 1023) / 1024 * 1024;
-    static constexpr int kStages = Q > 128 ? 3 : 4;
-    static constexpr int kBSlots = Q > 128 ? 2 : 1;         // stage slots a B tile occupies
+    static constexpr int kStages = (Q > 128 || NS > 128) ? 3 : 4;
     static constexpr int kBAtomBytes = kBRows * kRowBytes;
+    // B atoms per stage slot: all of them, or two when N = 256 (Q <= 128)
+    static constexpr bool kBSplit = NS > 128 && Q <= 128 && kNAtoms * kBAtomBytes > kStageBytes;
+    static constexpr int kBSlots = (Q > 128 || kBSplit) ? 2 : 1;   // stage slots a B tile occupies
+    static_assert(!kBSplit || 2 * kBAtomBytes <= kStageBytes, "two B atoms per stage slot");
     static constexpr int kBarBytes = 4096;  // barriers, TMEM holder, v_j tables
     static constexpr int kSmem = kCBufs * kCBytes + kStages * kStageBytes + kBarBytes + 1024;
     // TMEM columns (512 allocated)
@@ -126,14 +136,14 @@ __device__ __forceinline__ bool new_group(int u, int u0, int H, int hpg) {
     return u == u0 || (u % H) % hpg == 0;
 }
 
-template <int Q>
+template <int Q, int NS>
 __global__ void __launch_bounds__(kThreads, 1)
 compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_h,
                const float* __restrict__ Gcs, const float* __restrict__ dtT,
                const float* __restrict__ D, __nv_bfloat16* __restrict__ y, int L, int H, int P,
                int nc, int Lp, int hpg, int units, unsigned int* host_err) {
-    using Cfg = CoCfg<Q>;
+    using Cfg = CoCfg<Q, NS>;
     constexpr int NST = Cfg::kStages;
     constexpr int NCB = Cfg::kCBufs;
     extern __shared__ uint8_t smem_raw[];
@@ -211,16 +221,23 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     }
                     const uint32_t gbar = smem_u32(b_grp + cb);
                     mbar_arrive_expect_tx(gbar, Cfg::kNAtoms * (Q * kRowBytes) +
-                                                    Cfg::kBSlots * Cfg::kNAtoms * Cfg::kBAtomBytes);
+                                                    (Cfg::kBSplit ? 1 : Cfg::kBSlots) *
+                                                        Cfg::kNAtoms * Cfg::kBAtomBytes);
                     const uint32_t cdst = smem_u32(cbuf_ptr + cb * Cfg::kCBytes);
                     for (int a = 0; a < Cfg::kNAtoms; ++a)
                         tma_load_4d(cdst + a * Cfg::kCAtomBytes, &tm_c, gbar, a * 64, ui.grp,
                                     ui.c * Q, ui.b);
                     for (int j = 0; j < Cfg::kBSlots; ++j) {
                         const uint32_t bdst = smem_u32(stage_ptr + bslot[j] * Cfg::kStageBytes);
-                        for (int a = 0; a < Cfg::kNAtoms; ++a)
-                            tma_load_4d(bdst + a * Cfg::kBAtomBytes, &tm_b, gbar, a * 64, ui.grp,
-                                        ui.c * Q + j * 128, ui.b);
+                        if (Cfg::kBSplit) {   // atoms 2j, 2j + 1 of the chunk's keys
+                            for (int a2 = 0; a2 < 2; ++a2)
+                                tma_load_4d(bdst + a2 * Cfg::kBAtomBytes, &tm_b, gbar,
+                                            (2 * j + a2) * 64, ui.grp, ui.c * Q, ui.b);
+                        } else {              // all atoms of key block j
+                            for (int a = 0; a < Cfg::kNAtoms; ++a)
+                                tma_load_4d(bdst + a * Cfg::kBAtomBytes, &tm_b, gbar, a * 64, ui.grp,
+                                            ui.c * Q + j * 128, ui.b);
+                        }
                     }
                     // keep the slots' "full" phases in step with the ring (the B
                     // bytes themselves complete on the group barrier)
@@ -286,15 +303,23 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             const int J = (Q > 128) ? (r == 0 ? 0 : 1) : 0;
                             const uint32_t bbase =
                                 smem_u32(stage_ptr + ((sc + J) % NST) * Cfg::kStageBytes);
+                            // with split B, atoms 2 and 3 sit in the next stage slot
+                            const uint32_t bbase1 =
+                                smem_u32(stage_ptr + ((sc + 1) % NST) * Cfg::kStageBytes);
                             const uint32_t dcol = tmem + Cfg::kScratch + q * 128;
                             const uint64_t ad0 = smem_desc_sw128(cbase + I * 128 * kRowBytes, 16, 8 * kRowBytes);
-                            const uint64_t bd0 = smem_desc_sw128(bbase, 16, 8 * kRowBytes);
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)  // K = 128 state columns
+                            for (int kk = 0; kk < Cfg::kKSteps; ++kk) {  // K = the state columns
+                                const int atom = kk / 4;
+                                const uint32_t batom =
+                                    Cfg::kBSplit ? (atom < 2 ? bbase + atom * Cfg::kBAtomBytes
+                                                             : bbase1 + (atom - 2) * Cfg::kBAtomBytes)
+                                                 : bbase + atom * Cfg::kBAtomBytes;
                                 mma_f16_ss(dcol,
-                                           ad0 + (uint64_t)(((kk / 4) * Cfg::kCAtomBytes + (kk % 4) * 32) >> 4),
-                                           bd0 + (uint64_t)(((kk / 4) * Cfg::kBAtomBytes + (kk % 4) * 32) >> 4),
+                                           ad0 + (uint64_t)((atom * Cfg::kCAtomBytes + (kk % 4) * 32) >> 4),
+                                           smem_desc_sw128(batom + (kk % 4) * 32, 16, 8 * kRowBytes),
                                            kIdescCB, kk > 0 ? 1u : 0u);
+                            }
                         }
                         mma_commit(smem_u32(b_cbfull + r));
                     }
@@ -317,7 +342,7 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     // B = h^T tile [n][p]: MN-major (p contiguous), K = 16 state rows
                     const uint64_t bd0 = smem_desc_sw128(st + Cfg::kXBytes, 8 * kRowBytes, 8 * kRowBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
+                    for (int kk = 0; kk < Cfg::kKSteps; ++kk)
                         mma_f16_ss(acc, ad0 + (uint64_t)(((kk / 4) * Cfg::kCAtomBytes + (kk % 4) * 32) >> 4),
                                    bd0 + (uint64_t)((kk * 16 * kRowBytes) >> 4), kIdescS, kk > 0 ? 1u : 0u);
                     mma_commit(smem_u32(b_sdone + slot));
@@ -622,11 +647,11 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     }
 }
 
-template <int Q>
+template <int Q, int NS>
 cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void* C,
                      const float* Gcs, const float* dtT, const void* hid, const float* D, void* y,
                      cudaStream_t stream) {
-    using Cfg = CoCfg<Q>;
+    using Cfg = CoCfg<Q, NS>;
     CUtensorMap tx, tc, tb, th;
     const uint64_t xd[4] = {(uint64_t)p.P, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.b};
     const uint64_t xs[3] = {(uint64_t)p.P * 2, (uint64_t)p.H * p.P * 2,
@@ -639,7 +664,7 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
                             (uint64_t)(p.b * p.H * p.nc) * p.N * p.P * 2};
     const uint32_t box_x[4] = {64, 1, (uint32_t)Q, 1};
     const uint32_t box_b[4] = {64, 1, (uint32_t)Cfg::kBRows, 1};
-    const uint32_t box_h[4] = {64, 128, 1, 1};
+    const uint32_t box_h[4] = {64, (uint32_t)NS, 1, 1};
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
     if (!encode_tmap_4d(&tx, bf, x, xd, xs, box_x, sw) ||
@@ -651,7 +676,7 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    auto kern = compute_out_tc<Q>;
+    auto kern = compute_out_tc<Q, NS>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t units = p.b * p.nc * p.H;
@@ -675,16 +700,21 @@ cudaError_t launch_q(const Problem& p, const void* x, const void* B, const void*
 }  // namespace
 
 bool compute_out_tc_supports(const Problem& p) {
-    return p.dtype == SSD_BF16 && p.P <= 64 && p.N <= 128 && p.b * p.nc * p.H < (1LL << 31);
+    return p.dtype == SSD_BF16 && p.P <= 64 && (p.N <= 128 || (p.N <= 256 && p.Q <= 128)) &&
+           p.b * p.nc * p.H < (1LL << 31);
 }
 
 cudaError_t launch_compute_out_tc(const Problem& p, const void* x, const void* B, const void* C,
                                   const float* Gcs, const float* dtT, const void* hiddens,
                                   const float* D, void* y, cudaStream_t stream) {
+    if (p.N > 128) {   // Q <= 128 (compute_out_tc_supports)
+        return p.Q == 64 ? launch_q<64, 256>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream)
+                         : launch_q<128, 256>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+    }
     switch (p.Q) {
-        case 64: return launch_q<64>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
-        case 128: return launch_q<128>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
-        default: return launch_q<256>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+        case 64: return launch_q<64, 128>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+        case 128: return launch_q<128, 128>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
+        default: return launch_q<256, 128>(p, x, B, C, Gcs, dtT, hiddens, D, y, stream);
     }
 }
 

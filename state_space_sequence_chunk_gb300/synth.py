@@ -149,6 +149,11 @@ CONTEXT_WORKLOADS = {
     "pages_example_bf16": Workload("pages_example_bf16", 4, 16384, 8, 64, 128, 1, 128, "bf16",
                                    seed=20261202 + 5),
 }
+# The same page's chart sweeps the state size: the example problem at state
+# sizes 64 and 256 beside the 128 above (512 is outside this library's sizes).
+for _n in (64, 256):
+    CONTEXT_WORKLOADS[f"pages_example_n{_n}_bf16"] = Workload(
+        f"pages_example_n{_n}_bf16", 4, 16384, 8, 64, _n, 1, 128, "bf16", seed=20261202 + 5)
 
 
 def workload(name: str) -> Workload:

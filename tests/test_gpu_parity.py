@@ -87,6 +87,10 @@ CASES = [
     ("bf16", 128, 130, 8, 2, 64, 128, True, True),    # 4 heads per group
     ("bf16", 64, 200, 2, 2, 128, 256, True, True),    # P = 128 with the largest N
     ("bf16", 128, 300, 2, 1, 256, 256, True, True),   # largest P and N
+    # N = 256 on the tensor-core compute_out (Q <= 128)
+    ("bf16", 128, 777, 4, 2, 64, 256, True, True),    # Q = 128, ragged
+    ("bf16", 64, 500, 6, 2, 32, 256, False, True),    # Q = 64, P = 32
+    ("bf16", 128, 400, 2, 1, 64, 192, True, False),   # N = 192: padded to 256 by the TMA
     ("bf16", 256, 333, 4, 2, 256, 64, False, True),   # largest P, ragged, Q = 256
     ("f32", 64, 200, 2, 1, 256, 128, True, True),     # largest P, fp32
     ("bf16", 128, 333, 2, 1, 16, 16, True, True),     # smallest P and N
@@ -159,13 +163,15 @@ def test_workload(name):
     check_whole(name, w, inp, to_device(inp, w.dtype))
 
 
-def test_pages_example_shape():
-    """The pages' own example problem (b4, 16384 tokens, H8, P64, N128, G1,
-    chunk 128, bf16): 128 chunks per chain, so fwd_pass_state takes its
-    two-pass form; every output compared in full against the oracle."""
-    w = synth.CONTEXT_WORKLOADS["pages_example_bf16"]
+@pytest.mark.parametrize("name", list(synth.CONTEXT_WORKLOADS))
+def test_pages_example_shape(name):
+    """The pages' own example problem (b4, 16384 tokens, H8, P64, G1, chunk
+    128, bf16) at state sizes 64, 128 and 256: 128 chunks per chain, so
+    fwd_pass_state takes its two-pass form where the paired geometry allows
+    (N <= 128); every output compared in full against the oracle."""
+    w = synth.CONTEXT_WORKLOADS[name]
     inp = synth.make_inputs(w)
-    check_whole("pages_example_bf16", w, inp, to_device(inp, w.dtype))
+    check_whole(name, w, inp, to_device(inp, w.dtype))
 
 
 # --- properties -----------------------------------------------------------------
