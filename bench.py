@@ -160,18 +160,21 @@ def dram_traffic_record():
     return rec
 
 
-KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "fwd_pass_state": "fwd_pass_state_tc.cu",
-                  "compute_out": "compute_out_tc.cu", "ssd_step": "ssd_step.cu",
-                  "causal_conv1d": "causal_conv1d.cu", "gdn": "gdn_chunk.cu"}
+# The source files whose kernels serve each step (every dtype and shape path).
+KERNEL_SOURCES = {"chunk_cumsum": ["chunk_cumsum.cu"],
+                  "fwd_pass_state": ["fwd_pass_state_tc.cu", "tf32_path.cu", "simt_path.cu"],
+                  "compute_out": ["compute_out_tc.cu", "tf32_path.cu", "simt_path.cu"],
+                  "ssd_step": ["ssd_step.cu"], "causal_conv1d": ["causal_conv1d.cu"],
+                  "gdn": ["gdn_chunk.cu", "tf32_path.cu"]}
 
 
 def source_digest(kernel: str) -> str:
-    """Digest of one kernel's source file and the shared headers: a recorded
+    """Digest of one step's kernel sources and the shared headers: a recorded
     DRAM-traffic figure is valid only while this digest is unchanged."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "state_space_sequence_chunk_gb300", "csrc")
-    names = [KERNEL_SOURCES[kernel]] + sorted(n for n in os.listdir(csrc) if n.endswith(".cuh"))
+    names = KERNEL_SOURCES[kernel] + sorted(n for n in os.listdir(csrc) if n.endswith(".cuh"))
     for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
