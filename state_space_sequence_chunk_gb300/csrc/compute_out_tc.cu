@@ -583,6 +583,12 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         for (int ch = 0; ch < 8; ++ch)
                             xrow[ch] = *reinterpret_cast<const uint4*>(xr + ((ch ^ (i & 7)) << 4));
                     }
+                    // The row's values are first used after the release, and the
+                    // stage is refilled by the TMA (the async proxy): without this
+                    // fence the loads could still be outstanding when the next unit's
+                    // x lands in the stage (seen as the next unit's x in D x for the
+                    // last head of a group, Q = 256, a few calls in a hundred)
+                    fence_proxy_async_smem();
                     mbar_arrive(smem_u32(b_empty + s));
                     // y = acc + D x, 32 columns at a time, stored straight from
                     // registers: each thread writes its own row (128 contiguous
