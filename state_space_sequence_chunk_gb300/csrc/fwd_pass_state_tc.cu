@@ -160,12 +160,32 @@ __device__ __forceinline__ Piece piece_of(const Range& r, int i, const FpsParams
     return u;
 }
 
-template <bool kHasInit>
+// Long chains (many ranges per chain) run in two passes instead of handing
+// the state from range to range in order (a serial walk over every chunk of
+// the chain):
+//   kModeLocal  every piece starts from a zero state and keeps no hiddens; it
+//               writes its end state A and its log2 decay sum to the aggregate
+//               buffer (slot 2 k + [second chain of range k], per head of a
+//               pair in the paired kernel);
+//   scan        a CUDA-core kernel walks each chain's pieces in chunk order:
+//               start = S, S <- 2^{sum} S + A, replacing A by the piece's
+//               start state, and writes final_state;
+//   kModeApply  every piece starts from its start state and writes hiddens.
+// Ranges are then independent, and a chain's serial part is one fma per
+// element and piece.  A range spans at most two chains in these modes (range
+// length <= nc), so slot indices 2 k and 2 k + 1 cover every piece.
+constexpr int kModeHandoff = 0;
+constexpr int kModeLocal = 1;
+constexpr int kModeApply = 2;
+
+template <bool kHasInit, int kMode>
 __global__ void __maxnreg__(kMaxRegs)
 fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                   const float* init, const float* __restrict__ Gcs,
                   const float* __restrict__ dtT, __nv_bfloat16* __restrict__ hiddens,
-                  float* final_state, float* ring, unsigned int* ctrl, const FpsParams q) {
+                  float* final_state, float* ring, unsigned int* ctrl, float* agg,
+                  float* agg_lsum, const FpsParams q) {
+    static_assert(kMode == kModeHandoff || !kHasInit, "the two passes take the initial state in the scan");
     constexpr int S = stages<kHasInit>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -215,9 +235,9 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         fence_mbar_init();
         // chunk_cumsum (G, dt, the cleared control block) must be complete
         grid_dependency_wait();
-        // ranges in dispatch order: the range before this one belongs to a CTA
-        // that is already running
-        *range_id = (int)atomicAdd(ctrl, 1u);
+        // hand-offs need ranges in dispatch order (the range before this one
+        // belongs to a CTA that is already running); the two passes have none
+        *range_id = kMode == kModeHandoff ? (int)atomicAdd(ctrl, 1u) : (int)blockIdx.x;
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tc_fence_before();
@@ -440,8 +460,26 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 const Piece un = piece_of(rg, pi + 1, q);
                 gl_first = gfirst[(int64_t)un.bh * q.Lp + (int64_t)un.c0 * q.Q];
             }
+            // kModeLocal / kModeApply: the piece's aggregate slot
+            const int64_t aslot = 2 * (int64_t)rk + (u.ch == rg.ch_first ? 0 : 1);
+            float lsum = 0.f;   // kModeLocal: log2 of the piece's decay product
             // the piece's initial state -> TMEM slot sa
-            if (u.c0 == 0) {
+            if (kMode == kModeApply) {
+                // its start state, from the scan
+                const float* src = agg + aslot * kSlotFloats;
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float4 f = __ldcg(reinterpret_cast<const float4*>(src + ((4 * jj + q4) * 128 + rl) * 4));
+                        v[4 * q4] = __float_as_uint(f.x); v[4 * q4 + 1] = __float_as_uint(f.y);
+                        v[4 * q4 + 2] = __float_as_uint(f.z); v[4 * q4 + 3] = __float_as_uint(f.w);
+                    }
+                    __syncwarp();
+                    tmem_st_x16(sa + 16 * jj, v);
+                }
+            } else if (kMode == kModeLocal || u.c0 == 0) {
                 if (kHasInit) {
                     if (pi == 0) {  // later pieces found theirs in sa already
                         if (!take_tile(sa)) break;
@@ -482,6 +520,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             bool ok = true;
             for (int c = u.c0; c < u.c1; ++c, ++qc) {
                 const float e = exp2f(gl_next);
+                lsum += gl_next;
                 if (c + 1 < u.c1) gl_next = grow[(int64_t)(c + 1) * q.Q];
                 const int slot = qc % A;
                 if (!__all_sync(0xffffffffu, mbar_wait(acc_full(slot), (qc / A) & 1, &g_fps_error, 1u))) {
@@ -504,7 +543,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     tmem_st_x16(sa + 16 * jj, d);
                     // chunk-start state S -> hiddens[c] (row n holds S[:, n]): 16
                     // contiguous bf16 per slice (P is a multiple of 16)
-                    if (nok && p0 + 16 * jj < q.P) {
+                    if (kMode != kModeLocal && nok && p0 + 16 * jj < q.P) {
                         uint4 w0, w1;
                         w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
                         w0.y = pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3]));
@@ -525,6 +564,25 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                 mbar_arrive(acc_empty(slot));
             }
             if (!__all_sync(0xffffffffu, ok)) break;
+            if (kMode == kModeLocal) {
+                // the piece's end state and log2 decay, for the scan
+                float* dst = agg + aslot * kSlotFloats;
+#pragma unroll
+                for (int jj = 0; jj < kCols / 16; ++jj) {
+                    __syncwarp();
+                    uint32_t sv[16];
+                    tmem_ld_x16(sa + 16 * jj, sv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        __stcg(reinterpret_cast<float4*>(dst + ((4 * jj + q4) * 128 + rl) * 4),
+                               make_float4(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1]),
+                                           __uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3])));
+                }
+                if (rl == 0) agg_lsum[aslot] = lsum;
+                continue;
+            }
+            if (kMode == kModeApply) continue;   // final_state comes from the scan
             // the next piece's initial state into the spare slot, so that it can
             // start at once, before the tile buffer is reused below
             const bool next_tile = kHasInit && pi + 1 < rg.pieces() && piece_of(rg, pi + 1, q).c0 == 0;
@@ -656,23 +714,6 @@ __host__ __device__ constexpr int pair_smem() {
 }
 constexpr uint32_t kIdescPair = make_idesc(1, 128, 2 * kCols, 1, 1);
 
-// Long chains (many ranges per chain) run in two passes instead of handing
-// the state from range to range in order (a serial walk over every chunk of
-// the chain):
-//   kModeLocal  every piece starts from a zero state and keeps no hiddens; it
-//               writes its end state A and its log2 decay sum to the aggregate
-//               buffer (one slot per head of piece 2 k + [second chain of
-//               range k]);
-//   scan        a CUDA-core kernel walks each head's pieces in chunk order:
-//               start = S, S <- 2^{sum} S + A, replacing A by the piece's
-//               start state, and writes final_state;
-//   kModeApply  every piece starts from its start state and writes hiddens.
-// Ranges are then independent, and a chain's serial part is one fma per
-// element and piece.  A range spans at most two chains here (range length <=
-// nc), so slot indices 2 k and 2 k + 1 cover every piece.
-constexpr int kModeHandoff = 0;
-constexpr int kModeLocal = 1;
-constexpr int kModeApply = 2;
 static_assert(kPStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 
 template <bool kTmaH, int kMode>
@@ -1103,28 +1144,43 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 }
 
 // The scan between the two passes (CUDA cores).  Thread = one element of a
-// head's state in the aggregate-slot layout (float4 column group, TMEM lane,
-// component), blockIdx.y = batch * H + head.  It walks the head's pieces in
-// chunk order (ranges k = the one holding the chain's first unit, k + 1, ...):
-// start = S, S <- 2^{sum} S + A, with the piece's start state written over A.
-// S begins at init_state (or zero) and ends as final_state.  The pieces'
-// slots and decays are staged in shared memory, kScanBatch at a time, and
-// each thread loads the batch's A values before its serial fma chain, so that
-// the loads overlap instead of queueing behind one another.
+// chain's state in the aggregate-slot layout (float4 column group, TMEM lane,
+// component); blockIdx.y = the chain: batch * H + head for the paired kernel
+// (its chains are head pairs, its slots per head), the chain itself for the
+// one-head kernel (a 128-row block of N by a 64-column block of P of one
+// head).  It walks the chain's pieces in chunk order (ranges k = the one
+// holding the chain's first unit, k + 1, ...): start = S, S <- 2^{sum} S + A,
+// with the piece's start state written over A.  S begins at init_state (or
+// zero) and ends as final_state.  The pieces' slots and decays are staged in
+// shared memory, kScanBatch at a time, and each thread loads the batch's A
+// values before its serial fma chain, so that the loads overlap instead of
+// queueing behind one another.
 constexpr int kScanBatch = 32;
+template <bool kPair>
 __global__ void __launch_bounds__(256)
 fwd_pass_state_scan(const float* init, float* agg, const float* __restrict__ agg_lsum,
                     float* final_state, const FpsParams q) {
     __shared__ int s_slot[kScanBatch];
     __shared__ float s_decay[kScanBatch];
     const int f = blockIdx.x * blockDim.x + threadIdx.x;
-    const int bh = blockIdx.y, pc = bh >> 1, hd = bh & 1;
-    const int n = (f >> 2) & 127, p = (f >> 9) * 4 + (f & 3);
+    int pc, hd, bh, n, p;
+    if (kPair) {
+        bh = blockIdx.y; pc = bh >> 1; hd = bh & 1;
+        n = (f >> 2) & 127;
+        p = (f >> 9) * 4 + (f & 3);
+    } else {
+        pc = blockIdx.y; hd = 0;
+        const int rb = pc / q.npb, pb = pc - rb * q.npb;
+        bh = rb / q.nmb;
+        const int mb = rb - bh * q.nmb;
+        n = mb * 128 + ((f >> 2) & 127);
+        p = pb * kCols + (f >> 9) * 4 + (f & 3);
+    }
     const bool live = f < kSlotFloats;
     const bool valid = live && p < q.P && n < q.N;
     const int64_t sidx = ((int64_t)bh * q.P + p) * q.N + n;
     float S = (init != nullptr && valid) ? init[sidx] : 0.f;
-    const int u0 = pc * q.nc, u1 = u0 + q.nc;   // the pair-chain's units
+    const int u0 = pc * q.nc, u1 = u0 + q.nc;   // the chain's units
     auto range_lo = [&](int k) { return (int)((long long)k * q.W / q.G); };
     int k0 = (int)((long long)u0 * q.G / q.W);
     while (k0 + 1 < q.G && range_lo(k0 + 1) <= u0) ++k0;
@@ -1136,7 +1192,8 @@ fwd_pass_state_scan(const float* init, float* agg, const float* __restrict__ agg
         __syncthreads();   // the previous batch's table has been read
         if ((int)threadIdx.x < nb) {
             const int k = kb + (int)threadIdx.x;
-            const int slot = (2 * k + (range_lo(k) / q.nc == pc ? 0 : 1)) * 2 + hd;
+            const int piece = 2 * k + (range_lo(k) / q.nc == pc ? 0 : 1);
+            const int slot = kPair ? piece * 2 + hd : piece;
             s_slot[threadIdx.x] = slot;
             s_decay[threadIdx.x] = exp2f(__ldcg(agg_lsum + slot));
         }
@@ -1203,20 +1260,26 @@ bool pair_geometry(const Problem& p) {
 }
 bool paired(const Problem& p) { return pair_geometry(p); }
 
-// Two passes for long chains (the paired kernel's local and apply modes with
-// the scan between them), with an initial state or without.  The workspace
-// holds the aggregate slots for up to kTwoPassMaxCtas ranges whenever a
-// problem could take this path; whether it does depends on the device's SM
-// count (a range must not span more than two chains).
+// Two passes for long chains (the local and apply modes with the scan between
+// them), with an initial state or without, for either kernel.  The workspace
+// holds kAggSlots aggregate slots whenever a problem could take this path:
+// enough for 256 ranges of the paired kernel (four slots each: two pieces by
+// two heads) or 512 of the one-head kernel (two each).  Whether a problem takes
+// it depends on the device's SM count (a range must not span more than two
+// chains).
 constexpr int kTwoPassMinChunks = 64;
-constexpr int kTwoPassMaxCtas = 256;
+constexpr int kAggSlots = 1024;
 bool two_pass_candidate(const Problem& p) {
-    return p.dtype == SSD_BF16 && pair_geometry(p) && p.nc >= kTwoPassMinChunks;
+    return p.dtype == SSD_BF16 && p.nc >= kTwoPassMinChunks;
 }
-size_t agg_state_bytes() { return round_up256((size_t)2 * kTwoPassMaxCtas * 2 * kSlotFloats * 4); }
+size_t agg_state_bytes() { return round_up256((size_t)kAggSlots * kSlotFloats * 4); }
 size_t agg_bytes(const Problem& p) {
-    return two_pass_candidate(p) ? agg_state_bytes() + round_up256((size_t)2 * kTwoPassMaxCtas * 2 * 4)
-                                 : 0;
+    return two_pass_candidate(p) ? agg_state_bytes() + round_up256((size_t)kAggSlots * 4) : 0;
+}
+// Ranges of at most half a chain (so that every chain spans two or more
+// ranges and no range spans more than two chains), within the slot capacity.
+bool two_pass_fits(int64_t W, int64_t G, int64_t nc, int slots_per_range) {
+    return G > 0 && (W + G - 1) / G <= nc / 2 && G * slots_per_range <= kAggSlots;
 }
 
 }  // namespace
@@ -1267,13 +1330,13 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    bool two_pass = false;
-    if (two_pass_candidate(p)) {
+    float* agg = two_pass_candidate(p) ? (float*)((char*)scratch + ring_bytes(p) + ctrl_bytes(p)) : nullptr;
+    float* lsum = agg != nullptr ? (float*)((char*)agg + agg_state_bytes()) : nullptr;
+    if (paired(p)) {
         const int64_t W2 = (int64_t)(q.nchains / 2) * p.nc;
-        const int64_t G2 = std::min<int64_t>(std::min<int64_t>(W2, sms), kTwoPassMaxCtas);
-        two_pass = (W2 + G2 - 1) / G2 <= p.nc / 2;   // two or more ranges per chain
-    }
-    if (two_pass || paired(p)) {
+        const int64_t G2 = std::min<int64_t>(std::min<int64_t>(W2, sms), kAggSlots / 4);
+        const bool two_pass = two_pass_candidate(p) && two_pass_fits(W2, G2, p.nc, 4) &&
+                              p.b * p.H <= 65535;   // the scan's grid rows
         // one CTA per SM; a chain is a pair of heads (its flags and hand-off
         // slots stay per head: chains() counts heads)
         // P = 64: hiddens leave through TMA stores of [N rows][64 p] tiles
@@ -1290,8 +1353,7 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
         }
         q.nchains /= 2;
         q.W = q.nchains * q.nc;
-        q.G = std::min(q.W, sms);
-        if (two_pass) q.G = std::min(q.G, kTwoPassMaxCtas);
+        q.G = two_pass ? (int)G2 : std::min(q.W, sms);
         cfg.gridDim = dim3((unsigned)q.G);
         cfg.blockDim = dim3(kPThreads);
         using PairKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, const float*,
@@ -1314,12 +1376,10 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
                                        nullptr, nullptr)
                          : launch_pair(fwd_pass_state_pair_tc<false, kModeHandoff>, pair_smem<false>(),
                                        nullptr, nullptr);
-        float* agg = (float*)((char*)scratch + ring_bytes(p) + ctrl_bytes(p));
-        float* lsum = (float*)((char*)agg + agg_state_bytes());
         if ((e = launch_pair(fwd_pass_state_pair_tc<false, kModeLocal>, pair_smem<false>(), agg,
                              lsum)) != cudaSuccess)
             return e;
-        fwd_pass_state_scan<<<dim3((kSlotFloats + 255) / 256, (unsigned)(p.b * p.H)), 256, 0, stream>>>(
+        fwd_pass_state_scan<true><<<dim3((kSlotFloats + 255) / 256, (unsigned)(p.b * p.H)), 256, 0, stream>>>(
             init, agg, lsum, final_state, q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         cfg.numAttrs = p.chained ? 1 : 0;   // the apply pass may set up while the scan runs
@@ -1327,23 +1387,45 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
                      : launch_pair(fwd_pass_state_pair_tc<false, kModeApply>, pair_smem<false>(), agg,
                                    lsum);
     }
-    auto kern = init != nullptr ? fwd_pass_state_tc<true> : fwd_pass_state_tc<false>;
-    const int smem = init != nullptr ? smem_bytes<true>() : smem_bytes<false>();
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
+    // one-head kernel: two CTAs per SM
     int resident = 0;
     if ((e = resident_ctas(&resident)) != cudaSuccess) return e;
     q.W = q.nchains * q.nc;
-    q.G = std::min(q.W, resident);
+    const int64_t G1 = std::min<int64_t>(std::min<int64_t>(q.W, resident), kAggSlots / 2);
+    const bool two_pass = two_pass_candidate(p) && two_pass_fits(q.W, G1, p.nc, 2) &&
+                          q.nchains <= 65535;   // the scan's grid rows
+    q.G = two_pass ? (int)G1 : std::min(q.W, resident);
     cfg.gridDim = dim3((unsigned)q.G);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    e = cudaLaunchKernelEx(&cfg, kern, tx, tb, init, Gcs, dtT, (__nv_bfloat16*)hiddens,
-                           final_state, ring, ctrl, q);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    using OneKernel = void (*)(CUtensorMap, CUtensorMap, const float*, const float*, const float*,
+                               __nv_bfloat16*, float*, float*, unsigned int*, float*, float*, FpsParams);
+    auto launch_one = [&](OneKernel k1, int smem, const float* init_in, float* fin, float* ag,
+                          float* ls) -> cudaError_t {
+        cudaError_t le;
+        if ((le = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+                cudaSuccess ||   // all of the unified L1/shared storage as shared memory
+            (le = cudaFuncSetAttribute(k1, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return le;
+        cfg.dynamicSmemBytes = (size_t)smem;
+        le = cudaLaunchKernelEx(&cfg, k1, tx, tb, init_in, Gcs, dtT, (__nv_bfloat16*)hiddens, fin, ring,
+                                ctrl, ag, ls, q);
+        return le != cudaSuccess ? le : cudaGetLastError();
+    };
+    if (!two_pass)
+        return init != nullptr
+                   ? launch_one(fwd_pass_state_tc<true, kModeHandoff>, smem_bytes<true>(), init,
+                                final_state, nullptr, nullptr)
+                   : launch_one(fwd_pass_state_tc<false, kModeHandoff>, smem_bytes<false>(), nullptr,
+                                final_state, nullptr, nullptr);
+    if ((e = launch_one(fwd_pass_state_tc<false, kModeLocal>, smem_bytes<false>(), nullptr, nullptr, agg,
+                        lsum)) != cudaSuccess)
+        return e;
+    fwd_pass_state_scan<false><<<dim3((kSlotFloats + 255) / 256, (unsigned)q.nchains), 256, 0, stream>>>(
+        init, agg, lsum, final_state, q);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_one(fwd_pass_state_tc<false, kModeApply>, smem_bytes<false>(), nullptr, nullptr, agg,
+                      lsum);
 }
 
 cudaError_t set_fwd_pass_state_withhold(unsigned int on) {

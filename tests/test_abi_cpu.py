@@ -72,16 +72,19 @@ def test_workspace_bytes(lib):
     chains2 = 2 * 4 * 2
     assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(d2)) == (
         ru(chains2 * 2 * 128 * 128 * 4) + ru((32 + chains2) * 4))
-    # long chains (nc >= 64, paired-head geometry): + aggregate slots for up to
-    # 256 ranges (two fp32 state slots of 128 x 64 per range and head pair) and
-    # their log2 decay sums
+    # long chains (nc >= 64, either kernel): + 1024 aggregate slots (fp32 states
+    # of 128 x 64: four per range of the paired kernel, two per range of the
+    # one-head kernel) and their log2 decay sums
     dl = dims(seqlen=64 * 128)
     chains_l = 2 * 4
-    agg = ru(2 * 256 * 2 * 128 * 64 * 4) + ru(2 * 256 * 2 * 4)
+    agg = ru(1024 * 128 * 64 * 4) + ru(1024 * 4)
     assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(dl)) == (
         ru(chains_l * 2 * 128 * 64 * 4) + ru((32 + chains_l) * 4) + agg)
-    dodd = dims(seqlen=64 * 128, ngroups=4)   # one head per group: no pairs
+    dodd = dims(seqlen=64 * 128, ngroups=4)   # one head per group: the one-head kernel
     assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(dodd)) == (
+        ru(chains_l * 2 * 128 * 64 * 4) + ru((32 + chains_l) * 4) + agg)
+    dshort = dims(seqlen=63 * 128, ngroups=4)   # 63 chunks: no two-pass form
+    assert lib.ssd_fwd_pass_state_scratch_bytes(ctypes.byref(dshort)) == (
         ru(chains_l * 2 * 128 * 64 * 4) + ru((32 + chains_l) * 4))
     # the largest head and state sizes are accepted (P, N up to 256)
     assert ssd.ssd_fwd_workspace_bytes(dims(headdim=256, dstate=256)) > 0

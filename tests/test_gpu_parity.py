@@ -104,6 +104,11 @@ CASES = [
     # long chains: local pass, scan over each chain's ranges, apply pass
     ("bf16", 128, 15999, 4, 2, 64, 128, True, True),  # with an initial state, ragged
     ("bf16", 256, 20000, 2, 1, 32, 64, False, True),  # ~76 ranges per chain, P = 32
+    # long chains on the one-head kernel (unpaired heads, P > 64 or N > 128)
+    ("bf16", 64, 4096, 3, 3, 64, 128, True, True),    # odd heads: ranges of one or two chunks
+    ("bf16", 128, 9000, 2, 1, 128, 64, False, True),  # two 64-column blocks of P, ragged
+    ("bf16", 128, 8300, 2, 1, 64, 256, True, False),  # two 128-row blocks of N, ragged
+    ("bf16", 64, 40000, 1, 1, 64, 192, True, True),   # N = 192 (padded rows), ~8 chunks per range
 ]
 
 
