@@ -246,8 +246,10 @@ struct CoTf32 {
     int L, H, P, N, G, Q, nc, Lp, hpg;
     int KB;                      // keys per block: min(Q, 128)
     int nblk;                    // query blocks per chunk: Q / 128 (1 for Q <= 128)
+    int pt, npt;                 // columns of P per CTA (<= 64 when P > 64), column tiles
+    int crows;                   // rows of the C_I tile: min(Q, 128)
     uint32_t tmem_cols;
-    uint32_t scol;               // first TMEM column of S / A (acc holds columns [0, P))
+    uint32_t scol;               // first TMEM column of S / A (acc holds columns [0, pt))
     int c_bytes, b_bytes, h_bytes, x_bytes;   // C_I, B_J, h^T, (dt o X_J)^T tiles
     int x_sep;                   // 1: (dt o X)^T has a tile of its own (written up front);
                                  // 0: it reuses h^T's, once C h^T is done
@@ -333,14 +335,16 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     uint64_t* bar = reinterpret_cast<uint64_t*>(dv + q.Q);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int I = blockIdx.x, c = blockIdx.y, bh = blockIdx.z;
+    const int I = blockIdx.x / q.npt, c = blockIdx.y, bh = blockIdx.z;
+    const int p0 = (blockIdx.x - I * q.npt) * q.pt;          // this CTA's columns of P
+    const int pc = min(q.pt, q.P - p0);
     const int b = bh / q.H, h = bh % q.H, grp = h / q.hpg;
     const int t0 = c * q.Q;              // first token of the chunk
     const int i0 = I * 128;              // first query row of the block (in the chunk)
     const int64_t bc_stride = (int64_t)q.G * q.N;            // token stride of B and C
     const float* Cb = C + ((int64_t)b * q.L * q.G + grp) * q.N;
     const float* Bb = B + ((int64_t)b * q.L * q.G + grp) * q.N;
-    const float* xb = x + ((int64_t)b * q.L * q.H + h) * q.P;  // token t at xb + t H P
+    const float* xb = x + ((int64_t)b * q.L * q.H + h) * q.P + p0;  // token t at xb + t H P
     const int64_t x_stride = (int64_t)q.H * q.P;
 
     if (tid == 0) {
@@ -358,20 +362,23 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
             dv[i] = dtT[(int64_t)bh * q.Lp + t0 + i];
         }
     }
-    // C_I (rows = query rows) and B_0 (rows = keys)
-    put_rows(ct, 128, Cb + (int64_t)(t0 + i0) * bc_stride, bc_stride,
+    // C_I (rows = query rows) and B_0 (rows = keys).  With Q < 128 the C_I tile
+    // has Q rows; the M = 128 products read 128 rows from it regardless, and
+    // the rows past Q (whatever shared memory follows the tile) only reach
+    // accumulator lanes that are never used.
+    put_rows(ct, q.crows, Cb + (int64_t)(t0 + i0) * bc_stride, bc_stride,
              min(min(q.Q - i0, 128), q.L - (t0 + i0)), q.N, tid);
     put_rows(bt, q.KB, Bb + (int64_t)t0 * bc_stride, bc_stride, min(q.KB, q.L - t0), q.N, tid);
     // h^T: rows = p, K = state n (hiddens holds [n][p])
-    const float* hb = hiddens + ((int64_t)bh * q.nc + c) * (int64_t)q.N * q.P;
-    put_transposed(ht, q.P, q.N, q.P, [&](int n) { return hb + (int64_t)n * q.P; },
+    const float* hb = hiddens + ((int64_t)bh * q.nc + c) * (int64_t)q.N * q.P + p0;
+    put_transposed(ht, pc, q.N, pc, [&](int n) { return hb + (int64_t)n * q.P; },
                    [](int) { return 1.f; }, lane, warp);
     // (dt o X_J)^T: rows = p, K = keys of block J (zero past the sequence end)
     // (reads dv: the first call follows a barrier after dv is written; no
     // barrier inside, since later calls sit under the per-thread `ok`)
     auto put_x = [&](int J) {
         put_transposed(
-            xt, q.P, q.KB, q.P,
+            xt, pc, q.KB, pc,
             [&](int k) {
                 const int t = t0 + J * q.KB + k;
                 return t < q.L ? xb + (int64_t)t * x_stride : nullptr;
@@ -388,15 +395,15 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const uint32_t acc = tmem, sreg = tmem + q.scol;
-    const uint32_t idesc_p = make_idesc(2, 128, (uint32_t)q.P, 0, 0);
+    const uint32_t idesc_p = make_idesc(2, 128, (uint32_t)pc, 0, 0);
     const uint32_t idesc_k = make_idesc(2, 128, (uint32_t)q.KB, 0, 0);
     const int nk_state = q.N / 8;
     if (tid == 0) {
         for (int kk = 0; kk < nk_state; ++kk)
-            mma_tf32_ss(acc, kmajor_desc(ct, kk, 128), kmajor_desc(ht, kk, q.P), idesc_p,
+            mma_tf32_ss(acc, kmajor_desc(ct, kk, q.crows), kmajor_desc(ht, kk, pc), idesc_p,
                         kk > 0 ? 1u : 0u);
         for (int kk = 0; kk < nk_state; ++kk)
-            mma_tf32_ss(sreg, kmajor_desc(ct, kk, 128), kmajor_desc(bt, kk, q.KB), idesc_k,
+            mma_tf32_ss(sreg, kmajor_desc(ct, kk, q.crows), kmajor_desc(bt, kk, q.KB), idesc_k,
                         kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(bar));
     }
@@ -416,7 +423,7 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
         if (J == 0) {
             // acc *= 2^{g_i}
             const float sg = exp2f(gi);
-            for (int c0 = 0; c0 < q.P; c0 += 16) {
+            for (int c0 = 0; c0 < pc; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld_x16(acc + lane_off + c0, v);
                 tmem_wait_ld();
@@ -449,7 +456,7 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
         if (tid == 0 && ok) {
             tc_fence_after();
             for (int kk = 0; kk < q.KB / 8; ++kk)
-                mma_tf32_ts(acc, sreg + kk * 8, kmajor_desc(xt, kk, q.P), idesc_p, 1u);
+                mma_tf32_ts(acc, sreg + kk * 8, kmajor_desc(xt, kk, pc), idesc_p, 1u);
             mma_commit(smem_u32(bar));
         }
         if (J + 1 < nJ) {
@@ -465,7 +472,7 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
             if (tid == 0 && ok) {
                 tc_fence_after();
                 for (int kk = 0; kk < nk_state; ++kk)
-                    mma_tf32_ss(sreg, kmajor_desc(ct, kk, 128), kmajor_desc(bt, kk, q.KB), idesc_k,
+                    mma_tf32_ss(sreg, kmajor_desc(ct, kk, q.crows), kmajor_desc(bt, kk, q.KB), idesc_k,
                                 kk > 0 ? 1u : 0u);
                 mma_commit(smem_u32(bar));
             }
@@ -477,16 +484,16 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     const bool store = row_ok && t < q.L;
     const float dh = D ? D[h] : 0.f;
     const float* xr = xb + (int64_t)(store ? t : 0) * x_stride;
-    float* yr = y + ((int64_t)b * q.L * q.H + h) * q.P + (int64_t)(store ? t : 0) * x_stride;
+    float* yr = y + ((int64_t)b * q.L * q.H + h) * q.P + p0 + (int64_t)(store ? t : 0) * x_stride;
     float4 xv[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) xv[u] = (store && 4 * u < q.P) ? ldg4(xr + 4 * u) : zero4();
+    for (int u = 0; u < 16; ++u) xv[u] = (store && 4 * u < pc) ? ldg4(xr + 4 * u) : zero4();
     chain_wait(smem_u32(bar), phase, ok);   // the last acc += A X
     tc_fence_after();
     __syncwarp();
 #pragma unroll
     for (int c0 = 0; c0 < 128; c0 += 16) {
-        if (c0 >= q.P) break;
+        if (c0 >= pc) break;
         uint32_t v[16];
         tmem_ld_x16(acc + lane_off + c0, v);
         tmem_wait_ld();
@@ -895,18 +902,32 @@ namespace {
 int co_tf32_layout(CoTf32& q) {
     q.KB = q.Q < 128 ? q.Q : 128;
     q.nblk = q.Q > 128 ? q.Q / 128 : 1;
-    q.scol = (uint32_t)((q.P + 31) / 32 * 32);
+    // P > 64 is split into 64-column tiles (one CTA each): half the h^T and X
+    // tiles per CTA, so that two CTAs share an SM
+    q.pt = q.P > 64 ? 64 : q.P;
+    q.npt = (q.P + q.pt - 1) / q.pt;
+    q.crows = q.Q < 128 ? q.Q : 128;
+    q.scol = (uint32_t)((q.pt + 31) / 32 * 32);
     q.tmem_cols = tmem_cols_for((int)q.scol + q.KB);
-    q.c_bytes = up1024(tile_bytes(128, q.N));
+    q.c_bytes = up1024(tile_bytes(q.crows, q.N));
     q.b_bytes = up1024(tile_bytes(q.KB, q.N));
-    q.h_bytes = up1024(tile_bytes(q.P, q.N));
-    q.x_bytes = up1024(tile_bytes(q.P, q.KB));
+    const int h_own = up1024(tile_bytes(q.pt, q.N));
+    q.x_bytes = up1024(tile_bytes(q.pt, q.KB));
     const int extras = 2 * q.Q * 4 + 64 + 1024;
-    q.x_sep = q.c_bytes + q.b_bytes + q.h_bytes + q.x_bytes + extras <= 200 * 1024;
-    if (!q.x_sep) q.h_bytes = std::max(q.h_bytes, q.x_bytes);   // one tile for both
-    const int smem = q.c_bytes + q.b_bytes + q.h_bytes + (q.x_sep ? q.x_bytes : 0) + extras;
+    const int sep = q.c_bytes + q.b_bytes + h_own + q.x_bytes + extras;
+    const int shared = q.c_bytes + q.b_bytes + std::max(h_own, q.x_bytes) + extras;
+    // a tile of its own for X unless sharing h^T's lets more CTAs onto an SM
+    const int per_sm = 228 * 1024;
+    q.x_sep = sep <= 200 * 1024 && per_sm / (sep + 1024) >= per_sm / (shared + 1024);
+    q.h_bytes = q.x_sep ? h_own : std::max(h_own, q.x_bytes);
+    int smem = q.x_sep ? sep : shared;
+    // the M = 128 products read 128 rows of the C_I tile from each K atom's
+    // start: with fewer rows that runs past the tile, which must stay inside
+    // the allocation
+    const int c_read = ((q.N + 31) / 32 - 1) * q.crows * kRowBytes + 16 * 1024;
+    smem = std::max(smem, c_read + extras);
     const int by_tmem = 512 / (int)q.tmem_cols;
-    const int smem_cta = std::max(smem, (228 * 1024) / by_tmem - 1024);
+    const int smem_cta = std::max(smem, per_sm / by_tmem - 1024);
     return smem_cta > 227 * 1024 ? -1 : smem_cta;
 }
 }  // namespace
@@ -922,7 +943,7 @@ cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void*
     cudaError_t e = cudaFuncSetAttribute(compute_out_tf32<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
     if (e != cudaSuccess) return e;
-    compute_out_tf32<false><<<dim3((unsigned)q.nblk, (unsigned)p.nc, (unsigned)(p.b * p.H)),
+    compute_out_tf32<false><<<dim3((unsigned)(q.nblk * q.npt), (unsigned)p.nc, (unsigned)(p.b * p.H)),
                               kThreads, (size_t)smem_cta, stream>>>(
         (const float*)x, (const float*)B, (const float*)C, Gcs, dtT, (const float*)hiddens, D,
         (float*)y, q, host_timeout_word());
@@ -946,7 +967,7 @@ cudaError_t launch_gdn_fwd_o_tf32(const GdnProblem& p, const float* qm, const fl
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
     if (e != cudaSuccess) return e;
     // operand roles: C <- q, B <- k, x <- v_new, hiddens <- h, y <- o, Gcs <- g
-    compute_out_tf32<true><<<dim3((unsigned)q.nblk, (unsigned)p.NT, (unsigned)(p.B * p.H)),
+    compute_out_tf32<true><<<dim3((unsigned)(q.nblk * q.npt), (unsigned)p.NT, (unsigned)(p.B * p.H)),
                              kThreads, (size_t)smem_cta, stream>>>(
         v_new, k, qm, g, nullptr, h, nullptr, o, q, host_timeout_word());
     return cudaGetLastError();
