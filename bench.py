@@ -122,20 +122,26 @@ def job_throughput(world: int, tokens_per_rank: int, ms_per_step: float) -> floa
 
 
 def launches_per_step(w: synth.Workload, sms: int) -> int:
-    """Kernels one ssd_fwd enqueues: three for bf16, or five when fwd_pass_state
-    takes its two-pass form for long chains (same rule as the library's
-    launcher); four for fp32, whose fwd_pass_state is chunk products + scan."""
+    """Kernels one ssd_fwd enqueues (same rules as the library's launchers):
+    three for bf16 (chunk_cumsum, fwd_pass_state, compute_out), five when
+    fwd_pass_state takes its two-pass form for long chains (local pass, scan,
+    apply pass) on either of its kernels; four for fp32 (chunk products and scan
+    for step 2)."""
     if w.dtype != "bf16":
         return 4
     hpg = w.nheads // w.ngroups
     nc = -(-w.seqlen // w.chunk)
-    if (w.dtype == "bf16" and w.dstate <= 128 and w.headdim <= 64 and w.nheads % 2 == 0
-            and hpg % 2 == 0 and nc >= 64):
+    paired = w.dstate <= 128 and w.headdim <= 64 and w.nheads % 2 == 0 and hpg % 2 == 0
+    if paired:
+        rows = w.batch * w.nheads                 # the scan's grid rows
         W = w.batch * w.nheads // 2 * nc
-        G = min(W, sms, 256)
-        if -(-W // G) <= nc // 2:
-            return 5
-    return 3
+        G = min(W, sms, 1024 // 4)
+    else:
+        rows = w.batch * w.nheads * -(-w.dstate // 128) * -(-w.headdim // 64)
+        W = rows * nc
+        G = min(W, 2 * sms, 1024 // 2)            # two CTAs per SM
+    two = nc >= 64 and G > 0 and -(-W // G) <= nc // 2 and rows <= 65535
+    return 5 if two else 3
 
 
 def measured_peaks():

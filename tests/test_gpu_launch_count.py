@@ -1,7 +1,8 @@
 """The number of this library's kernels one ssd_fwd launches, as seen by the
 CUDA profiler, equals the count bench.py reports as ``gpu_launches`` per step
 (``launches_per_step``): three for bf16, five when fwd_pass_state takes its
-two-pass form for long chains, four for fp32 (chunk products and scan)."""
+two-pass form for long chains (on either of its kernels), four for fp32 (chunk
+products and scan)."""
 import re
 
 import pytest
@@ -24,6 +25,8 @@ CASES = {
                                             dstate=128, chunk=64, dtype="bf16", init_std=0.0),
     "bf16, P = 128 (one-head kernel, CUDA-core compute_out)": small(seqlen=300, headdim=128,
                                                                      dstate=64, dtype="bf16"),
+    "bf16, N = 256, long chains (one-head kernel, two passes)": small(
+        seqlen=64 * 64, nheads=2, ngroups=1, headdim=64, dstate=256, chunk=64, dtype="bf16"),
     "fp32": small(seqlen=500, headdim=32, dstate=16, chunk=64, dtype="f32"),
 }
 
