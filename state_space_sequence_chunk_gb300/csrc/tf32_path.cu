@@ -541,6 +541,11 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
 // read as zero rows, so their v_new and gated terms vanish.
 // ===========================================================================
 constexpr int kGdnVt = 64;   // V columns per CTA (TMEM lanes 0..63)
+// Eight warps: warps 0, 1, 4, 5 reach TMEM lanes 0..63 (the tile's columns of
+// V) and split the per-chunk state work by columns; warps 2, 3, 6, 7 issue the
+// copies; every warp shares the conversions and the stores.
+constexpr int kGdnThreads = 256;
+constexpr int kGdnWarps = kGdnThreads / 32;
 
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
@@ -554,7 +559,7 @@ struct GdnH {
     uint32_t tmem_cols;
 };
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kGdnThreads)
 gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
                const float* __restrict__ u, const float* __restrict__ g,
                const float* __restrict__ h0, float* __restrict__ hout, float* __restrict__ v_new,
@@ -577,9 +582,12 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v0 = blockIdx.x * kGdnVt, bh = blockIdx.y, b = bh / q.H, h = bh % q.H;
-    const int v = v0 + tid;                           // this thread's column of V (warps 0, 1)
-    const bool lane_ok = tid < kGdnVt && v < q.V;
-    const bool state_warp = warp < kGdnVt / 32;       // warps whose TMEM lanes hold the tile
+    const int vl = (warp & 3) * 32 + lane;            // this thread's TMEM lane
+    const bool state_warp = (warp & 3) < kGdnVt / 32; // warps whose TMEM lanes hold the tile
+    const int half = warp >> 2;                       // state warps: which share of the columns
+    const int v = v0 + vl;                            // state warps: this thread's column of V
+    const bool lane_ok = state_warp && v < q.V;
+    const int nsi = half * 64 + (tid & 63);           // copy warps: index among the 128
     const int vt = min(kGdnVt, q.V - v0);             // columns of this tile (a multiple of 16)
     const int v4s = vt / 4;
     const int64_t tok_stride_k = (int64_t)q.H * q.K, tok_stride_v = (int64_t)q.H * q.V;
@@ -596,23 +604,23 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
     if (warp == 0) tmem_alloc(smem_u32(tmem_holder), q.tmem_cols);
     // asynchronous copies of chunk c: w rows into their swizzled operand tile
     // (buffer c & 1), raw k rows and g (zero past the end)
-    auto stage_wkg = [&](int c, int i0, int ni) {   // issued by threads [i0, i0 + ni)
+    auto stage_wkg = [&](int c, int i, int ni) {   // issued by thread i of ni
         const int t0 = c * q.C, nv = min(q.C, q.T - t0), k4s = q.K / 4;
         const uint32_t wt = s0 + (c & 1) * buf_bytes;
-        for (int e = tid - i0; e < q.C * k4s; e += ni) {
+        for (int e = i; e < q.C * k4s; e += ni) {
             const int t = e / k4s, k4 = e - t * k4s;
             const bool in = t < nv;
             const int64_t off = (int64_t)(t0 + (in ? t : 0)) * tok_stride_k + 4 * k4;
             cp_async_16(wt + swz(t, 4 * k4, q.C), wb + off, in ? 16u : 0u);
             cp_async_16(smem_u32(kraw + t * kpitch + 4 * k4), kb + off, in ? 16u : 0u);
         }
-        for (int t = tid - i0; t < q.C; t += ni)
+        for (int t = i; t < q.C; t += ni)
             cp_async_4(smem_u32(gstage + t), gb + (int64_t)(t0 + min(t, nv - 1)) * q.H, 4u);
     };
     // the u tile of chunk c: [C][vt]
-    auto stage_u = [&](int c, int i0, int ni) {   // issued by threads [i0, i0 + ni)
+    auto stage_u = [&](int c, int i, int ni) {   // issued by thread i of ni
         const int t0 = c * q.C, nv = min(q.C, q.T - t0);
-        for (int e = tid - i0; e < q.C * v4s; e += ni) {
+        for (int e = i; e < q.C * v4s; e += ni) {
             const int t = e / v4s, v4 = e - t * v4s;
             const bool in = t < nv;
             cp_async_16(smem_u32(ubuf + t * kGdnVt + 4 * v4),
@@ -625,11 +633,11 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
     auto convert = [&](int c) {
         const uint32_t wt = s0 + (c & 1) * buf_bytes, kt = wt + q.w_bytes;
         const int k4s = q.K / 4, total = q.C * k4s;
-        for (int e0 = tid; e0 < total; e0 += kThreads * 8) {
+        for (int e0 = tid; e0 < total; e0 += kGdnThreads * 8) {
             uint4 x[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int e = e0 + j * kThreads, t = e / k4s, k4 = e - t * k4s;
+                const int e = e0 + j * kGdnThreads, t = e / k4s, k4 = e - t * k4s;
                 if (e < total)
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(x[j].x), "=r"(x[j].y), "=r"(x[j].z), "=r"(x[j].w)
@@ -637,7 +645,7 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int e = e0 + j * kThreads, t = e / k4s, k4 = e - t * k4s;
+                const int e = e0 + j * kGdnThreads, t = e / k4s, k4 = e - t * k4s;
                 if (e < total)
                     st_shared_v4(wt + swz(t, 4 * k4, q.C), to_tf32(__uint_as_float(x[j].x)),
                                  to_tf32(__uint_as_float(x[j].y)), to_tf32(__uint_as_float(x[j].z)),
@@ -646,17 +654,17 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         }
         for (int t0 = 0; t0 < q.C; t0 += 32) {               // k^T: rows k, lanes take tokens t
             const int t = t0 + lane;
-            for (int k40 = warp; k40 < k4s; k40 += 4 * 8) {
+            for (int k40 = warp; k40 < k4s; k40 += kGdnWarps * 8) {
                 float4 x[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int k4 = k40 + 4 * j;
+                    const int k4 = k40 + kGdnWarps * j;
                     x[j] = (t < q.C && k4 < k4s) ? *reinterpret_cast<const float4*>(kraw + t * kpitch + 4 * k4)
                                                  : zero4();
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int k4 = k40 + 4 * j;
+                    const int k4 = k40 + kGdnWarps * j;
                     if (t < q.C && k4 < k4s) {
                         st_shared_u32(kt + swz(4 * k4 + 0, t, q.K), to_tf32(x[j].x));
                         st_shared_u32(kt + swz(4 * k4 + 1, t, q.K), to_tf32(x[j].y));
@@ -669,11 +677,11 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         const int nv = min(q.C, q.T - c * q.C);
         float* gc = gbuf + (c & 1) * 64;
         const float gl = gstage[nv - 1];
-        for (int t = tid; t < q.C; t += kThreads) gc[t] = t < nv ? expf(gl - gstage[t]) : 0.f;
+        for (int t = tid; t < q.C; t += kGdnThreads) gc[t] = t < nv ? expf(gl - gstage[t]) : 0.f;
         if (tid == 0) glast_s[c & 1] = gl;
     };
     if (q.NT > 0) {
-        stage_wkg(0, 0, kThreads);
+        stage_wkg(0, tid, kGdnThreads);
         cp_async_wait_all();
         __syncthreads();
         convert(0);
@@ -684,11 +692,11 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const uint32_t st_col = 0, r_col = 128, d_col = 256;   // S^T, R, D1^T / A2
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     // S^T = h0^T (or 0)
     if (state_warp) {
         const float* hb0 = h0 ? h0 + (int64_t)bh * q.K * q.V + v : nullptr;
-        for (int k0 = 0; k0 < q.K; k0 += 16) {
+        for (int k0 = 16 * half; k0 < q.K; k0 += 32) {
             uint32_t r[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
@@ -708,15 +716,15 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         // requests that complete while the chain below runs, issued by the two
         // warps that hold no lanes of the state while the other two run (a)
         if (!state_warp) {
-            stage_u(c, 64, kThreads - 64);
-            if (c + 1 < q.NT) stage_wkg(c + 1, 64, kThreads - 64);
+            stage_u(c, nsi, 128);
+            if (c + 1 < q.NT) stage_wkg(c + 1, nsi, 128);
         }
         const float dec = expf(glast_s[c & 1]);
         // (a) h[c] = S (staged); R = tf32(S^T); S^T <- e^{g_last} S^T, 32
         // columns at a time (16 for the last block when K % 32 == 16)
         if (state_warp) {
             __syncwarp();
-            for (int k0 = 0; k0 < q.K; k0 += 32) {
+            for (int k0 = 32 * half; k0 < q.K; k0 += 64) {
                 const int n = min(32, q.K - k0);   // 16 or 32: K is a multiple of 16
                 uint32_t r[32];
                 if (n == 32) {
@@ -731,7 +739,7 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e)   // hst[k][v]: lanes write consecutive words
-                    if (e < n) hst[(k0 + e) * kGdnVt + tid] = __uint_as_float(r[e]);
+                    if (e < n) hst[(k0 + e) * kGdnVt + vl] = __uint_as_float(r[e]);
                 uint32_t rt[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -765,7 +773,7 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         // meanwhile: h[c] out as 16-byte stores by all four warps
         if (ok) {
             float* hc = hout + ((int64_t)bh * q.NT + c) * q.K * q.V + v0;
-            for (int e = tid; e < q.K * v4s; e += kThreads) {
+            for (int e = tid; e < q.K * v4s; e += kGdnThreads) {
                 const int k = e / v4s, v4 = e - k * v4s;
                 *reinterpret_cast<float4*>(hc + (int64_t)k * q.V + 4 * v4) =
                     *reinterpret_cast<const float4*>(hst + k * kGdnVt + 4 * v4);
@@ -783,7 +791,7 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         // (c) v_new = u - D1 (over the staged u); A2 = tf32(v_new e^{g_last - g_t}) over D1^T
         if (state_warp) {
             __syncwarp();
-            for (int c0 = 0; c0 < q.C; c0 += 32) {
+            for (int c0 = 32 * half; c0 < q.C; c0 += 64) {
                 const int n = min(32, q.C - c0);   // 16 or 32 (C is 16, 32 or 64)
                 uint32_t r[32];
                 if (n == 32) {
@@ -800,14 +808,14 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
                 float uv[32], gt[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    uv[e] = e < n ? ubuf[(c0 + e) * kGdnVt + tid] : 0.f;
+                    uv[e] = e < n ? ubuf[(c0 + e) * kGdnVt + vl] : 0.f;
                     gt[e] = e < n ? gc[c0 + e] : 0.f;
                 }
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const float vn = uv[e] - __uint_as_float(r[e]);
-                    if (e < n) ubuf[(c0 + e) * kGdnVt + tid] = vn;
+                    if (e < n) ubuf[(c0 + e) * kGdnVt + vl] = vn;
                     r[e] = to_tf32(vn * gt[e]);   // gate 0 past the end and beyond n
                 }
                 if (n == 32) {
@@ -833,7 +841,7 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         }
         // meanwhile: v_new of the chunk's real tokens out as 16-byte stores
         if (ok) {
-            for (int e = tid; e < nv * v4s; e += kThreads) {
+            for (int e = tid; e < nv * v4s; e += kGdnThreads) {
                 const int t = e / v4s, v4 = e - t * v4s;
                 *reinterpret_cast<float4*>(vnb + (int64_t)(t0 + t) * tok_stride_v + 4 * v4) =
                     *reinterpret_cast<const float4*>(ubuf + t * kGdnVt + 4 * v4);
@@ -847,7 +855,7 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
     if (state_warp && final_state != nullptr) {
         __syncwarp();
         float* fs = final_state + (int64_t)bh * q.K * q.V + v;
-        for (int k0 = 0; k0 < q.K; k0 += 16) {
+        for (int k0 = 16 * half; k0 < q.K; k0 += 32) {
             uint32_t r[16];
             tmem_ld_x16(tmem + lane_off + st_col + k0, r);
             tmem_wait_ld();
@@ -989,7 +997,7 @@ cudaError_t launch_gdn_fwd_h_tf32(const GdnProblem& p, const float* k, const flo
     cudaError_t e = cudaFuncSetAttribute(gdn_fwd_h_tf32, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smem);
     if (e != cudaSuccess) return e;
-    gdn_fwd_h_tf32<<<dim3((unsigned)((p.V + kGdnVt - 1) / kGdnVt), (unsigned)(p.B * p.H)), kThreads,
+    gdn_fwd_h_tf32<<<dim3((unsigned)((p.V + kGdnVt - 1) / kGdnVt), (unsigned)(p.B * p.H)), kGdnThreads,
                      (size_t)smem, stream>>>(k, w, u, g, h0, h, v_new, final_state, q,
                                              host_timeout_word());
     return cudaGetLastError();
