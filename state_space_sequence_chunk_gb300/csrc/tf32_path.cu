@@ -690,19 +690,28 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // chunk 1's rows, a chunk ahead of their conversion (one cp.async group per
+    // request: the copy warps keep the next chunk's rows and the current u tile
+    // in flight at once)
+    if (!state_warp && q.NT > 1) {
+        stage_wkg(1, nsi, 128);
+        cp_async_commit();
+    }
     const uint32_t tmem = *tmem_holder;
     const uint32_t st_col = 0, r_col = 128, d_col = 256;   // S^T, R, D1^T / A2
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    // S^T = h0^T (or 0)
+    // S^T = h0^T (or 0), in the 32-column blocks that (a) of chunk 0 reads
+    // back from the same warp (no barrier lies between them)
     if (state_warp) {
         const float* hb0 = h0 ? h0 + (int64_t)bh * q.K * q.V + v : nullptr;
-        for (int k0 = 16 * half; k0 < q.K; k0 += 32) {
-            uint32_t r[16];
+        for (int kb = 32 * half; kb < q.K; kb += 64)
+            for (int k0 = kb; k0 < min(kb + 32, q.K); k0 += 16) {
+                uint32_t r[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                r[e] = __float_as_uint((hb0 && lane_ok) ? hb0[(int64_t)(k0 + e) * q.V] : 0.f);
-            tmem_st_x16(tmem + lane_off + st_col + k0, r);
-        }
+                for (int e = 0; e < 16; ++e)
+                    r[e] = __float_as_uint((hb0 && lane_ok) ? hb0[(int64_t)(k0 + e) * q.V] : 0.f);
+                tmem_st_x16(tmem + lane_off + st_col + k0, r);
+            }
         tmem_wait_st();
     }
     const uint32_t idesc1 = make_idesc(2, 128, (uint32_t)q.C, 0, 0);
@@ -713,11 +722,10 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         const int t0 = c * q.C, nv = min(q.C, q.T - t0);
         const float* gc = gbuf + (c & 1) * 64;
         const uint32_t wt = s0 + (c & 1) * buf_bytes, kt = wt + q.w_bytes;
-        // requests that complete while the chain below runs, issued by the two
-        // warps that hold no lanes of the state while the other two run (a)
+        // the u tile of chunk c, issued by the copy warps while the state warps run (a)
         if (!state_warp) {
             stage_u(c, nsi, 128);
-            if (c + 1 < q.NT) stage_wkg(c + 1, nsi, 128);
+            cp_async_commit();
         }
         const float dec = expf(glast_s[c & 1]);
         // (a) h[c] = S (staged); R = tf32(S^T); S^T <- e^{g_last} S^T, 32
@@ -779,15 +787,23 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
                     *reinterpret_cast<const float4*>(hst + k * kGdnVt + 4 * v4);
             }
         }
-        // ... and the staged rows (landed) become the next chunk's operand
-        // tiles in the other buffer (its last reader, (d) of chunk c - 1, is
-        // complete)
-        cp_async_wait_all();
+        // ... and the staged rows of chunk c + 1 (requested a chunk ago) become its
+        // operand tiles in the other buffer (its last reader, (d) of chunk c - 1,
+        // is complete)
+        cp_async_wait_group<1>();   // all but the u tile of chunk c
         __syncthreads();
         if (c + 1 < q.NT && ok) convert(c + 1);
         fence_proxy_async_smem();
+        cp_async_wait_group<0>();   // the u tile
+        __syncthreads();
         chain_wait(smem_u32(bar), phase, ok);
         tc_fence_after();
+        // the rows of chunk c + 2: its w tile goes where (b) of chunk c just read,
+        // its raw k and g where convert(c + 1) just read
+        if (!state_warp && c + 2 < q.NT) {
+            stage_wkg(c + 2, nsi, 128);
+            cp_async_commit();
+        }
         // (c) v_new = u - D1 (over the staged u); A2 = tf32(v_new e^{g_last - g_t}) over D1^T
         if (state_warp) {
             __syncwarp();
@@ -851,6 +867,7 @@ gdn_fwd_h_tf32(const float* __restrict__ kmat, const float* __restrict__ w,
         tc_fence_after();
         __syncthreads();   // ubuf and hst are read above before the next chunk refills them
     }
+    cp_async_wait_all();   // no copy into shared memory outlives the CTA
     // final_state = S
     if (state_warp && final_state != nullptr) {
         __syncwarp();

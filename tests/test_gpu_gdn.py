@@ -116,3 +116,28 @@ def test_gdn_bench_shape_whole_tensors():
           ", ".join(f"{n} {e:.3e}" for n, e in errs.items()))
     for n, e in errs.items():
         assert e < TOL["f32"], (n, e)
+
+
+def test_gdn_repeatable_at_bench_shape():
+    """Twenty calls of both kernels at the benchmark's shape give bit-identical
+    h, v_new, final_state and o (the chunk walk's warps hand TMEM columns and
+    shared tiles to one another: a missing ordering shows up as a call that
+    differs)."""
+    B, T, H, K, V, C = 4, 4096, 16, 128, 128, 64
+    q, k, w, u, g, h0 = gdn_inputs(B, T, H, K, V, C, seed=11)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    tq, tk, tw, tu, tg, th = dev(q), dev(k), dev(w), dev(u), dev(g), dev(h0)
+
+    def run():
+        h, v_new, fin = ssd.gdn_chunk_fwd_h(tk, tw, tu, tg, th, chunk=C)
+        return h, v_new, fin, ssd.gdn_chunk_fwd_o(tq, tk, v_new, h, tg, chunk=C)
+
+    first = run()
+    differ = []
+    for i in range(20):
+        out = run()
+        if not all(torch.equal(a, b) for a, b in zip(out, first)):
+            differ.append(i)
+    torch.cuda.synchronize()
+    assert ssd.ssd_take_device_errors() == 0
+    assert not differ, f"calls {differ} differ from the first"
