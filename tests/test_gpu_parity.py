@@ -310,6 +310,43 @@ def test_repeatable_across_group_switches():
     assert err["y"] < TOL["bf16"] and err["final_state"] < TOL["bf16"], err
 
 
+@pytest.mark.parametrize("name,chunk", [
+    ("mamba2_layer_bf16", 256),        # paired fwd_pass_state with hand-offs, Q = 256
+    ("long_context_bf16", 256),        # paired two-pass form, initial state
+    ("short_streams_bf16", 128),       # paired, initial state, 4 heads per group
+    ("pages_example_n256_bf16", 128),  # one-head two-pass form, N = 256 compute_out
+    ("small_fp32", 64),                # TF32 kernels
+])
+def test_repeatable_full_size(name, chunk):
+    """Twenty calls of ssd_fwd on a full-size workload, L2 flushed between them,
+    all bit-identical to the first (every kernel here reduces in a fixed order,
+    so a call that differs exposes a missing ordering between warps or CTAs)."""
+    w = synth.workload(name).replace(chunk=chunk)
+    dev = to_device(synth.make_inputs(w), w.dtype)
+    dims = ssd.dims_for(dev["x"], dev["B"], w.chunk)
+    ws = torch.empty(ssd.ssd_fwd_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(dev["x"])
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def run():
+        flush.fill_(1)
+        ssd.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["init_state"],
+                    chunk_size=w.chunk, workspace=ws, out=y, final_out=fin)
+
+    run()
+    torch.cuda.synchronize()
+    y0, f0 = y.clone(), fin.clone()
+    differ = []
+    for i in range(20):
+        run()
+        torch.cuda.synchronize()
+        if not (torch.equal(y, y0) and torch.equal(fin, f0)):
+            differ.append(i)
+    assert ssd.ssd_take_device_errors() == 0
+    assert not differ, f"calls {differ} differ from the first"
+
+
 def test_workspace_contents_do_not_matter():
     """The workspace (and its fwd_pass_state control block) may hold anything
     on entry: fill it with 0xFF bytes, run twice through the same buffer, and
