@@ -126,6 +126,46 @@ def test_fwd_small(case):
     assert rel_err(fin, fin_ref) < TOL[dtype]
 
 
+def _random_cases(n=48, seed=20261202):
+    """Seeded random shapes across the whole size contract (dtype, chunk, ragged
+    length, heads and groups, P and N multiples of 16 up to 256, initial state
+    and D on or off), with the oracle's work kept to a few seconds per case."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        dtype = ["f32", "bf16"][rng.integers(2)]
+        Q = int(rng.choice([64, 128, 256]))
+        L = int(rng.integers(1, 1500))
+        G = int(rng.choice([1, 2, 3]))
+        H = G * int(rng.integers(1, 4))
+        P = 16 * int(rng.integers(1, 17))
+        N = 16 * int(rng.integers(1, 17))
+        b = int(rng.integers(1, 3))
+        if b * L * H * P * N > 6e8:       # oracle budget
+            continue
+        cases.append((dtype, Q, L, H, G, P, N, bool(rng.integers(2)), bool(rng.integers(2)), b))
+    return cases
+
+
+RANDOM_CASES = _random_cases()
+
+
+@pytest.mark.parametrize("case", RANDOM_CASES,
+                         ids=[f"{c[0]}-Q{c[1]}-L{c[2]}-H{c[3]}G{c[4]}-P{c[5]}N{c[6]}-b{c[9]}"
+                              for c in RANDOM_CASES])
+def test_random_shapes(case):
+    dtype, Q, L, H, G, P, N, with_init, with_D, b = case
+    w = small(seqlen=L, nheads=H, ngroups=G, headdim=P, dstate=N, chunk=Q, dtype=dtype,
+              init_std=0.1 if with_init else 0.0, with_D=with_D, batch=b)
+    inp = synth.make_inputs(w)
+    y, fin = gpu_fwd(to_device(inp, dtype), Q)
+    y_ref, fin_ref = oracle_fwd(inp)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(fin))
+    assert rel_err(y, y_ref) < TOL[dtype]
+    assert rel_err(fin, fin_ref) < TOL[dtype]
+    assert ssd.ssd_take_device_errors() == 0
+
+
 # --- the five workloads -------------------------------------------------------
 
 def fwd_with_hiddens(w, dev):
