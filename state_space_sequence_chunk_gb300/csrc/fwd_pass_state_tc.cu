@@ -74,7 +74,11 @@ constexpr int kMaxAccSlots = 3;
 template <bool kHasInit> __host__ __device__ constexpr int acc_slots() { return kHasInit ? 2 : 3; }
 // TMA ring depth: four stages, or three when a 32 KB init-state tile shares
 // the shared memory.
-template <bool kHasInit> __host__ __device__ constexpr int stages() { return kHasInit ? 3 : 4; }
+// kTmaH (P a multiple of 64, no init tile): the chunk-start states leave
+// through a 16 KB shared tile and TMA tensor stores, which takes one stage.
+template <bool kHasInit, bool kTmaH = false> __host__ __device__ constexpr int stages() {
+    return (kHasInit || kTmaH) ? 3 : 4;
+}
 constexpr int kVecSlots = 2;        // per-chunk g / dt buffers
 constexpr int kMinBlocks = 2;       // CTAs per SM
 // Register cap: two 384-thread CTAs per SM stay below the register file's
@@ -89,10 +93,11 @@ constexpr int kTmemCols = 256;
 constexpr int kBarBytes = 512;
 // state tile in shared memory (init in, final out): fp32 [64 p][128 n]
 constexpr int kInitBytes = kCols * 128 * 4;
-template <bool kHasInit>
+constexpr int kHTileBytes = 128 * kRowBytes;      // chunk-start state tile: 128 rows of 64 p
+template <bool kHasInit, bool kTmaH = false>
 __host__ __device__ constexpr int smem_bytes() {
-    return stages<kHasInit>() * kStageBytes + (kHasInit ? kInitBytes : 0) +
-           kVecSlots * kVecSlotBytes + kBarBytes + 1024;
+    return stages<kHasInit, kTmaH>() * kStageBytes + (kHasInit ? kInitBytes : 0) +
+           (kTmaH ? kHTileBytes : 0) + kVecSlots * kVecSlotBytes + kBarBytes + 1024;
 }
 constexpr uint32_t kIdesc = make_idesc(1, 128, kCols, 1, 1);
 constexpr int kSlotFloats = 128 * kCols;           // one state slot of the hand-off buffer
@@ -178,20 +183,22 @@ constexpr int kModeHandoff = 0;
 constexpr int kModeLocal = 1;
 constexpr int kModeApply = 2;
 
-template <bool kHasInit, int kMode>
+template <bool kHasInit, int kMode, bool kTmaH>
 __global__ void __maxnreg__(kMaxRegs)
 fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                  const float* init, const float* __restrict__ Gcs,
+                  const __grid_constant__ CUtensorMap tm_h, const float* init, const float* __restrict__ Gcs,
                   const float* __restrict__ dtT, __nv_bfloat16* __restrict__ hiddens,
                   float* final_state, float* ring, unsigned int* ctrl, float* agg,
                   float* agg_lsum, const FpsParams q) {
     static_assert(kMode == kModeHandoff || !kHasInit, "the two passes take the initial state in the scan");
-    constexpr int S = stages<kHasInit>();
+    static_assert(!kTmaH || (!kHasInit && kMode != kModeLocal), "the TMA-stored states need the shared tile");
+    constexpr int S = stages<kHasInit, kTmaH>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float* init_tile = reinterpret_cast<float*>(smem + S * kStageBytes);   // [64 p][128 n]
-    uint8_t* vecs = smem + S * kStageBytes + (kHasInit ? kInitBytes : 0);   // kVecSlots x (g[Q], dt[Q])
+    uint8_t* htile = smem + S * kStageBytes + (kHasInit ? kInitBytes : 0);  // kTmaH: [128 n][64 p], swizzled
+    uint8_t* vecs = htile + (kTmaH ? kHTileBytes : 0);                       // kVecSlots x (g[Q], dt[Q])
     uint64_t* bars = reinterpret_cast<uint64_t*>(vecs + kVecSlots * kVecSlotBytes);
     // barrier indices
     auto full = [&](int s) { return smem_u32(bars + s); };
@@ -207,7 +214,10 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     const uint32_t init_full = smem_u32(bars + kB + 2 * kVecSlots + 1);
     const uint32_t tile_free = smem_u32(bars + kB + 2 * kVecSlots + 2);
     const uint32_t mma_drain = smem_u32(bars + kB + 2 * kVecSlots + 3);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kB + 2 * kVecSlots + 4);
+    // kTmaH: the state tile written (one arrival per fold warp) / read by its store
+    const uint32_t h_full = smem_u32(bars + kB + 2 * kVecSlots + 4);
+    const uint32_t h_free = smem_u32(bars + kB + 2 * kVecSlots + 5);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kB + 2 * kVecSlots + 6);
     int* range_id = reinterpret_cast<int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -232,6 +242,8 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         mbar_init(init_full, 32 * kFoldWarps);
         mbar_init(tile_free, 32 * kFoldWarps);
         mbar_init(mma_drain, 1);
+        mbar_init(h_full, kFoldWarps);
+        mbar_init(h_free, 1);
         fence_mbar_init();
         // chunk_cumsum (G, dt, the cleared control block) must be complete
         grid_dependency_wait();
@@ -527,9 +539,22 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     ok = false;
                     break;
                 }
+                if (kTmaH && qc > 0) {
+                    // the previous chunk's store has read the state tile
+                    if (rl == 0) {
+                        bulk_wait_group_read0();
+                        mbar_arrive(h_free);
+                    }
+                    if (!__all_sync(0xffffffffu, mbar_wait(h_free, (qc - 1) & 1, &g_fps_error, 1u))) {
+                        ok = false;
+                        break;
+                    }
+                }
                 tc_fence_after();
                 const uint32_t acc = lane_base + slot * kCols;
                 __nv_bfloat16* hp = hiddens + (((int64_t)u.bh * q.nc + c) * q.N + n) * q.P + p0;
+                // kTmaH: row rl of the 128-byte-swizzled tile, 16-byte chunk j at (j ^ (rl % 8)) * 16
+                uint8_t* trow = htile + rl * kRowBytes;
 #pragma unroll
                 for (int jj = 0; jj < kCols / 16; ++jj) {
                     __syncwarp();
@@ -543,7 +568,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                     tmem_st_x16(sa + 16 * jj, d);
                     // chunk-start state S -> hiddens[c] (row n holds S[:, n]): 16
                     // contiguous bf16 per slice (P is a multiple of 16)
-                    if (kMode != kModeLocal && nok && p0 + 16 * jj < q.P) {
+                    if (kMode != kModeLocal && nok && (kTmaH || p0 + 16 * jj < q.P)) {
                         uint4 w0, w1;
                         w0.x = pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1]));
                         w0.y = pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3]));
@@ -553,15 +578,40 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                         w1.y = pack_bf16(__uint_as_float(sv[10]), __uint_as_float(sv[11]));
                         w1.z = pack_bf16(__uint_as_float(sv[12]), __uint_as_float(sv[13]));
                         w1.w = pack_bf16(__uint_as_float(sv[14]), __uint_as_float(sv[15]));
-                        uint4* hdst = reinterpret_cast<uint4*>(hp + 16 * jj);
-                        hdst[0] = w0;
-                        hdst[1] = w1;
+                        if (kTmaH) {
+                            *reinterpret_cast<uint4*>(trow + (((2 * jj) ^ (rl & 7)) << 4)) = w0;
+                            *reinterpret_cast<uint4*>(trow + (((2 * jj + 1) ^ (rl & 7)) << 4)) = w1;
+                        } else {
+                            uint4* hdst = reinterpret_cast<uint4*>(hp + 16 * jj);
+                            hdst[0] = w0;
+                            hdst[1] = w1;
+                        }
                     }
+                }
+                if (kTmaH) {
+                    fence_proxy_async_smem();   // tile writes -> the TMA store
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(h_full);
                 }
                 __syncwarp();
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(acc_empty(slot));
+                if (kTmaH) {
+                    // one thread stores the chunk's [128 n][64 p] block of hiddens
+                    bool okh = true;
+                    if (rl == 0) {
+                        okh = mbar_wait(h_full, qc & 1, &g_fps_error, 1u);
+                        if (okh) {
+                            tma_store_3d(&tm_h, smem_u32(htile), p0, u.mb * 128, u.bh * q.nc + c);
+                            bulk_commit_group();
+                        }
+                    }
+                    if (!__all_sync(0xffffffffu, okh)) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
             if (kMode == kModeLocal) {
@@ -667,6 +717,7 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             }
         }
         if (kHasInit) cp_async_wait_all();  // no copy into shared memory outlives the CTA
+        if (kTmaH && rl == 0) bulk_wait_group0();   // the state stores have completed
     }
     tc_fence_before();
     __syncthreads();
@@ -1397,8 +1448,22 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     q.G = two_pass ? (int)G1 : std::min(q.W, resident);
     cfg.gridDim = dim3((unsigned)q.G);
     cfg.blockDim = dim3(kThreads);
-    using OneKernel = void (*)(CUtensorMap, CUtensorMap, const float*, const float*, const float*,
-                               __nv_bfloat16*, float*, float*, unsigned int*, float*, float*, FpsParams);
+    // P a multiple of 64: the chunk-start states leave as TMA stores of
+    // [min(N, 128) rows][64 p] blocks (rows past N are clipped by the TMA)
+    const bool tma_h = p.P % 64 == 0;
+    CUtensorMap th;
+    memset(&th, 0, sizeof(th));
+    if (tma_h) {
+        const uint64_t hd[3] = {(uint64_t)p.P, (uint64_t)p.N, (uint64_t)(p.b * p.H * p.nc)};
+        const uint64_t hs[2] = {(uint64_t)p.P * 2, (uint64_t)p.N * p.P * 2};
+        const uint32_t hbox[3] = {64, (uint32_t)std::min<int64_t>(p.N, 128), 1};
+        if (!encode_tmap(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, hiddens, hd, hs, hbox,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    using OneKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, const float*,
+                               const float*, __nv_bfloat16*, float*, float*, unsigned int*, float*,
+                               float*, FpsParams);
     auto launch_one = [&](OneKernel k1, int smem, const float* init_in, float* fin, float* ag,
                           float* ls) -> cudaError_t {
         cudaError_t le;
@@ -1408,24 +1473,29 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
                                        (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
             return le;
         cfg.dynamicSmemBytes = (size_t)smem;
-        le = cudaLaunchKernelEx(&cfg, k1, tx, tb, init_in, Gcs, dtT, (__nv_bfloat16*)hiddens, fin, ring,
-                                ctrl, ag, ls, q);
+        le = cudaLaunchKernelEx(&cfg, k1, tx, tb, th, init_in, Gcs, dtT, (__nv_bfloat16*)hiddens, fin,
+                                ring, ctrl, ag, ls, q);
         return le != cudaSuccess ? le : cudaGetLastError();
     };
-    if (!two_pass)
-        return init != nullptr
-                   ? launch_one(fwd_pass_state_tc<true, kModeHandoff>, smem_bytes<true>(), init,
-                                final_state, nullptr, nullptr)
-                   : launch_one(fwd_pass_state_tc<false, kModeHandoff>, smem_bytes<false>(), nullptr,
-                                final_state, nullptr, nullptr);
-    if ((e = launch_one(fwd_pass_state_tc<false, kModeLocal>, smem_bytes<false>(), nullptr, nullptr, agg,
-                        lsum)) != cudaSuccess)
+    if (!two_pass) {
+        if (init != nullptr)
+            return launch_one(fwd_pass_state_tc<true, kModeHandoff, false>, smem_bytes<true>(), init,
+                              final_state, nullptr, nullptr);
+        return tma_h ? launch_one(fwd_pass_state_tc<false, kModeHandoff, true>, smem_bytes<false, true>(),
+                                  nullptr, final_state, nullptr, nullptr)
+                     : launch_one(fwd_pass_state_tc<false, kModeHandoff, false>, smem_bytes<false>(),
+                                  nullptr, final_state, nullptr, nullptr);
+    }
+    if ((e = launch_one(fwd_pass_state_tc<false, kModeLocal, false>, smem_bytes<false>(), nullptr, nullptr,
+                        agg, lsum)) != cudaSuccess)
         return e;
     fwd_pass_state_scan<false><<<dim3((kSlotFloats + 255) / 256, (unsigned)q.nchains), 256, 0, stream>>>(
         init, agg, lsum, final_state, q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return launch_one(fwd_pass_state_tc<false, kModeApply>, smem_bytes<false>(), nullptr, nullptr, agg,
-                      lsum);
+    return tma_h ? launch_one(fwd_pass_state_tc<false, kModeApply, true>, smem_bytes<false, true>(), nullptr,
+                              nullptr, agg, lsum)
+                 : launch_one(fwd_pass_state_tc<false, kModeApply, false>, smem_bytes<false>(), nullptr,
+                              nullptr, agg, lsum);
 }
 
 cudaError_t set_fwd_pass_state_withhold(unsigned int on) {
