@@ -8,6 +8,7 @@
 // (sections "Kernel 2: fwd_pass_state" and "Kernel 3: compute_out"), with all
 // arithmetic in fp32; they serve the shapes the tensor-core kernels do not
 // (fp32 with N or P above 128, bf16 compute_out with P > 64 or N > 128).
+#include "sm100_ptx.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -99,6 +100,8 @@ constexpr int kScanBatch = 8;
 __global__ void __launch_bounds__(kThreads)
 fps_state_scan(const float* __restrict__ Gcs, const float* init, float* __restrict__ hiddens,
                float* final_state, int H, int P, int N, int Q, int nc, int Lp) {
+    grid_launch_dependents();   // chained launch: compute_out may set up meanwhile
+    grid_dependency_wait();     // the chunk products
     const int f = blockIdx.x * kThreads + threadIdx.x, bh = blockIdx.y;
     if (f >= P * N) return;
     const int n = f / P, p = f - n * P;
@@ -268,10 +271,10 @@ cudaError_t launch_fps(const Problem& p, const void* x, const void* B, const flo
                                                        (int)p.Lp, (int)p.hpg);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    fps_state_scan<<<dim3((unsigned)((p.P * p.N + kThreads - 1) / kThreads), (unsigned)(p.b * p.H)),
-                     kThreads, 0, stream>>>(Gcs, init, (float*)hid, fin, (int)p.H, (int)p.P,
-                                            (int)p.N, (int)p.Q, (int)p.nc, (int)p.Lp);
-    return cudaGetLastError();
+    return launch_chained(fps_state_scan,
+                          dim3((unsigned)((p.P * p.N + kThreads - 1) / kThreads), (unsigned)(p.b * p.H)),
+                          dim3(kThreads), 0, stream, p.chained, Gcs, init, (float*)hid, fin, (int)p.H,
+                          (int)p.P, (int)p.N, (int)p.Q, (int)p.nc, (int)p.Lp);
 }
 
 template <typename T>

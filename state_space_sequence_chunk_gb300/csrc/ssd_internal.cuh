@@ -127,6 +127,26 @@ unsigned int take_fwd_pass_state_error();
 cudaError_t set_fwd_pass_state_withhold(unsigned int on);
 unsigned int take_compute_out_error();
 
+// Launch kern on stream, with programmatic dependent launch when pdl is set
+// (the kernel then waits on the previous grid with griddepcontrol.wait before
+// it reads that grid's output).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Element loads/stores shared by the kernels.
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }

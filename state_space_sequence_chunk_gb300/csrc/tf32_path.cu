@@ -170,6 +170,10 @@ fps_products_tf32(const float* __restrict__ x, const float* __restrict__ B,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // chained launch: the next grid may start (every CTA of this one holds its
+    // TMEM already); G and dt come from chunk_cumsum
+    grid_launch_dependents();
+    grid_dependency_wait();
 
     const float* grow = Gcs + (int64_t)bh * q.Lp + (int64_t)c * q.Q;
     const float* drow = dtT + (int64_t)bh * q.Lp + (int64_t)c * q.Q;
@@ -352,6 +356,7 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(smem_u32(tmem_holder), q.tmem_cols);
+    grid_dependency_wait();   // chained launch: the state scan's output
     for (int i = tid; i < q.Q; i += kThreads) {
         if (kGdn) {
             const int t = t0 + i;
@@ -914,10 +919,9 @@ cudaError_t launch_fps_products_tf32(const Problem& p, const void* x, const void
     cudaError_t e = cudaFuncSetAttribute(fps_products_tf32,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
     if (e != cudaSuccess) return e;
-    fps_products_tf32<<<dim3((unsigned)p.nc, (unsigned)(p.b * p.H)), kThreads, (size_t)smem_cta,
-                        stream>>>((const float*)x, (const float*)B, Gcs, dtT, (float*)hiddens, q,
-                                  host_timeout_word());
-    return cudaGetLastError();
+    return launch_chained(fps_products_tf32, dim3((unsigned)p.nc, (unsigned)(p.b * p.H)), dim3(kThreads),
+                          (size_t)smem_cta, stream, p.chained, (const float*)x, (const float*)B, Gcs,
+                          dtT, (float*)hiddens, q, host_timeout_word());
 }
 
 namespace {
@@ -968,11 +972,11 @@ cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void*
     cudaError_t e = cudaFuncSetAttribute(compute_out_tf32<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
     if (e != cudaSuccess) return e;
-    compute_out_tf32<false><<<dim3((unsigned)(q.nblk * q.npt), (unsigned)p.nc, (unsigned)(p.b * p.H)),
-                              kThreads, (size_t)smem_cta, stream>>>(
-        (const float*)x, (const float*)B, (const float*)C, Gcs, dtT, (const float*)hiddens, D,
-        (float*)y, q, host_timeout_word());
-    return cudaGetLastError();
+    return launch_chained(compute_out_tf32<false>,
+                          dim3((unsigned)(q.nblk * q.npt), (unsigned)p.nc, (unsigned)(p.b * p.H)),
+                          dim3(kThreads), (size_t)smem_cta, stream, p.chained, (const float*)x,
+                          (const float*)B, (const float*)C, Gcs, dtT, (const float*)hiddens, D,
+                          (float*)y, q, host_timeout_word());
 }
 
 bool gdn_tf32_supports(const GdnProblem& p) {
