@@ -1213,6 +1213,8 @@ fwd_pass_state_scan(const float* init, float* agg, const float* __restrict__ agg
                     float* final_state, const FpsParams q) {
     __shared__ int s_slot[kScanBatch];
     __shared__ float s_decay[kScanBatch];
+    grid_launch_dependents();   // chained launch: the apply pass may set up meanwhile
+    grid_dependency_wait();     // the local pass's aggregates
     const int f = blockIdx.x * blockDim.x + threadIdx.x;
     int pc, hd, bh, n, p;
     if (kPair) {
@@ -1430,9 +1432,10 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
         if ((e = launch_pair(fwd_pass_state_pair_tc<false, kModeLocal>, pair_smem<false>(), agg,
                              lsum)) != cudaSuccess)
             return e;
-        fwd_pass_state_scan<true><<<dim3((kSlotFloats + 255) / 256, (unsigned)(p.b * p.H)), 256, 0, stream>>>(
-            init, agg, lsum, final_state, q);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_chained(fwd_pass_state_scan<true>, dim3((kSlotFloats + 255) / 256, (unsigned)(p.b * p.H)),
+                                dim3(256), 0, stream, p.chained, init, agg, (const float*)lsum, final_state,
+                                q)) != cudaSuccess)
+            return e;
         cfg.numAttrs = p.chained ? 1 : 0;   // the apply pass may set up while the scan runs
         return tma_h ? launch_pair(fwd_pass_state_pair_tc<true, kModeApply>, pair_smem<true>(), agg, lsum)
                      : launch_pair(fwd_pass_state_pair_tc<false, kModeApply>, pair_smem<false>(), agg,
@@ -1489,9 +1492,10 @@ cudaError_t launch_fwd_pass_state_tc(const Problem& p, const void* x, const void
     if ((e = launch_one(fwd_pass_state_tc<false, kModeLocal, false>, smem_bytes<false>(), nullptr, nullptr,
                         agg, lsum)) != cudaSuccess)
         return e;
-    fwd_pass_state_scan<false><<<dim3((kSlotFloats + 255) / 256, (unsigned)q.nchains), 256, 0, stream>>>(
-        init, agg, lsum, final_state, q);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_chained(fwd_pass_state_scan<false>, dim3((kSlotFloats + 255) / 256, (unsigned)q.nchains),
+                            dim3(256), 0, stream, p.chained, init, agg, (const float*)lsum, final_state,
+                            q)) != cudaSuccess)
+        return e;
     return tma_h ? launch_one(fwd_pass_state_tc<false, kModeApply, true>, smem_bytes<false, true>(), nullptr,
                               nullptr, agg, lsum)
                  : launch_one(fwd_pass_state_tc<false, kModeApply, false>, smem_bytes<false>(), nullptr,
