@@ -203,6 +203,8 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     if (warp == kProducerWarp) {
         // ===================== TMA producer =====================
         if (lane == 0) {
+            // each chunk-start state is read once: its lines go first in L2
+            const uint64_t h_pol = l2_policy_evict_first();
             int sc = 0;   // stage ring counter
             int gi = -1;  // group counter
             for (int u = u0; u < u1; ++u) {
@@ -255,7 +257,8 @@ compute_out_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 mbar_arrive_expect_tx(fb, Cfg::kXBytes + Cfg::kHBytes + 2 * Cfg::kVecBytes);
                 tma_load_4d(smem_u32(st), &tm_x, fb, 0, ui.h, ui.c * Q, ui.b);
                 const int bh = ui.b * H + ui.h;
-                tma_load_4d(smem_u32(st + Cfg::kXBytes), &tm_h, fb, 0, 0, bh * nc + ui.c, 0);
+                tma_load_4d_hint(smem_u32(st + Cfg::kXBytes), &tm_h, fb, 0, 0, bh * nc + ui.c, 0,
+                                 h_pol);
                 const int64_t vo = (int64_t)bh * Lp + (int64_t)ui.c * Q;
                 bulk_load(smem_u32(st + Cfg::kXBytes + Cfg::kHBytes), Gcs + vo, Cfg::kVecBytes, fb);
                 bulk_load(smem_u32(st + Cfg::kXBytes + Cfg::kHBytes + Cfg::kVecBytes), dtT + vo,

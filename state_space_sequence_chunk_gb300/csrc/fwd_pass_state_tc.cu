@@ -265,6 +265,11 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
+            // a chain reads its x block once when the state is one block of N
+            // rows: its lines then go first, so the hiddens written here stay in
+            // L2 for compute_out (with two blocks the other chain reads it too)
+            const bool x_once = q.nmb == 1;
+            const uint64_t x_pol = x_once ? l2_policy_evict_first() : 0;
             int i = 0;   // stage counter
             int cv = 0;  // chunk counter (g / dt ring position)
             bool ok = true;
@@ -292,7 +297,10 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                         const uint32_t xs = stage0 + s * kStageBytes, bs = xs + kXBytes;
                         const int tok = c * q.Q + sub * kSub;
                         mbar_arrive_expect_tx(full(s), kXBytes + kBBytes);
-                        tma_load_4d(xs, &tm_x, full(s), u.pb * kCols, h, tok, b);
+                        if (x_once)
+                            tma_load_4d_hint(xs, &tm_x, full(s), u.pb * kCols, h, tok, b, x_pol);
+                        else
+                            tma_load_4d(xs, &tm_x, full(s), u.pb * kCols, h, tok, b);
 #pragma unroll
                         for (int jb = 0; jb < 2; ++jb)
                             tma_load_4d(bs + jb * kSub * kRowBytes, &tm_b, full(s),
@@ -843,6 +851,9 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
+            // x is read once here: its lines go first, so the hiddens written
+            // by this kernel stay in L2 for compute_out
+            const uint64_t x_pol = l2_policy_evict_first();
             int i = 0, cv = 0;
             bool ok = true;
             for (int pi = 0; pi < rg.pieces() && ok; ++pi) {
@@ -872,8 +883,8 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                         const uint32_t xs = stage0 + s * kPStageBytes, bs = xs + 2 * kXBytes;
                         const int tok = c * q.Q + sub * kSub;
                         mbar_arrive_expect_tx(full(s), kPStageBytes);
-                        tma_load_4d(xs, &tm_x, full(s), 0, h0, tok, b);
-                        tma_load_4d(xs + kXBytes, &tm_x, full(s), 0, h0 + 1, tok, b);
+                        tma_load_4d_hint(xs, &tm_x, full(s), 0, h0, tok, b, x_pol);
+                        tma_load_4d_hint(xs + kXBytes, &tm_x, full(s), 0, h0 + 1, tok, b, x_pol);
 #pragma unroll
                         for (int jb = 0; jb < 2; ++jb)
                             tma_load_4d(bs + jb * kSub * kRowBytes, &tm_b, full(s), jb * 64, grp, tok, b);
