@@ -483,7 +483,7 @@ def conv1d_main(args):
 # Gated DeltaNet configuration for --gdn: 4 sequences of 4096 tokens, 16 heads,
 # K = V = 128, chunk 64, fp32 (the gallery's kernels use C = 64 and K/V 64-128).
 GDN = dict(B=4, T=4096, H=16, K=128, V=128, chunk=64)
-GDN_METRIC = "Gated DeltaNet chunk_fwd_h + chunk_fwd_o tokens/s on 1 GB300 and % of the TF32 tensor peak"
+GDN_METRIC = "Gated DeltaNet chunk_fwd_h + chunk_fwd_o tokens/s on 1 GB300 and % of roofline (HBM GB/s / tensor-pipe)"
 # Nominal dense tensor rates of GB300 (TF32 1.1, bf16 2.25 PFLOP/s): the TF32 peak
 # is the measured bf16 GEMM rate scaled by their ratio.
 TF32_PER_BF16 = 1.1 / 2.25
@@ -579,18 +579,31 @@ def gdn_main(args):
     macs = B * H * NT * (2 * C * K * V + C * K * V + C * (C + 1) // 2 * (K + V))
     achieved = 2 * macs / (ms * 1e-3) / 1e12
     peak_tf, peak_kind_tf = tf32_peak()
+    # algorithmic bytes (fp32): chunk_fwd_h reads k, w, u, g and h0 and writes h,
+    # v_new and the final state; chunk_fwd_o reads q, k, v_new, h and g and writes o
+    gdn_bytes = 4 * (B * T * H * (4 * K + 4 * V + 2) + B * H * K * V * (2 + 2 * NT))
+    hbm, hbm_kind = measured_peaks()
+    bw = gdn_bytes / (ms * 1e-3) / 1e9
+    hbm_bound = gdn_bytes / (hbm * 1e9) >= 2 * macs / (peak_tf * 1e12)
     line = {
         "metric": GDN_METRIC, "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "gdn_chunk_f32", "B": B, "T": T, "H": H, "K": K, "V": V, "chunk": C,
                    "l2": "flushed before every step"},
-        "roofline": {"bound": "tensor", "kernel": "gdn_fwd_h + gdn_fwd_o", "achieved": achieved,
-                     "peak": peak_tf, "peak_kind": peak_kind_tf,
-                     "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                     # DRAM bytes of both launches of one step
-                     "traffic": recorded_traffic("gdn", "gdn_chunk_f32"),
-                     "algorithmic_flops": 2 * macs},
+        # the binding bound is the slower of the bytes at HBM bandwidth and the
+        # FLOPs at the TF32 tensor rate; the other is reported beside it
+        "roofline": dict(
+            ({"bound": "hbm", "kernel": "gdn_fwd_h + gdn_fwd_o", "achieved": bw, "peak": hbm,
+              "peak_kind": hbm_kind, "unit": "GB/s", "frac": bw / hbm}
+             if hbm_bound else
+             {"bound": "tensor", "kernel": "gdn_fwd_h + gdn_fwd_o", "achieved": achieved,
+              "peak": peak_tf, "peak_kind": peak_kind_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf}),
+            # DRAM bytes of both launches of one step
+            traffic=recorded_traffic("gdn", "gdn_chunk_f32"),
+            algorithmic_bytes=gdn_bytes, algorithmic_flops=2 * macs,
+            tensor={"achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": achieved / peak_tf, "peak_kind": peak_kind_tf}),
         "e2e": {"value": B * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": sum(t.numel() * 4 for t in host.values()),
                 "d2h_bytes_per_step": o_h.numel() * 4},
