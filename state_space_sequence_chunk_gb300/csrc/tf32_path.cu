@@ -50,6 +50,11 @@ namespace {
 __device__ unsigned int g_tf32_error;  // bit 0: a bounded wait gave up
 
 constexpr int kThreads = 128;
+// Registers are held to 65536 / (4 x 128) = 128 per thread, so that the
+// register file is not what limits the CTAs per SM to fewer than four (the
+// number that the tensor memory and the shared memory allow on the small
+// shapes: a grid of 512 CTAs then runs in one wave on 152 SMs)
+constexpr int kCtasPerSm = 4;
 constexpr int kRowBytes = 128;   // one swizzle row: 32 fp32 values of K
 
 __device__ __forceinline__ uint32_t to_tf32(float v) {
@@ -146,7 +151,7 @@ struct FpsTf32 {
     int a_bytes, x_bytes;   // one buffer's A tile (128 rows x 32) and X^T tile (P rows x 32)
 };
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 fps_products_tf32(const float* __restrict__ x, const float* __restrict__ B,
                   const float* __restrict__ Gcs, const float* __restrict__ dtT,
                   float* __restrict__ hiddens, const FpsTf32 q, unsigned int* host_err) {
@@ -283,32 +288,48 @@ __device__ __forceinline__ void put_rows(uint32_t tile, int rows, const float* b
 }
 
 // A transposed K-major tile: tile[p][k] = tf32(scale(k) * src(k)[p]) for
-// k < Kdim (lanes take k), p < cols (warps take groups of 4 columns); src(k)
-// is NULL for a zero row.  Up to 16 loads per thread are issued before their
-// stores.
+// k < Kdim and p < cols (a multiple of 4); src(k) is NULL for a zero row.
+// The warps take blocks of 32 values of k by 16 columns in turn: lane l reads
+// the four source rows k = 4 (l % 8) + i at columns 4 (l / 8) + e (16 bytes
+// each), transposes the 4 x 4 values in registers and writes each column's
+// four values of k as one 16-byte store; the eight lanes of a store phase then
+// fill eight different 16-byte chunks of one tile row.  Up to four blocks (16
+// loads per lane) are in flight before their stores.
 template <typename Src, typename Scale>
 __device__ __forceinline__ void put_transposed(uint32_t tile, int rows, int Kdim, int cols, Src src,
                                                Scale scale, int lane, int warp) {
-    const int nkb = (Kdim + 31) / 32;
-    for (int it0 = 0; it0 < nkb * kMaxGroups; it0 += 16) {
-        float4 v[16];
+    constexpr int kWarps = kThreads / 32;
+    const int ncb = (cols + 15) / 16, nblk = (Kdim + 31) / 32 * ncb;
+    const int kl = 4 * (lane & 7), cl = 4 * (lane >> 3);
+    for (int b0 = warp; b0 < nblk; b0 += 4 * kWarps) {
+        float4 v[4][4];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int it = it0 + m, kb = it / kMaxGroups, c4 = warp + 4 * (it % kMaxGroups);
-            const int k = kb * 32 + lane;
-            const float* sp = (kb < nkb && k < Kdim && 4 * c4 < cols) ? src(k) : nullptr;
-            v[m] = sp ? ldg4(sp + 4 * c4) : zero4();
+        for (int m = 0; m < 4; ++m) {
+            const int blk = b0 + m * kWarps, kb = blk / ncb;
+            const int k = 32 * kb + kl, c = 16 * (blk - kb * ncb) + cl;
+            const bool live = blk < nblk && c < cols;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float* sp = (live && k + i < Kdim) ? src(k + i) : nullptr;
+                v[m][i] = sp ? ldg4(sp + c) : zero4();
+            }
         }
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int it = it0 + m, kb = it / kMaxGroups, c4 = warp + 4 * (it % kMaxGroups);
-            const int k = kb * 32 + lane;
-            if (kb < nkb && k < Kdim && 4 * c4 < cols) {
-                const float sc = scale(k);
-                st_shared_u32(tile + swz(4 * c4 + 0, k, rows), to_tf32(v[m].x * sc));
-                st_shared_u32(tile + swz(4 * c4 + 1, k, rows), to_tf32(v[m].y * sc));
-                st_shared_u32(tile + swz(4 * c4 + 2, k, rows), to_tf32(v[m].z * sc));
-                st_shared_u32(tile + swz(4 * c4 + 3, k, rows), to_tf32(v[m].w * sc));
+        for (int m = 0; m < 4; ++m) {
+            const int blk = b0 + m * kWarps, kb = blk / ncb;
+            const int k = 32 * kb + kl, c = 16 * (blk - kb * ncb) + cl;
+            if (blk < nblk && c < cols && k < Kdim) {
+                float sc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[i] = k + i < Kdim ? scale(k + i) : 0.f;
+                st_shared_v4(tile + swz(c, k, rows), to_tf32(v[m][0].x * sc[0]), to_tf32(v[m][1].x * sc[1]),
+                             to_tf32(v[m][2].x * sc[2]), to_tf32(v[m][3].x * sc[3]));
+                st_shared_v4(tile + swz(c + 1, k, rows), to_tf32(v[m][0].y * sc[0]), to_tf32(v[m][1].y * sc[1]),
+                             to_tf32(v[m][2].y * sc[2]), to_tf32(v[m][3].y * sc[3]));
+                st_shared_v4(tile + swz(c + 2, k, rows), to_tf32(v[m][0].z * sc[0]), to_tf32(v[m][1].z * sc[1]),
+                             to_tf32(v[m][2].z * sc[2]), to_tf32(v[m][3].z * sc[3]));
+                st_shared_v4(tile + swz(c + 3, k, rows), to_tf32(v[m][0].w * sc[0]), to_tf32(v[m][1].w * sc[1]),
+                             to_tf32(v[m][2].w * sc[2]), to_tf32(v[m][3].w * sc[3]));
             }
         }
     }
@@ -320,7 +341,7 @@ __device__ __forceinline__ void put_transposed(uint32_t tile, int rows, int Kdim
 // one "group" per head, no dt (1) and no D; Gcs then points at the natural-log
 // gate g [batch, T, H], scaled by log2(e) on load.
 template <bool kGdn>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
                  const float* __restrict__ C, const float* __restrict__ Gcs,
                  const float* __restrict__ dtT, const float* __restrict__ hiddens,
