@@ -287,6 +287,35 @@ __device__ __forceinline__ void put_rows(uint32_t tile, int rows, const float* b
     }
 }
 
+// put_rows' tile copied by cp.async instead (16-byte pieces of raw fp32, rows
+// past `nvalid` zeroed), so that the loads of the other tiles need not wait
+// for it; round_rows then rounds it to TF32 in place once the copies have
+// landed, each thread the pieces it copied itself.
+__device__ __forceinline__ void async_rows(uint32_t tile, int rows, const float* base, int64_t row_stride,
+                                           int nvalid, int N, int tid) {
+    const int n4s = N / 4, total = rows * n4s;
+    for (int e = tid; e < total; e += kThreads) {
+        const int r = e / n4s, n4 = e - r * n4s;
+        const uint32_t dst = tile + swz(r, 4 * n4, rows);
+        if (r < nvalid) cp_async_16(dst, base + r * row_stride + 4 * n4, 16u);
+        else st_shared_v4(dst, 0u, 0u, 0u, 0u);
+    }
+}
+__device__ __forceinline__ void round_rows(uint32_t tile, int rows, int N, int tid) {
+    const int n4s = N / 4, total = rows * n4s;
+    for (int e = tid; e < total; e += kThreads) {
+        const int r = e / n4s, n4 = e - r * n4s;
+        const uint32_t a = tile + swz(r, 4 * n4, rows);
+        uint32_t v0, v1, v2, v3;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                     : "r"(a)
+                     : "memory");
+        st_shared_v4(a, to_tf32(__uint_as_float(v0)), to_tf32(__uint_as_float(v1)),
+                     to_tf32(__uint_as_float(v2)), to_tf32(__uint_as_float(v3)));
+    }
+}
+
 // A transposed K-major tile: tile[p][k] = tf32(scale(k) * src(k)[p]) for
 // k < Kdim and p < cols (a multiple of 4); src(k) is NULL for a zero row.
 // The warps take blocks of 32 values of k by 16 columns in turn: lane l reads
@@ -378,6 +407,16 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     }
     if (warp == 0) tmem_alloc(smem_u32(tmem_holder), q.tmem_cols);
     grid_dependency_wait();   // chained launch: the state scan's output
+    // C_I (rows = query rows) and B_0 (rows = keys) by cp.async, in flight while
+    // the other operands are loaded.  With Q < 128 the C_I tile has Q rows;
+    // the M = 128 products read 128 rows from it regardless, and the rows past
+    // Q (whatever shared memory follows the tile) only reach accumulator lanes
+    // that are never used.
+    const int c_valid = min(min(q.Q - i0, 128), q.L - (t0 + i0));
+    const int b_valid = min(q.KB, q.L - t0);
+    async_rows(ct, q.crows, Cb + (int64_t)(t0 + i0) * bc_stride, bc_stride, c_valid, q.N, tid);
+    async_rows(bt, q.KB, Bb + (int64_t)t0 * bc_stride, bc_stride, b_valid, q.N, tid);
+    cp_async_commit();
     for (int i = tid; i < q.Q; i += kThreads) {
         if (kGdn) {
             const int t = t0 + i;
@@ -388,13 +427,6 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
             dv[i] = dtT[(int64_t)bh * q.Lp + t0 + i];
         }
     }
-    // C_I (rows = query rows) and B_0 (rows = keys).  With Q < 128 the C_I tile
-    // has Q rows; the M = 128 products read 128 rows from it regardless, and
-    // the rows past Q (whatever shared memory follows the tile) only reach
-    // accumulator lanes that are never used.
-    put_rows(ct, q.crows, Cb + (int64_t)(t0 + i0) * bc_stride, bc_stride,
-             min(min(q.Q - i0, 128), q.L - (t0 + i0)), q.N, tid);
-    put_rows(bt, q.KB, Bb + (int64_t)t0 * bc_stride, bc_stride, min(q.KB, q.L - t0), q.N, tid);
     // h^T: rows = p, K = state n (hiddens holds [n][p])
     const float* hb = hiddens + ((int64_t)bh * q.nc + c) * (int64_t)q.N * q.P + p0;
     put_transposed(ht, pc, q.N, pc, [&](int n) { return hb + (int64_t)n * q.P; },
@@ -415,6 +447,9 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
         __syncthreads();   // dv complete
         put_x(0);
     }
+    cp_async_wait_all();
+    round_rows(ct, q.crows, q.N, tid);
+    round_rows(bt, q.KB, q.N, tid);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
