@@ -262,6 +262,7 @@ struct CoTf32 {
     int c_bytes, b_bytes, h_bytes, x_bytes;   // C_I, B_J, h^T, (dt o X_J)^T tiles
     int x_sep;                   // 1: (dt o X)^T has a tile of its own (written up front);
                                  // 0: it reuses h^T's, once C h^T is done
+    int kh, nks;                 // state columns per pass of the C h^T / C B^T products, passes
 };
 
 // A K-major tile whose rows are consecutive tokens of a [token][group][N]
@@ -369,7 +370,7 @@ __device__ __forceinline__ void put_transposed(uint32_t tile, int rows, int Kdim
 // e^{g_i - g_j}) v_new -- C -> q, B -> k, x -> v_new, hiddens -> h, y -> o,
 // one "group" per head, no dt (1) and no D; Gcs then points at the natural-log
 // gate g [batch, T, H], scaled by log2(e) on load.
-template <bool kGdn>
+template <bool kGdn, bool kSplit>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
                  const float* __restrict__ C, const float* __restrict__ Gcs,
@@ -414,8 +415,11 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     // that are never used.
     const int c_valid = min(min(q.Q - i0, 128), q.L - (t0 + i0));
     const int b_valid = min(q.KB, q.L - t0);
-    async_rows(ct, q.crows, Cb + (int64_t)(t0 + i0) * bc_stride, bc_stride, c_valid, q.N, tid);
-    async_rows(bt, q.KB, Bb + (int64_t)t0 * bc_stride, bc_stride, b_valid, q.N, tid);
+    // kSplit: the C h^T and C B^T products run in q.nks passes of q.kh state
+    // columns, so that the tiles (and with them more CTAs) fit an SM; Q <= 128
+    const int kh = kSplit ? q.kh : q.N;
+    async_rows(ct, q.crows, Cb + (int64_t)(t0 + i0) * bc_stride, bc_stride, c_valid, kh, tid);
+    async_rows(bt, q.KB, Bb + (int64_t)t0 * bc_stride, bc_stride, b_valid, kh, tid);
     cp_async_commit();
     for (int i = tid; i < q.Q; i += kThreads) {
         if (kGdn) {
@@ -429,7 +433,7 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     }
     // h^T: rows = p, K = state n (hiddens holds [n][p])
     const float* hb = hiddens + ((int64_t)bh * q.nc + c) * (int64_t)q.N * q.P + p0;
-    put_transposed(ht, pc, q.N, pc, [&](int n) { return hb + (int64_t)n * q.P; },
+    put_transposed(ht, pc, kh, pc, [&](int n) { return hb + (int64_t)n * q.P; },
                    [](int) { return 1.f; }, lane, warp);
     // (dt o X_J)^T: rows = p, K = keys of block J (zero past the sequence end)
     // (reads dv: the first call follows a barrier after dv is written; no
@@ -448,8 +452,8 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
         put_x(0);
     }
     cp_async_wait_all();
-    round_rows(ct, q.crows, q.N, tid);
-    round_rows(bt, q.KB, q.N, tid);
+    round_rows(ct, q.crows, kh, tid);
+    round_rows(bt, q.KB, kh, tid);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -458,7 +462,7 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     const uint32_t acc = tmem, sreg = tmem + q.scol;
     const uint32_t idesc_p = make_idesc(2, 128, (uint32_t)pc, 0, 0);
     const uint32_t idesc_k = make_idesc(2, 128, (uint32_t)q.KB, 0, 0);
-    const int nk_state = q.N / 8;
+    const int nk_state = kh / 8;
     if (tid == 0) {
         for (int kk = 0; kk < nk_state; ++kk)
             mma_tf32_ss(acc, kmajor_desc(ct, kk, q.crows), kmajor_desc(ht, kk, pc), idesc_p,
@@ -468,6 +472,35 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
                         kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(bar));
     }
+    uint32_t phase = 0;
+    bool ok = true;
+    if constexpr (kSplit) {
+        // the remaining passes: each reloads the three tiles once the products
+        // of the pass before have read them
+        for (int ks = 1; ks < q.nks; ++ks) {
+            const int n0 = ks * kh;
+            chain_wait(smem_u32(bar), phase, ok);
+            async_rows(ct, q.crows, Cb + (int64_t)(t0 + i0) * bc_stride + n0, bc_stride, c_valid, kh, tid);
+            async_rows(bt, q.KB, Bb + (int64_t)t0 * bc_stride + n0, bc_stride, b_valid, kh, tid);
+            cp_async_commit();
+            put_transposed(ht, pc, kh, pc, [&](int n) { return hb + (int64_t)(n0 + n) * q.P; },
+                           [](int) { return 1.f; }, lane, warp);
+            cp_async_wait_all();
+            round_rows(ct, q.crows, kh, tid);
+            round_rows(bt, q.KB, kh, tid);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (tid == 0 && ok) {
+                for (int kk = 0; kk < nk_state; ++kk)
+                    mma_tf32_ss(acc, kmajor_desc(ct, kk, q.crows), kmajor_desc(ht, kk, pc), idesc_p, 1u);
+                for (int kk = 0; kk < nk_state; ++kk)
+                    mma_tf32_ss(sreg, kmajor_desc(ct, kk, q.crows), kmajor_desc(bt, kk, q.KB), idesc_k, 1u);
+                mma_commit(smem_u32(bar));
+            }
+        }
+    }
 
     const int r = tid;                     // query row in the block <-> TMEM lane
     const int i = i0 + r;                  // query row in the chunk
@@ -475,8 +508,6 @@ compute_out_tf32(const float* __restrict__ x, const float* __restrict__ B,
     const float gi = row_ok ? gv[i] : 0.f;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const int nJ = q.Q > 128 ? I + 1 : 1;
-    uint32_t phase = 0;
-    bool ok = true;
     for (int J = 0; J < nJ; ++J) {
         chain_wait(smem_u32(bar), phase, ok);   // S = C_I B_J^T (and, for J = 0, acc = C_I h^T)
         tc_fence_after();
@@ -994,26 +1025,50 @@ int co_tf32_layout(CoTf32& q) {
     q.crows = q.Q < 128 ? q.Q : 128;
     q.scol = (uint32_t)((q.pt + 31) / 32 * 32);
     q.tmem_cols = tmem_cols_for((int)q.scol + q.KB);
-    q.c_bytes = up1024(tile_bytes(q.crows, q.N));
-    q.b_bytes = up1024(tile_bytes(q.KB, q.N));
-    const int h_own = up1024(tile_bytes(q.pt, q.N));
-    q.x_bytes = up1024(tile_bytes(q.pt, q.KB));
-    const int extras = 2 * q.Q * 4 + 64 + 1024;
-    const int sep = q.c_bytes + q.b_bytes + h_own + q.x_bytes + extras;
-    const int shared = q.c_bytes + q.b_bytes + std::max(h_own, q.x_bytes) + extras;
-    // a tile of its own for X unless sharing h^T's lets more CTAs onto an SM
     const int per_sm = 228 * 1024;
-    q.x_sep = sep <= 200 * 1024 && per_sm / (sep + 1024) >= per_sm / (shared + 1024);
-    q.h_bytes = q.x_sep ? h_own : std::max(h_own, q.x_bytes);
-    int smem = q.x_sep ? sep : shared;
-    // the M = 128 products read 128 rows of the C_I tile from each K atom's
-    // start: with fewer rows that runs past the tile, which must stay inside
-    // the allocation
-    const int c_read = ((q.N + 31) / 32 - 1) * q.crows * kRowBytes + 16 * 1024;
-    smem = std::max(smem, c_read + extras);
     const int by_tmem = 512 / (int)q.tmem_cols;
-    const int smem_cta = std::max(smem, per_sm / by_tmem - 1024);
-    return smem_cta > 227 * 1024 ? -1 : smem_cta;
+    const int extras = 2 * q.Q * 4 + 64 + 1024;
+    // The tiles for products over kh state columns per pass; returns the
+    // dynamic shared memory per CTA, or -1 if it does not fit.
+    auto fit = [&](CoTf32& o, int kh, bool allow_sep) {
+        o = q;
+        o.kh = kh;
+        o.nks = q.N / kh;
+        o.c_bytes = up1024(tile_bytes(o.crows, kh));
+        o.b_bytes = up1024(tile_bytes(o.KB, kh));
+        const int h_own = up1024(tile_bytes(o.pt, kh));
+        o.x_bytes = up1024(tile_bytes(o.pt, o.KB));
+        const int sep = o.c_bytes + o.b_bytes + h_own + o.x_bytes + extras;
+        const int shared = o.c_bytes + o.b_bytes + std::max(h_own, o.x_bytes) + extras;
+        // a tile of its own for X unless sharing h^T's lets more CTAs onto an SM
+        o.x_sep = allow_sep && sep <= 200 * 1024 && per_sm / (sep + 1024) >= per_sm / (shared + 1024);
+        o.h_bytes = o.x_sep ? h_own : std::max(h_own, o.x_bytes);
+        int smem = o.x_sep ? sep : shared;
+        // the M = 128 products read 128 rows of the C_I tile from each K atom's
+        // start: with fewer rows that runs past the tile, which must stay
+        // inside the allocation
+        const int c_read = ((kh + 31) / 32 - 1) * o.crows * kRowBytes + 16 * 1024;
+        smem = std::max(smem, c_read + extras);
+        const int smem_cta = std::max(smem, per_sm / by_tmem - 1024);
+        return smem_cta > 227 * 1024 ? -1 : smem_cta;
+    };
+    auto ctas = [&](int smem_cta) {
+        return smem_cta < 0 ? 0 : std::min(std::min(by_tmem, kCtasPerSm), per_sm / (smem_cta + 1024));
+    };
+    CoTf32 whole, split;
+    int smem_cta = fit(whole, q.N, true);
+    q = whole;
+    // two passes over a state of 128 (64 columns each, X sharing h^T's tile)
+    // when that lets more CTAs share an SM; the query blocks of a 256-token
+    // chunk reuse the whole C_I tile, so only for Q <= 128
+    if (q.N > 64 && q.N % 64 == 0 && q.nblk == 1) {
+        const int s2 = fit(split, 64, false);
+        if (ctas(s2) > ctas(smem_cta)) {
+            q = split;
+            smem_cta = s2;
+        }
+    }
+    return smem_cta;
 }
 }  // namespace
 
@@ -1025,10 +1080,10 @@ cudaError_t launch_compute_out_tf32(const Problem& p, const void* x, const void*
     q.Q = (int)p.Q; q.nc = (int)p.nc; q.Lp = (int)p.Lp; q.hpg = (int)p.hpg;
     const int smem_cta = co_tf32_layout(q);
     if (smem_cta < 0) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(compute_out_tf32<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
+    auto kern = q.nks > 1 ? compute_out_tf32<false, true> : compute_out_tf32<false, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
     if (e != cudaSuccess) return e;
-    return launch_chained(compute_out_tf32<false>,
+    return launch_chained(kern,
                           dim3((unsigned)(q.nblk * q.npt), (unsigned)p.nc, (unsigned)(p.b * p.H)),
                           dim3(kThreads), (size_t)smem_cta, stream, p.chained, (const float*)x,
                           (const float*)B, (const float*)C, Gcs, dtT, (const float*)hiddens, D,
@@ -1048,12 +1103,12 @@ cudaError_t launch_gdn_fwd_o_tf32(const GdnProblem& p, const float* qm, const fl
     q.Q = (int)p.C; q.nc = (int)p.NT; q.Lp = 0; q.hpg = 1;
     const int smem_cta = co_tf32_layout(q);
     if (smem_cta < 0) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(compute_out_tf32<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
+    auto kern = q.nks > 1 ? compute_out_tf32<true, true> : compute_out_tf32<true, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cta);
     if (e != cudaSuccess) return e;
     // operand roles: C <- q, B <- k, x <- v_new, hiddens <- h, y <- o, Gcs <- g
-    compute_out_tf32<true><<<dim3((unsigned)(q.nblk * q.npt), (unsigned)p.NT, (unsigned)(p.B * p.H)),
-                             kThreads, (size_t)smem_cta, stream>>>(
+    kern<<<dim3((unsigned)(q.nblk * q.npt), (unsigned)p.NT, (unsigned)(p.B * p.H)), kThreads,
+           (size_t)smem_cta, stream>>>(
         v_new, k, qm, g, nullptr, h, nullptr, o, q, host_timeout_word());
     return cudaGetLastError();
 }

@@ -81,6 +81,7 @@ CASES = [
     # fp32 on the TF32 tensor-core kernels
     ("f32", 256, 700, 4, 2, 64, 128, True, True),     # two query blocks per chunk, ragged
     ("f32", 128, 333, 2, 1, 128, 128, True, True),    # largest TF32 P and N
+    ("f32", 64, 450, 4, 2, 64, 128, True, True),      # C h^T, C B^T in two passes over N, Q = 64
     ("f32", 64, 300, 4, 4, 48, 48, False, True),      # P, N not multiples of 32
     ("bf16", 256, 511, 4, 1, 64, 128, False, True),   # ragged, Q = 256
     ("bf16", 256, 4096, 2, 1, 64, 128, True, True),
