@@ -489,6 +489,15 @@ GDN_METRIC = "Gated DeltaNet chunk_fwd_h + chunk_fwd_o tokens/s on 1 GB300 and %
 TF32_PER_BF16 = 1.1 / 2.25
 
 
+def gdn_bytes(B: int, T: int, H: int, K: int, V: int, C: int) -> int:
+    """Algorithmic bytes of one Gated DeltaNet step (fp32, each operand read once
+    and each result written once): chunk_fwd_h reads k, w [B,T,H,K], u [B,T,H,V],
+    g [B,T,H] and h0 [B,H,K,V] and writes h [B,H,NT,K,V], v_new [B,T,H,V] and the
+    final state; chunk_fwd_o reads q, k, v_new, h and g and writes o [B,T,H,V]."""
+    NT = -(-T // C)
+    return 4 * (B * T * H * (4 * K + 4 * V + 2) + B * H * K * V * (2 + 2 * NT))
+
+
 def tf32_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -579,12 +588,10 @@ def gdn_main(args):
     macs = B * H * NT * (2 * C * K * V + C * K * V + C * (C + 1) // 2 * (K + V))
     achieved = 2 * macs / (ms * 1e-3) / 1e12
     peak_tf, peak_kind_tf = tf32_peak()
-    # algorithmic bytes (fp32): chunk_fwd_h reads k, w, u, g and h0 and writes h,
-    # v_new and the final state; chunk_fwd_o reads q, k, v_new, h and g and writes o
-    gdn_bytes = 4 * (B * T * H * (4 * K + 4 * V + 2) + B * H * K * V * (2 + 2 * NT))
+    step_bytes = gdn_bytes(B, T, H, K, V, C)
     hbm, hbm_kind = measured_peaks()
-    bw = gdn_bytes / (ms * 1e-3) / 1e9
-    hbm_bound = gdn_bytes / (hbm * 1e9) >= 2 * macs / (peak_tf * 1e12)
+    bw = step_bytes / (ms * 1e-3) / 1e9
+    hbm_bound = step_bytes / (hbm * 1e9) >= 2 * macs / (peak_tf * 1e12)
     line = {
         "metric": GDN_METRIC, "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -601,7 +608,7 @@ def gdn_main(args):
               "peak": peak_tf, "peak_kind": peak_kind_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf}),
             # DRAM bytes of both launches of one step
             traffic=recorded_traffic("gdn", "gdn_chunk_f32"),
-            algorithmic_bytes=gdn_bytes, algorithmic_flops=2 * macs,
+            algorithmic_bytes=step_bytes, algorithmic_flops=2 * macs,
             tensor={"achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                     "frac": achieved / peak_tf, "peak_kind": peak_kind_tf}),
         "e2e": {"value": B * T / (e2e_ms * 1e-3), "unit": "tokens/s",
