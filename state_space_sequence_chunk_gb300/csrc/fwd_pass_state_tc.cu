@@ -266,8 +266,8 @@ fwd_pass_state_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             // a chain reads its x block once when the state is one block of N
-            // rows: its lines then go first, so the hiddens written here stay in
-            // L2 for compute_out (with two blocks the other chain reads it too)
+            // rows: its lines are then loaded evict-first, leaving the L2 to what
+            // is read again (with two blocks the other chain reads the same x)
             const bool x_once = q.nmb == 1;
             const uint64_t x_pol = x_once ? l2_policy_evict_first() : 0;
             int i = 0;   // stage counter
@@ -851,8 +851,8 @@ fwd_pass_state_pair_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            // x is read once here: its lines go first, so the hiddens written
-            // by this kernel stay in L2 for compute_out
+            // x is read once here: its lines are loaded evict-first, leaving the
+            // L2 to what is read again (the group's B tiles, the states written here)
             const uint64_t x_pol = l2_policy_evict_first();
             int i = 0, cv = 0;
             bool ok = true;

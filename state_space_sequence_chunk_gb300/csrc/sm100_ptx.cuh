@@ -203,9 +203,8 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
-// L2 eviction priority for data read or written once (a streaming operand or an
-// output): its lines are the first the L2 gives up, so that data still to be
-// reused (a state written here and read by the next kernel) stays resident.
+// L2 eviction priority for data read once (a streaming operand): its lines are
+// the first the L2 gives up, ahead of data that is still to be read again.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
